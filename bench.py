@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Benchmark of the CSA2 hot path on one B300 (one JSON line on stdout).
+
+Headline workload: hierarchical long-context decode, batch 1, context 1,048,576: a Full layer
+scans every index key and builds the 2,048-block candidate pool, three Reindex layers rescore the
+pool with their own FP8 indexer queries (Top-K 2048), two Reuse layers reuse the last indices;
+all six layers run FP4 sparse attention with 64 heads.  One step = the whole layer sequence plus
+the quantisation of the new token's KV row.  Metric: decode tokens/s, with the step's
+algorithmic HBM bytes/s against 8 TB/s, and (`prefill`) chunked-prefill TFLOP/s on 4,096 new
+tokens after a 262,144-token cached prefix.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-prefill]
+
+--impl reference times the CPU oracle (single-threaded C, the definition of the path) on the same
+workload and metric.  Multi-GPU: replicas only (every rank runs the full workload on its own GPU;
+`value` sums the ranks); this path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+HEADLINE = "hier_decode_l1m"
+PREFILL = "prefill_t4096_p262144"
+METRIC = "sparse-attn decode tokens/s + HBM GB/s vs 8 TB/s at 1M ctx; prefill TFLOP/s"
+HBM_TARGET_GBS = 8000.0
+ROOT = os.path.dirname(os.path.abspath(__file__))
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+def run_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    from fp4_kv_top_csa2_b300 import csa2, synth
+    from fp4_kv_top_csa2_b300.step import Step
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks = _peaks()
+    w = synth.WORKLOADS[HEADLINE]
+    inp = synth.make_inputs(w)
+    st = Step(inp, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > 126 MB L2
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    launches0 = csa2.kernel_launches()
+
+    # timed region: K steps, per-step events, L2 flushed between steps (outside the events)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            st.run()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier()
+    launches = csa2.kernel_launches() - launches0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    by = st.algorithmic_bytes()
+    tokens_per_s = world * w.B / (ms / 1e3)
+    step_gbs = by["total"] / (ms / 1e3) / 1e9
+
+    # breakdown by C-ABI call (same work, events between calls), for the dominant call's roofline
+    parts = profile_calls(st, args.steps, flush)
+    dom_name, dom_ms, dom_bytes = "csa2_index_score_topk (Full, 1,048,576 keys)", parts["full_index"], by["index_keys_full"]
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+
+    # end to end through the C ABI with host buffers
+    e2e = run_e2e(st, args.steps, dev)
+
+    line = {
+        "metric": METRIC, "value": round(tokens_per_s, 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp4-e2m1/e4m3 kv, fp8 indexer, bf16 attn (fp32 acc)",
+        "data": "synthetic (seeded N(0,1) x log-uniform channel scales; no weights)",
+        "config": {"workload": HEADLINE, "batch": w.B, "context": w.L[0], "heads": w.H,
+                   "d_latent": 512, "indexer": f"{w.Hi}x{w.Di} e4m3", "topk": w.topk,
+                   "pool": f"{w.n_pool_blocks}x8", "modes": list(w.modes),
+                   "l2": "flushed between timed steps (512 MB write)", "parallelism": "replicas"},
+        "hbm": {"algorithmic_bytes_per_step": by["total"], "gbs": round(step_gbs, 1),
+                "frac_of_8tbs": round(step_gbs / HBM_TARGET_GBS, 4),
+                "frac_of_measured": round(step_gbs / peaks["hbm_gbs"], 4), "bytes_by_part": by},
+        "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"] + " (burst copy)", "traffic": None,
+                     "ms_per_launch": round(dom_ms, 5), "algorithmic_bytes": dom_bytes},
+        "breakdown_ms": {k: round(v, 5) for k, v in parts.items()},
+        "e2e": e2e, "gpu_launches": launches, "wall_s_timed": round(wall, 4),
+        "clocks": clk.summary(),
+    }
+    if args.prefill and rank == 0:
+        line["prefill"] = run_prefill(args, dev, peaks)
+    if rank == 0 and args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, w, args.cpu_steps)
+    return line
+
+
+def profile_calls(st, steps, flush):
+    """Per-call CUDA-event times of the step (same calls as Step.run)."""
+    import torch
+    from fp4_kv_top_csa2_b300 import csa2
+    names = []
+    recs = []
+    stream = torch.cuda.current_stream()
+
+    def mark(name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        recs.append((name, e))
+
+    acc = {}
+    for _ in range(steps):
+        flush.zero_()
+        recs.clear()
+        mark("start")
+        st.quantize_new_rows()
+        mark("kv_quant")
+        last = None
+        for i, L in enumerate(st.layers):
+            if L["mode"] == "full":
+                st.index(L, block_max=st.bm)
+                mark("full_index")
+                csa2.csa2_hier_candidate_pool(st.bm, st.q_vis, st.w.n_pool_blocks, st.pool)
+                mark("pool")
+                last = L["idx"]
+            elif L["mode"] == "reindex":
+                st.index(L, cand=st.pool)
+                mark("reindex_index")
+                last = L["idx"]
+            st.attend(L, last)
+            mark("attention")
+        torch.cuda.synchronize()
+        for (n0, e0), (n1, e1) in zip(recs[:-1], recs[1:]):
+            acc.setdefault(n1, []).append(e0.elapsed_time(e1))
+    out = {}
+    for k, v in acc.items():  # average per call, and total per step
+        out[k] = sum(v) / len(v)
+        out[k + "_per_step"] = sum(v) / steps
+    return out
+
+
+def run_e2e(st, steps, dev):
+    """Same step through the C ABI, inputs copied from pinned host memory each step and the
+    attention outputs read back, all inside the timed region."""
+    import torch
+    host_in = {"new_x": st.new_x.cpu().pin_memory()}
+    for i, L in enumerate(st.layers):
+        host_in[f"q_attn{i}"] = L["q_attn"].cpu().pin_memory()
+        if "q_idx" in L:
+            host_in[f"q_idx{i}"] = L["q_idx"].cpu().pin_memory()
+            host_in[f"w{i}"] = L["w"].cpu().pin_memory()
+    host_out = [torch.empty_like(L["out"], device="cpu").pin_memory() for L in st.layers]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def one():
+        st.new_x.copy_(host_in["new_x"], non_blocking=True)
+        for i, L in enumerate(st.layers):
+            L["q_attn"].copy_(host_in[f"q_attn{i}"], non_blocking=True)
+            if "q_idx" in L:
+                L["q_idx"].copy_(host_in[f"q_idx{i}"], non_blocking=True)
+                L["w"].copy_(host_in[f"w{i}"], non_blocking=True)
+        st.run()
+        for i, L in enumerate(st.layers):
+            host_out[i].copy_(L["out"], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(st.w.B / dt, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 4)}
+
+
+def run_prefill(args, dev, peaks):
+    import torch
+    from fp4_kv_top_csa2_b300 import synth
+    from fp4_kv_top_csa2_b300.step import Step
+    w = synth.WORKLOADS[PREFILL]
+    inp = synth.make_inputs(w)
+    st = Step(inp, device=dev)
+    stream = torch.cuda.current_stream()
+    L = st.layers[0]
+    for _ in range(max(1, args.warmup // 2)):
+        st.run()
+    torch.cuda.synchronize()
+    ti, ta, tq = [], [], []
+    for _ in range(args.prefill_steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        st.quantize_new_rows()
+        e[1].record(stream)
+        st.index(L)
+        e[2].record(stream)
+        st.attend(L, L["idx"])
+        e[3].record(stream)
+        torch.cuda.synchronize()
+        tq.append(e[0].elapsed_time(e[1]))
+        ti.append(e[1].elapsed_time(e[2]))
+        ta.append(e[2].elapsed_time(e[3]))
+    P0 = w.L[0]
+    pairs = sum(P0 + i + 1 for i in range(w.T))
+    f_idx = 2.0 * pairs * w.Hi * w.Di
+    f_attn = 4.0 * w.T * w.topk * w.H * 512
+    mi, ma, mq = (statistics.median(x) for x in (ti, ta, tq))
+    return {"workload": PREFILL, "tokens": w.T, "cached": P0, "topk": w.topk, "heads": w.H,
+            "ms_indexer": round(mi, 4), "ms_attention": round(ma, 4), "ms_kv_quant": round(mq, 4),
+            "indexer_tflops": round(f_idx / (mi / 1e3) / 1e12, 2),
+            "attention_tflops": round(f_attn / (ma / 1e3) / 1e12, 2),
+            "tokens_per_s": round(w.T / ((mi + ma + mq) / 1e3), 1),
+            "flops_indexer": f_idx, "flops_attention": f_attn}
+
+
+# ------------------------------------------------------------------------------------------------
+# the oracle (CPU): reference arm and cpu_baseline
+# ------------------------------------------------------------------------------------------------
+def oracle_step(inp, w):
+    """One decode step of the headline workload, executed by the CPU oracle.  The oracle gathers
+    FP4 rows by quantising the selected bf16 rows on demand (bit-identical to the cache)."""
+    import numpy as np
+    import oracle
+    from fp4_kv_top_csa2_b300.synth import new_token_rows, to_numpy_bits
+    kv = inp["_np_kv"]
+    cu = inp["cu_ctx"].numpy()
+    k_idx = inp["_np_k"]
+    q_seq, q_vis = inp["q_seq"].numpy(), inp["q_vis"].numpy()
+    oracle.kv_quant_fp4(kv[new_token_rows(inp).numpy()])
+    pool = None
+    last = None
+    scale = 1.0 / np.sqrt(512)
+    for L in inp["layers"]:
+        if L["mode"] == "full":
+            r = oracle.index_score_topk(to_numpy_bits(L["q_idx"]), w.idx_dtype, L["w"].numpy(),
+                                        k_idx, cu, q_seq, q_vis, w.topk)
+            last = np.stack([r[n]["idx"] for n in range(len(q_seq))])
+            if w.kind == "hier" and pool is None:
+                pool = np.stack([oracle.candidate_pool(r[n]["bm"], w.n_pool_blocks)
+                                 for n in range(len(q_seq))])
+        elif L["mode"] == "reindex":
+            r = oracle.index_score_topk(to_numpy_bits(L["q_idx"]), w.idx_dtype, L["w"].numpy(),
+                                        k_idx, cu, q_seq, q_vis, w.topk, cand_blocks=pool)
+            last = np.stack([r[n]["idx"] for n in range(len(q_seq))])
+        qa = to_numpy_bits(L["q_attn"])
+        for b in range(len(q_seq)):
+            sel = last[b][last[b] >= 0]
+            rows = kv[cu[b] + sel]
+            c, s = oracle.kv_quant_fp4(rows)
+            oracle.sparse_attn(oracle.bf16_to_double(qa[b]), c, s, np.arange(len(sel), dtype=np.int32),
+                               scale)
+
+
+def cpu_baseline(inp, w, steps):
+    from fp4_kv_top_csa2_b300.synth import to_numpy_bits
+    inp["_np_kv"] = to_numpy_bits(inp["kv_bf16"])
+    inp["_np_k"] = to_numpy_bits(inp["k_idx"])
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(inp, w)
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(w.B / dt, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{steps} full decode step(s) of {HEADLINE} on 1 host core "
+                      f"(of {os.cpu_count()}), {dt:.2f} s/step"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from fp4_kv_top_csa2_b300 import synth
+    from fp4_kv_top_csa2_b300.synth import to_numpy_bits
+    w = synth.WORKLOADS[HEADLINE]
+    inp = synth.make_inputs(w)
+    inp["_np_kv"] = to_numpy_bits(inp["kv_bf16"])
+    inp["_np_k"] = to_numpy_bits(inp["k_idx"])
+    for _ in range(args.warmup):
+        oracle_step(inp, w)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(inp, w)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = round(w.B / dt, 4)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": HEADLINE, "batch": w.B, "context": w.L[0], "heads": w.H,
+                       "topk": w.topk, "pool": f"{w.n_pool_blocks}x8", "modes": list(w.modes)},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} full decode steps of {HEADLINE}, 1 core"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false")
+    ap.add_argument("--prefill-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-steps", type=int, default=2)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    sys.path.insert(0, ROOT)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,280 @@
+// api.cu -- the extern "C" entry points declared in include/csa2.h: host-side validation,
+// workspace carving and kernel launches.  Nothing here allocates device memory.
+#include <atomic>
+
+#include "common.cuh"
+
+using namespace csa2;
+
+namespace {
+
+constexpr size_t kWsAlign = 256;
+
+size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Per-device "is sm_103" cache: 0 unknown, 1 yes, 2 no.  Idempotent writes, so a benign race.
+std::atomic<int> g_arch_ok[64];
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return CSA2_ERR_UNSUPPORTED;
+  int st = g_arch_ok[dev].load(std::memory_order_relaxed);
+  if (st == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return CSA2_ERR_CUDA;
+    st = (major == 10 && minor == 3) ? 1 : 2;
+    g_arch_ok[dev].store(st, std::memory_order_relaxed);
+  }
+  return st == 1 ? CSA2_OK : CSA2_ERR_UNSUPPORTED;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+
+struct WsCursor {
+  char *p;
+  size_t used = 0;
+  explicit WsCursor(void *base) : p(static_cast<char *>(base)) {}
+  template <class T>
+  T *take(size_t count) {
+    T *r = p ? reinterpret_cast<T *>(p + used) : nullptr;
+    used += align_up(count * sizeof(T));
+    return r;
+  }
+};
+
+// Workspace layout of csa2_index_score_topk (also used to size it).
+struct ScoreWs {
+  float *bm = nullptr;
+  int32_t *blocks = nullptr;
+  float *scores = nullptr;
+  size_t bytes = 0;
+  int64_t nb_max = 0;
+  int kb = 0;
+};
+
+ScoreWs score_ws(void *base, int nq, int64_t max_vis, int n_cand_blocks, int topk) {
+  ScoreWs w;
+  WsCursor c(base);
+  if (n_cand_blocks > 0) {
+    w.scores = c.take<float>((size_t)nq * n_cand_blocks * kBlock);
+  } else {
+    w.nb_max = (max_vis + kBlock - 1) / kBlock;
+    w.kb = (int)std::min<int64_t>(topk, w.nb_max);
+    w.bm = c.take<float>((size_t)nq * w.nb_max);
+    w.blocks = c.take<int32_t>((size_t)nq * w.kb);
+    w.scores = c.take<float>((size_t)nq * w.kb * kBlock);
+  }
+  w.bytes = c.used;
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *csa2_error_string(int status) {
+  switch (status) {
+    case CSA2_OK: return "CSA2_OK";
+    case CSA2_ERR_INVALID_ARG: return "CSA2_ERR_INVALID_ARG: invalid argument";
+    case CSA2_ERR_UNSUPPORTED: return "CSA2_ERR_UNSUPPORTED: device is not sm_103";
+    case CSA2_ERR_CUDA: return "CSA2_ERR_CUDA: CUDA runtime or launch failure";
+    case CSA2_ERR_WORKSPACE: return "CSA2_ERR_WORKSPACE: workspace too small";
+    case CSA2_ERR_TIMEOUT: return "CSA2_ERR_TIMEOUT: bounded device wait expired";
+    default: return "unknown CSA2 status";
+  }
+}
+
+int csa2_kv_quant_fp4(const void *x_bf16, int64_t n_rows, int d, const int64_t *out_rows,
+                      uint8_t *codes, uint8_t *sf, void *stream) {
+  if (n_rows < 0 || d < 32 || d > 4096 || d % 32 != 0) return CSA2_ERR_INVALID_ARG;
+  if (n_rows == 0) return CSA2_OK;
+  if (!x_bf16 || !codes || !sf) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(codes) || !aligned16(sf) || !aligned16(out_rows))
+    return CSA2_ERR_INVALID_ARG;
+  if (int r = check_device()) return r;
+  return cuda_status(launch_kv_quant(x_bf16, n_rows, d, out_rows, codes, sf,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+size_t csa2_index_score_topk_workspace_size(int nq, int64_t max_vis, int n_cand_blocks,
+                                            int topk) {
+  if (nq < 0 || max_vis < 0 || n_cand_blocks < 0 || topk < 1) return 0;
+  return score_ws(nullptr, nq, max_vis, n_cand_blocks, topk).bytes;
+}
+
+int csa2_index_score_topk(const void *q_idx, int q_dtype, const float *w, int nq, int Hi, int Di,
+                          const void *k_idx, int k_dtype, const float *k_scale,
+                          const int64_t *cu_ctx, int B, const int32_t *q_seq,
+                          const int32_t *q_vis, int64_t max_vis, const int32_t *cand_blocks,
+                          int n_cand_blocks, int topk, int32_t *out_idx, float *out_block_max,
+                          void *workspace, size_t ws_bytes, void *stream) {
+  if (nq < 0 || nq > 65535 || B < 1 || Hi < 1 || Hi > 16 || topk < 1 || topk > 4096 ||
+      max_vis < 0 || max_vis > (int64_t)1 << 30)
+    return CSA2_ERR_INVALID_ARG;
+  if (q_dtype != k_dtype) return CSA2_ERR_INVALID_ARG;
+  if (!((q_dtype == CSA2_BF16 && Di == 64) || (q_dtype == CSA2_E4M3 && Di == 128)))
+    return CSA2_ERR_INVALID_ARG;
+  if (cand_blocks ? (n_cand_blocks < 1 || n_cand_blocks > 65536 || out_block_max)
+                  : (n_cand_blocks != 0))
+    return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  if (!q_idx || !w || !k_idx || !cu_ctx || !q_seq || !q_vis || !out_idx)
+    return CSA2_ERR_INVALID_ARG;
+  const void *ptrs[] = {q_idx, w, k_idx, k_scale, cu_ctx, q_seq, q_vis,
+                        cand_blocks, out_idx, out_block_max};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return CSA2_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) return CSA2_ERR_INVALID_ARG;
+  ScoreWs need = score_ws(nullptr, nq, max_vis, n_cand_blocks, topk);
+  if (ws_bytes < need.bytes || (need.bytes && !workspace)) return CSA2_ERR_WORKSPACE;
+  if (int r = check_device()) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ScoreWs ws = score_ws(workspace, nq, max_vis, n_cand_blocks, topk);
+  cudaError_t e;
+  if (cand_blocks) {  // Reindex: score the listed blocks, select
+    e = launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
+                          cand_blocks, n_cand_blocks, ws.scores, st);
+    if (e == cudaSuccess)
+      e = launch_topk(ws.scores, (int64_t)n_cand_blocks * kBlock, (int64_t)n_cand_blocks * kBlock,
+                      cand_blocks, n_cand_blocks, 1, q_vis, nq, topk, out_idx, st);
+    return cuda_status(e);
+  }
+  // Full: block maxima over every visible position; the Top-K positions lie inside the Top-K
+  // blocks by block maximum (each block ahead of a selected position's block holds a position
+  // ranked ahead of it), so select those blocks first, then rescore and select their positions.
+  float *bm = out_block_max ? out_block_max : ws.bm;
+  e = launch_score_scan(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
+                        max_vis, bm, ws.nb_max, st);
+  if (e == cudaSuccess)
+    e = launch_topk(bm, ws.nb_max, ws.nb_max, nullptr, 0, kBlock, q_vis, nq, ws.kb, ws.blocks, st);
+  if (e == cudaSuccess)
+    e = launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
+                          ws.blocks, ws.kb, ws.scores, st);
+  if (e == cudaSuccess)
+    e = launch_topk(ws.scores, (int64_t)ws.kb * kBlock, (int64_t)ws.kb * kBlock, ws.blocks,
+                    ws.kb, 1, q_vis, nq, topk, out_idx, st);
+  return cuda_status(e);
+}
+
+size_t csa2_hier_candidate_pool_workspace_size(int nq, int64_t max_blocks, int n_pool_blocks) {
+  (void)nq; (void)max_blocks; (void)n_pool_blocks;
+  return 0;
+}
+
+int csa2_hier_candidate_pool(const float *block_max, int nq, const int32_t *q_vis,
+                             int64_t max_blocks, int block_size, int n_pool_blocks,
+                             int32_t *out_pool_blocks, void *workspace, size_t ws_bytes,
+                             void *stream) {
+  (void)workspace; (void)ws_bytes;
+  if (nq < 0 || nq > 65535 || max_blocks < 0 || max_blocks > (int64_t)1 << 27 ||
+      block_size != kBlock || n_pool_blocks < 1 || n_pool_blocks > 4096)
+    return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  if (!block_max || !q_vis || !out_pool_blocks) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(block_max) || !aligned16(q_vis) || !aligned16(out_pool_blocks))
+    return CSA2_ERR_INVALID_ARG;
+  if (int r = check_device()) return r;
+  return cuda_status(launch_topk(block_max, max_blocks, max_blocks, nullptr, 0, block_size, q_vis,
+                                 nq, n_pool_blocks, out_pool_blocks,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+size_t csa2_sparse_attn_decode_workspace_size(int B, int H, int topk) {
+  if (B < 0 || H < 1 || topk < 1) return 0;
+  return align_up(attn_workspace_bytes(B, H, topk));
+}
+
+static int attn_args_ok(int nq, int H, const uint8_t *codes, const uint8_t *sf,
+                        const int64_t *cu_ctx, const int32_t *idx, int topk, float scale,
+                        const void *q, const void *out, const float *lse, const void *ws) {
+  if (nq < 0 || nq > 65535 || H < 1 || H > 128 || topk < 1 || topk > 16384 || !(scale > 0.0f))
+    return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  if (!q || !codes || !sf || !cu_ctx || !idx || !out) return CSA2_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, codes, sf, cu_ctx, idx, out, lse};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return CSA2_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) % kWsAlign) return CSA2_ERR_INVALID_ARG;
+  return CSA2_OK;
+}
+
+int csa2_sparse_attn_decode(const void *q_bf16, int B, int H, const uint8_t *codes,
+                            const uint8_t *sf, const int64_t *cu_ctx, const int32_t *idx, int topk,
+                            float softmax_scale, void *out_bf16, float *lse, void *workspace,
+                            size_t ws_bytes, void *stream) {
+  if (int r = attn_args_ok(B, H, codes, sf, cu_ctx, idx, topk, softmax_scale, q_bf16, out_bf16,
+                           lse, workspace))
+    return r;
+  if (B == 0) return CSA2_OK;
+  const size_t need = csa2_sparse_attn_decode_workspace_size(B, H, topk);
+  if (ws_bytes < need || (need && !workspace)) return CSA2_ERR_WORKSPACE;
+  if (int r = check_device()) return r;
+  return cuda_status(launch_attn(q_bf16, nullptr, nullptr, B, H, nullptr, codes, sf, cu_ctx, idx,
+                                 topk, softmax_scale, out_bf16, lse, workspace,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+size_t csa2_sparse_attn_prefill_workspace_size(int T, int H, int topk) {
+  if (T < 0 || H < 1 || topk < 1) return 0;
+  const size_t rows = (size_t)T * H;
+  return align_up(rows * kCodeBytes) + align_up(rows * kSfBytes) +
+         align_up(attn_workspace_bytes(T, H, topk));
+}
+
+int csa2_sparse_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_seq,
+                             const uint8_t *codes, const uint8_t *sf, const int64_t *cu_ctx,
+                             int B, const int32_t *idx, int topk, float softmax_scale,
+                             void *out_bf16, float *lse, void *workspace, size_t ws_bytes,
+                             void *stream) {
+  if (int r = attn_args_ok(T, H, codes, sf, cu_ctx, idx, topk, softmax_scale, q_bf16, out_bf16,
+                           lse, workspace))
+    return r;
+  if (B < 1) return CSA2_ERR_INVALID_ARG;
+  if (T == 0) return CSA2_OK;
+  if (!q_seq || !aligned16(q_seq)) return CSA2_ERR_INVALID_ARG;
+  const size_t need = csa2_sparse_attn_prefill_workspace_size(T, H, topk);
+  if (ws_bytes < need || !workspace) return CSA2_ERR_WORKSPACE;
+  if (int r = check_device()) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsCursor c(workspace);
+  const size_t rows = (size_t)T * H;
+  uint8_t *q_codes = c.take<uint8_t>(rows * kCodeBytes);
+  uint8_t *q_sf = c.take<uint8_t>(rows * kSfBytes);
+  void *attn_ws = c.take<char>(attn_workspace_bytes(T, H, topk));
+  // the query is quantised per (token, head) row with the main-KV FP4 rule
+  cudaError_t e = launch_kv_quant(q_bf16, (int64_t)rows, kD, nullptr, q_codes, q_sf, st);
+  if (e == cudaSuccess)
+    e = launch_attn(nullptr, q_codes, q_sf, T, H, q_seq, codes, sf, cu_ctx, idx, topk,
+                    softmax_scale, out_bf16, lse, attn_ws, st);
+  return cuda_status(e);
+}
+
+int csa2_device_status(int *status, int reset, void *stream) {
+  if (!status) return CSA2_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_csa2_status, sizeof(int), 0, cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return CSA2_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return CSA2_ERR_CUDA;
+  *status = v;
+  if (reset) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_csa2_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                                st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return CSA2_ERR_CUDA;
+  }
+  return CSA2_OK;
+}
+
+uint64_t csa2_kernel_launches(void) {
+  return g_kernel_launches.load(std::memory_order_relaxed);
+}
+
+}  // extern "C"

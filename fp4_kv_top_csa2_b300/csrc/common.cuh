@@ -1,0 +1,131 @@
+// common.cuh -- shared device helpers of the CSA2 CUDA library (sm_103a only).
+#pragma once
+
+#include <atomic>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "csa2.h"
+
+namespace csa2 {
+
+constexpr int kD = CSA2_D;              // latent width of a main-KV row
+constexpr int kCodeBytes = kD / 2;      // 256 bytes of E2M1 codes per row
+constexpr int kSfBytes = kD / 16;       // 32 E4M3 scales per row
+constexpr int kBlock = 8;               // positions per indexer block (pool granularity)
+
+// ------------------------------------------------------------------------------------------
+// Number formats, device side.  Written independently of any CPU code: bit placement, not
+// tables or search.
+// ------------------------------------------------------------------------------------------
+
+// E4M3 ("fn") byte -> float, exact.  Normal: sign | (e + 120) << 23 | m << 20; subnormal m * 2^-9.
+__device__ __forceinline__ float e4m3_to_float(uint32_t b) {
+  uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  float mag = (e == 0) ? (float)m * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+  return (b & 0x80u) ? -mag : mag;
+}
+
+// E2M1 code (low nibble) -> float magnitude with sign, exact.
+__device__ __forceinline__ float e2m1_to_float(uint32_t c) {
+  // magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} as exponent/mantissa placement:
+  // e = (c>>1)&3, m = c&1; e == 0 -> 0.5*m; else (1 + m/2) * 2^(e-1)
+  uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  float mag = (e == 0) ? 0.5f * (float)m : __uint_as_float(((e + 126u) << 23) | (m << 22));
+  return (c & 8u) ? -mag : mag;
+}
+
+// float >= 0 -> E4M3 code, round to nearest even, saturating at 448 (0x7E).
+__device__ __forceinline__ uint32_t float_to_e4m3_sat(float s) {
+  if (!(s < 448.0f)) return 0x7Eu;  // also catches +inf
+  if (s < 0x1p-6f) {                 // subnormal range: quantum 2^-9
+    return (uint32_t)__float2int_rn(s * 512.0f);  // 8 -> code 8 == 2^-6, continuous
+  }
+  uint32_t u = __float_as_uint(s);
+  uint32_t exp = u >> 23, man = u & 0x7FFFFFu;
+  uint32_t r = man >> 20, rem = man & 0xFFFFFu;
+  uint32_t up = (rem > 0x80000u) || (rem == 0x80000u && (r & 1u));
+  // (exp - 127 + 7) << 3 | r, plus the rounding carry into the exponent field
+  return (((exp - 120u) << 3) | r) + up;
+}
+
+// |q| -> E2M1 magnitude code, round to nearest even, saturating at 6.  Decision points are the
+// midpoints between neighbours; at a midpoint the even code (mantissa bit 0) wins, which is why
+// some comparisons are strict and some are not.
+__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
+  return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+         (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+         (uint32_t)(a > 5.0f);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Order-preserving map of a finite float to uint32 (larger float -> larger key), with -0 == +0.
+// Finite floats map to [0x00800000, 0xFF7FFFFF]; key 0 never comes from a finite float.
+__device__ __forceinline__ uint32_t float_key(float v) {
+  uint32_t u = (v == 0.0f) ? 0u : __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Per-device status word written by bounded device-side waits that ran out.  The library is
+// built as one translation unit (csa2_lib.cu), so this is its single definition.
+__device__ int g_csa2_status = 0;
+
+}  // namespace csa2
+
+// ------------------------------------------------------------------------------------------
+// Host-side launchers (defined in the kernel files, called from api.cu).  All return
+// cudaError_t of the launch.
+// ------------------------------------------------------------------------------------------
+namespace csa2 {
+
+// Process-wide count of kernels enqueued by the library (csa2_kernel_launches).
+inline std::atomic<uint64_t> g_kernel_launches{0};
+inline void note_launches(int n) { g_kernel_launches.fetch_add(n, std::memory_order_relaxed); }
+
+cudaError_t launch_kv_quant(const void *x, int64_t n_rows, int d, const int64_t *out_rows,
+                            uint8_t *codes, uint8_t *sf, cudaStream_t st);
+
+// Full-mode scan: block maxima of the score for every visible position of every query.
+cudaError_t launch_score_scan(const void *q_idx, int dtype, const float *w, int nq, int Hi,
+                              int Di, const void *k_idx, const float *k_scale,
+                              const int64_t *cu_ctx, const int32_t *q_seq, const int32_t *q_vis,
+                              int64_t max_vis, float *bm, int64_t bm_stride, cudaStream_t st);
+
+// Candidate scoring: scores of the positions of n_cand_blocks listed blocks per query.
+cudaError_t launch_score_cand(const void *q_idx, int dtype, const float *w, int nq, int Hi,
+                              int Di, const void *k_idx, const float *k_scale,
+                              const int64_t *cu_ctx, const int32_t *q_seq, const int32_t *q_vis,
+                              const int32_t *cand_blocks, int n_cand_blocks, float *scores,
+                              cudaStream_t st);
+
+// Top-K selection.  Element i of query n lives at vals[n*stride + i], i < n_elems.
+//   map == nullptr: element i is block/position i, valid iff i < ceil(q_vis[n] / unit)
+//                   (unit = 8 for block maxima, 1 for positions);
+//   map != nullptr: element i is position map[n*map_stride + i/8]*8 + i%8, valid iff the block
+//                   id is >= 0 and the position is < q_vis[n].
+cudaError_t launch_topk(const float *vals, int64_t stride, int64_t n_elems, const int32_t *map,
+                        int64_t map_stride, int unit, const int32_t *q_vis, int nq, int topk,
+                        int32_t *out, cudaStream_t st);
+
+cudaError_t launch_attn(const void *q_bf16, const uint8_t *q_codes, const uint8_t *q_sf, int nq,
+                        int H, const int32_t *q_seq, const uint8_t *codes, const uint8_t *sf,
+                        const int64_t *cu_ctx, const int32_t *idx, int topk, float scale,
+                        void *out_bf16, float *lse, void *workspace, cudaStream_t st);
+size_t attn_workspace_bytes(int nq, int H, int topk);
+
+}  // namespace csa2

@@ -1,0 +1,7 @@
+// csa2_lib.cu -- the whole CSA2 CUDA library as one translation unit (one device module, so the
+// kernels share the device status word and the compiler sees every call).
+#include "kv_quant.cu"
+#include "index_score.cu"
+#include "topk.cu"
+#include "attn_simt.cu"
+#include "api.cu"

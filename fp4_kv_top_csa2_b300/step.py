@@ -1,0 +1,132 @@
+"""The CSA2 decode and prefill steps as sequences of C-ABI calls.
+
+Decode (one token per sequence; every layer of the workload's mode list, in order):
+  * the new token's latent row is quantised into the FP4 cache;
+  * Full layer: indexer scan + Top-K (and, in the hierarchical decoder, the block maxima that
+    build the candidate pool: 2,048 blocks of 8 positions, "DeepSeek V4.1-Flash", aiwiki.ai,
+    section "Compressed Sparse Attention 2"), then sparse attention;
+  * Reindex layer: its own index query/weights over the pool, Top-K, sparse attention;
+  * Reuse layer: sparse attention with the most recent layer's indices.
+Prefill: the T new rows are quantised into the cache, the indexer selects Top-K per query token
+(query i sees positions [0, P0 + i]), then sparse prefill attention.
+
+All device buffers (cache, queries, outputs, workspaces) are allocated once here with torch
+(caller-side allocation); `run()` only enqueues C-ABI calls on the current stream.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import csa2
+from .synth import BLOCK, D, new_token_rows
+
+
+class Step:
+    def __init__(self, inputs: dict, device="cuda", build_cache=True):
+        self.inp = inputs
+        self.w = w = inputs["workload"]
+        self.dev = device
+        dev = device
+        self.scale = 1.0 / math.sqrt(D)
+        self.kv_bf16 = inputs["kv_bf16"].to(dev)
+        rows = self.kv_bf16.shape[0]
+        self.codes = torch.empty((rows, D // 2), dtype=torch.uint8, device=dev)
+        self.sf = torch.empty((rows, D // 16), dtype=torch.uint8, device=dev)
+        self.k_idx = inputs["k_idx"].to(dev)
+        self.cu_ctx = inputs["cu_ctx"].to(dev)
+        self.q_seq = inputs["q_seq"].to(dev)
+        self.q_vis = inputs["q_vis"].to(dev)
+        self.max_vis = inputs["max_vis"]
+        self.nq = inputs["q_seq"].numel()
+        self.new_rows = new_token_rows(inputs).to(dev)
+        self.new_x = self.kv_bf16[self.new_rows].contiguous()
+        if build_cache:  # the cache as it stands before the step (all rows), quantised on the GPU
+            csa2.csa2_kv_quant_fp4(self.kv_bf16, self.codes, self.sf)
+        self.layers = []
+        nb = (self.max_vis + BLOCK - 1) // BLOCK
+        hier = w.kind == "hier"
+        for L in inputs["layers"]:
+            d = {"mode": L["mode"], "q_attn": L["q_attn"].to(dev)}
+            if "q_idx" in L:
+                d["q_idx"] = L["q_idx"].to(dev)
+                d["w"] = L["w"].to(dev)
+                d["idx"] = torch.empty((self.nq, w.topk), dtype=torch.int32, device=dev)
+            d["out"] = torch.empty((self.nq, w.H, D), dtype=torch.bfloat16, device=dev)
+            d["lse"] = torch.empty((self.nq, w.H), dtype=torch.float32, device=dev)
+            self.layers.append(d)
+        self.bm = torch.empty((self.nq, nb), dtype=torch.float32, device=dev) if hier else None
+        self.pool = (torch.empty((self.nq, w.n_pool_blocks), dtype=torch.int32, device=dev)
+                     if hier else None)
+        ws = csa2.csa2_index_score_topk_workspace_size(self.nq, self.max_vis, 0, w.topk)
+        if hier:
+            ws = max(ws, csa2.csa2_index_score_topk_workspace_size(self.nq, self.max_vis,
+                                                                   w.n_pool_blocks, w.topk))
+        self.ws_index = csa2.workspace(ws, dev)
+        if w.kind == "prefill":
+            self.ws_attn = csa2.workspace(
+                csa2.csa2_sparse_attn_prefill_workspace_size(self.nq, w.H, w.topk), dev)
+        else:
+            self.ws_attn = csa2.workspace(
+                csa2.csa2_sparse_attn_decode_workspace_size(self.nq, w.H, w.topk), dev)
+
+    # ------------------------------------------------------------------------------------------
+    def quantize_new_rows(self, stream=None):
+        csa2.csa2_kv_quant_fp4(self.new_x, self.codes, self.sf, out_rows=self.new_rows,
+                               stream=stream)
+
+    def index(self, layer, cand=None, block_max=None, stream=None):
+        csa2.csa2_index_score_topk(
+            layer["q_idx"], self.w.idx_dtype, layer["w"], self.k_idx, self.cu_ctx, self.q_seq,
+            self.q_vis, self.max_vis, self.w.topk, layer["idx"], cand_blocks=cand,
+            out_block_max=block_max, ws=self.ws_index, stream=stream)
+
+    def attend(self, layer, idx, stream=None):
+        if self.w.kind == "prefill":
+            csa2.csa2_sparse_attn_prefill(layer["q_attn"], self.q_seq, self.codes, self.sf,
+                                          self.cu_ctx, idx, self.scale, layer["out"],
+                                          layer["lse"], ws=self.ws_attn, stream=stream)
+        else:
+            csa2.csa2_sparse_attn_decode(layer["q_attn"], self.codes, self.sf, self.cu_ctx, idx,
+                                         self.scale, layer["out"], layer["lse"],
+                                         ws=self.ws_attn, stream=stream)
+
+    def run(self, stream=None):
+        """One step: quantise the new rows, then every layer in order."""
+        self.quantize_new_rows(stream)
+        last_idx = None
+        for i, L in enumerate(self.layers):
+            if L["mode"] == "full":
+                first_full = self.pool is not None and all(
+                    M["mode"] != "full" for M in self.layers[:i])
+                self.index(L, block_max=self.bm if first_full else None, stream=stream)
+                if first_full:
+                    csa2.csa2_hier_candidate_pool(self.bm, self.q_vis, self.w.n_pool_blocks,
+                                                  self.pool, stream=stream)
+                last_idx = L["idx"]
+            elif L["mode"] == "reindex":
+                self.index(L, cand=self.pool, stream=stream)
+                last_idx = L["idx"]
+            self.attend(L, last_idx, stream=stream)
+
+    # ------------------------------------------------------------------------------------------
+    def algorithmic_bytes(self) -> dict:
+        """Bytes the step must move at least once (HBM), by part."""
+        w = self.w
+        key_row = 128
+        vis_total = int(self.inp["q_vis"].to(torch.int64).sum())
+        n_full = sum(1 for L in self.layers if L["mode"] == "full")
+        n_re = sum(1 for L in self.layers if L["mode"] == "reindex")
+        n_att = len(self.layers)
+        row = D // 2 + D // 16
+        by = {
+            "new_rows": self.new_x.numel() * 2 + self.new_rows.numel() * row,
+            "index_keys_full": n_full * vis_total * key_row if w.kind != "prefill"
+            else int(self.inp["cu_ctx"][-1]) * key_row,
+            "index_keys_reindex": n_re * self.nq * w.n_pool_blocks * BLOCK * key_row,
+            "gathered_rows": n_att * self.nq * w.topk * row,
+            "q_out": n_att * self.nq * w.H * D * 2 * 2,
+        }
+        by["total"] = sum(by.values())
+        return by

@@ -204,6 +204,12 @@ int csa2_sparse_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_
  */
 int csa2_device_status(int *status, int reset, void *stream);
 
+/*
+ * Number of kernels this library has enqueued in this process since it was loaded (all devices
+ * and streams; calls that only validate or enqueue nothing add 0).  For launch accounting.
+ */
+uint64_t csa2_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,251 @@
+"""GPU-vs-oracle parity of each C-ABI call on small inputs that still span several tiles and a
+ragged tail, plus the degenerate cases (empty inputs, fewer candidates than K, empty slots)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import check_attn, check_topk
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def csa2():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from fp4_kv_top_csa2_b300 import csa2 as c
+    return c
+
+
+def _bits(t):
+    return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _kv(n, seed):
+    g = torch.Generator().manual_seed(seed)
+    sigma = 10.0 ** (torch.rand(512, generator=g) * 2 - 1)
+    return (torch.randn(n, 512, generator=g) * sigma).to(torch.bfloat16)
+
+
+# ------------------------------------------------------------------------------------------------
+# FP4 quantisation: bit-exact
+# ------------------------------------------------------------------------------------------------
+def _edge_rows():
+    rows = []
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    for k in range(-12, 12, 3):  # every E2M1 midpoint at scale 2^k (amax = 6 * 2^k)
+        for sign in (1, -1):
+            r = np.zeros(512)
+            for g in range(32):
+                v = np.array(mids + [6.0] + mids[::-1] + [0.0]) * 2.0 ** k * sign
+                r[16 * g:16 * g + 16] = np.roll(v, g)
+            rows.append(r)
+    tiny = np.zeros(512)
+    tiny[::16] = 2.0 ** -11
+    tiny[1::16] = -(2.0 ** -20)
+    rows.append(tiny)
+    sub = np.zeros(512)
+    for g in range(32):  # scales across the E4M3 subnormal range
+        sub[16 * g:16 * g + 16] = np.linspace(-1, 1, 16) * 6 * 2.0 ** (-14 + g / 4)
+    rows.append(sub)
+    big = np.zeros(512)
+    big[::2] = 3.0e38
+    big[1::2] = -1e30
+    rows.append(big)
+    z = np.zeros(512)
+    z[::3] = -0.0
+    rows.append(z)
+    return torch.tensor(np.array(rows), dtype=torch.float32).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("n", [1, 7, 1000])
+def test_kv_quant_bit_exact(csa2, n):
+    x = torch.cat([_kv(n, n), _edge_rows()])
+    codes = torch.empty((x.shape[0], 256), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((x.shape[0], 32), dtype=torch.uint8, device="cuda")
+    csa2.csa2_kv_quant_fp4(x.cuda(), codes, sf)
+    rc, rs = oracle.kv_quant_fp4(_bits(x))
+    assert np.array_equal(sf.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+def test_kv_quant_scattered_rows_and_empty(csa2):
+    x = _kv(37, 2)
+    out_rows = torch.randperm(100, generator=torch.Generator().manual_seed(0))[:37]
+    codes = torch.zeros((100, 256), dtype=torch.uint8, device="cuda")
+    sf = torch.zeros((100, 32), dtype=torch.uint8, device="cuda")
+    csa2.csa2_kv_quant_fp4(x.cuda(), codes, sf, out_rows=out_rows.cuda())
+    rc, rs = oracle.kv_quant_fp4(_bits(x))
+    c, s = codes.cpu().numpy(), sf.cpu().numpy()
+    assert np.array_equal(c[out_rows.numpy()], rc) and np.array_equal(s[out_rows.numpy()], rs)
+    untouched = np.setdiff1d(np.arange(100), out_rows.numpy())
+    assert not c[untouched].any() and not s[untouched].any()
+    csa2.csa2_kv_quant_fp4(x[:0].cuda(), codes, sf)  # n_rows = 0 is a no-op
+
+
+# ------------------------------------------------------------------------------------------------
+# Indexer score + Top-K, pool
+# ------------------------------------------------------------------------------------------------
+def _index_case(lengths, dtype, Hi, seed, dup=0.0):
+    g = torch.Generator().manual_seed(seed)
+    Di = 64 if dtype == 0 else 128
+    n = sum(lengths)
+    kf = torch.randn(n, Di, generator=g)
+    if dup:
+        m = int(dup * n)
+        dst = torch.randperm(n, generator=g)[:m]
+        src = (torch.rand(m, generator=g) * n).long()
+        kf[dst] = kf[src] + 1e-3 * torch.randn(m, Di, generator=g)
+    qf = torch.randn(len(lengths), Hi, Di, generator=g)
+    if dtype == 0:
+        k, q = kf.to(torch.bfloat16), qf.to(torch.bfloat16)
+        kn, qn = _bits(k), _bits(q)
+    else:
+        k = kf.to(torch.float8_e4m3fn).view(torch.uint8)
+        q = qf.to(torch.float8_e4m3fn).view(torch.uint8)
+        kn, qn = k.numpy(), q.numpy()
+    w = torch.rand(len(lengths), Hi, generator=g)
+    cu = torch.tensor([0] + list(np.cumsum(lengths)), dtype=torch.int64)
+    return k, q, w, cu, kn, qn
+
+
+def _run_index(csa2, k, q, w, cu, vis, dtype, topk, cand=None, bm=None):
+    nq = q.shape[0]
+    max_vis = int(max(vis)) if len(vis) else 0
+    out = torch.empty((nq, topk), dtype=torch.int32, device="cuda")
+    ncand = 0 if cand is None else cand.shape[1]
+    ws = csa2.workspace(csa2.csa2_index_score_topk_workspace_size(nq, max_vis, ncand, topk))
+    csa2.csa2_index_score_topk(q.cuda(), dtype, w.cuda(), k.cuda(), cu.cuda(),
+                               torch.arange(nq, dtype=torch.int32, device="cuda"),
+                               torch.tensor(vis, dtype=torch.int32, device="cuda"), max_vis, topk,
+                               out, cand_blocks=None if cand is None else cand.cuda(),
+                               out_block_max=bm, ws=ws)
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("dtype,Hi,lengths,topk,dup", [
+    (1, 8, [5, 3001, 20000], 2048, 0.0),
+    (1, 8, [9000, 40000], 100, 0.1),
+    (1, 8, [17000], 1, 0.1),
+    (0, 4, [4096, 700], 512, 0.0),
+    (1, 16, [3000], 3000, 0.0),
+])
+def test_full_topk_and_block_max(csa2, dtype, Hi, lengths, topk, dup):
+    k, q, w, cu, kn, qn = _index_case(lengths, dtype, Hi, sum(lengths) + topk, dup)
+    vis = list(lengths)
+    nb = (max(vis) + 7) // 8
+    bm = torch.full((len(vis), nb), float("nan"), device="cuda")
+    got = _run_index(csa2, k, q, w, cu, vis, dtype, topk, bm=bm)
+    ref = oracle.index_score_topk(qn, dtype, w.numpy(), kn, cu.numpy(), np.arange(len(vis)),
+                                  np.array(vis), topk)
+    bmh = bm.cpu().numpy()
+    for n in range(len(vis)):
+        check_topk(got[n], ref[n], topk, f"query {n}")
+        nbn = (vis[n] + 7) // 8
+        np.testing.assert_allclose(bmh[n, :nbn], ref[n]["bm"], rtol=2e-6, atol=1e-6)
+
+
+def test_full_short_and_empty_visibility(csa2):
+    k, q, w, cu, kn, qn = _index_case([1000, 1000, 1000], 1, 8, 5)
+    vis = [0, 3, 999]  # nothing visible / fewer candidates than K / ragged
+    got = _run_index(csa2, k, q, w, cu, vis, 1, 64)
+    ref = oracle.index_score_topk(qn, 1, w.numpy(), kn, cu.numpy(), np.arange(3), np.array(vis), 64)
+    assert np.all(got[0] == -1)
+    for n in (1, 2):
+        check_topk(got[n], ref[n], 64, f"query {n}")
+
+
+def test_pool_and_reindex(csa2):
+    lengths = [30000, 16384 * 2 + 5]
+    k, q, w, cu, kn, qn = _index_case(lengths, 1, 8, 11, dup=0.05)
+    vis = lengths
+    nb = (max(vis) + 7) // 8
+    bm = torch.empty((2, nb), device="cuda")
+    _run_index(csa2, k, q, w, cu, vis, 1, 2048, bm=bm)
+    for n_pool in (2048, 100):
+        pool = torch.empty((2, n_pool), dtype=torch.int32, device="cuda")
+        csa2.csa2_hier_candidate_pool(bm, torch.tensor(vis, dtype=torch.int32, device="cuda"),
+                                      n_pool, pool)
+        bmh = bm.cpu().numpy()
+        ref_pool = oracle.hier_candidate_pool(bmh, vis, n_pool)  # same fp32 input: exact
+        for n in range(2):
+            assert np.array_equal(pool[n].cpu().numpy(), ref_pool[n])
+    # Reindex with new queries over the GPU pool (2048 blocks)
+    pool = torch.empty((2, 2048), dtype=torch.int32, device="cuda")
+    csa2.csa2_hier_candidate_pool(bm, torch.tensor(vis, dtype=torch.int32, device="cuda"), 2048,
+                                  pool)
+    g = torch.Generator().manual_seed(99)
+    q2 = torch.randn(2, 8, 128, generator=g).to(torch.float8_e4m3fn).view(torch.uint8)
+    w2 = torch.rand(2, 8, generator=g)
+    for topk in (2048, 512):
+        got = _run_index(csa2, k, q2, w2, cu, vis, 1, topk, cand=pool)
+        ref = oracle.index_score_topk(q2.numpy(), 1, w2.numpy(), kn, cu.numpy(), np.arange(2),
+                                      np.array(vis), topk, cand_blocks=pool.cpu().numpy())
+        for n in range(2):
+            check_topk(got[n], ref[n], topk, f"reindex query {n}")
+
+
+# ------------------------------------------------------------------------------------------------
+# Sparse attention
+# ------------------------------------------------------------------------------------------------
+def _attn_case(B, H, n_rows, topk, seed, holes=True):
+    g = torch.Generator().manual_seed(seed)
+    x = _kv(B * n_rows, seed)
+    q = torch.randn(B, H, 512, generator=g).to(torch.bfloat16)
+    idx = torch.stack([torch.randperm(n_rows, generator=g)[:topk] for _ in range(B)]).to(torch.int32)
+    if topk > n_rows:
+        raise ValueError
+    if holes:
+        idx[:, ::7] = -1
+    cu = torch.arange(0, (B + 1) * n_rows, n_rows, dtype=torch.int64)
+    return x, q, idx, cu
+
+
+@pytest.mark.parametrize("B,H,n_rows,topk", [(3, 64, 3000, 2048), (2, 16, 600, 512),
+                                              (1, 64, 100, 33), (4, 64, 50, 1)])
+def test_decode_attention(csa2, B, H, n_rows, topk):
+    x, q, idx, cu = _attn_case(B, H, n_rows, topk, B * 1000 + topk)
+    if topk == 1:
+        idx[1] = -1  # a sequence with no valid slot
+    codes = torch.empty((x.shape[0], 256), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((x.shape[0], 32), dtype=torch.uint8, device="cuda")
+    csa2.csa2_kv_quant_fp4(x.cuda(), codes, sf)
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H), device="cuda")
+    ws = csa2.workspace(csa2.csa2_sparse_attn_decode_workspace_size(B, H, topk))
+    scale = 1 / math.sqrt(512)
+    csa2.csa2_sparse_attn_decode(q.cuda(), codes, sf, cu.cuda(), idx.cuda(), scale, out, lse, ws=ws)
+    ref = oracle.sparse_attn_decode(_bits(q), codes.cpu().numpy(), sf.cpu().numpy(), cu.numpy(),
+                                    idx.numpy(), scale)
+    ob, lh = _bits(out), lse.cpu().numpy()
+    for b in range(B):
+        check_attn(ob[b], lh[b], ref[b][0], ref[b][1], oracle.double_to_bf16(ref[b][0]), f"seq {b}")
+
+
+@pytest.mark.parametrize("T,H,topk", [(5, 64, 2048), (3, 16, 100)])
+def test_prefill_attention(csa2, T, H, topk):
+    n_rows = 4000
+    x, _, _, _ = _attn_case(1, H, n_rows, topk, T)
+    g = torch.Generator().manual_seed(T + 7)
+    q = torch.randn(T, H, 512, generator=g).to(torch.bfloat16)
+    idx = torch.stack([torch.randperm(n_rows, generator=g)[:topk] for _ in range(T)]).to(torch.int32)
+    idx[:, 3::11] = -1
+    cu = torch.tensor([0, n_rows], dtype=torch.int64)
+    q_seq = torch.zeros(T, dtype=torch.int32)
+    codes = torch.empty((n_rows, 256), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((n_rows, 32), dtype=torch.uint8, device="cuda")
+    csa2.csa2_kv_quant_fp4(x.cuda(), codes, sf)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, H), device="cuda")
+    ws = csa2.workspace(csa2.csa2_sparse_attn_prefill_workspace_size(T, H, topk))
+    scale = 1 / math.sqrt(512)
+    csa2.csa2_sparse_attn_prefill(q.cuda(), q_seq.cuda(), codes, sf, cu.cuda(), idx.cuda(), scale,
+                                  out, lse, ws=ws)
+    ref = oracle.sparse_attn_prefill(_bits(q), q_seq.numpy(), codes.cpu().numpy(),
+                                     sf.cpu().numpy(), cu.numpy(), idx.numpy(), scale)
+    ob, lh = _bits(out), lse.cpu().numpy()
+    for i in range(T):
+        check_attn(ob[i], lh[i], ref[i][0], ref[i][1], oracle.double_to_bf16(ref[i][0]), f"tok {i}")
