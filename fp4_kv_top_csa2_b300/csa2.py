@@ -34,8 +34,8 @@ def _load() -> ctypes.CDLL:
         "csa2_error_string": (ctypes.c_char_p, [I]),
         "csa2_kv_quant_fp4": (I, [P, I64, I, P, P, P, P]),
         "csa2_index_score_topk_workspace_size": (SZ, [I, I64, I, I]),
-        "csa2_index_score_topk": (I, [P, I, P, I, I, I, P, I, P, P, I, P, P, I64, P, I, I, P, P, P,
-                                      SZ, P]),
+        "csa2_index_score_topk": (I, [P, I, P, I, I, I, P, I, I64, P, P, I, P, P, I64, P, I, I, P,
+                                      P, P, SZ, P]),
         "csa2_hier_candidate_pool_workspace_size": (SZ, [I, I64, I]),
         "csa2_hier_candidate_pool": (I, [P, I, P, I64, I, I, P, P, SZ, P]),
         "csa2_sparse_attn_decode_workspace_size": (SZ, [I, I, I]),
@@ -99,7 +99,8 @@ def csa2_index_score_topk(q_idx, q_dtype, w, k_idx, cu_ctx, q_seq, q_vis, max_vi
     n_cand = 0 if cand_blocks is None else cand_blocks.shape[1]
     wp, wn = _ws(ws)
     _check("csa2_index_score_topk", lib.csa2_index_score_topk(
-        _ptr(q_idx), q_dtype, _ptr(w), nq, Hi, Di, _ptr(k_idx), q_dtype, _ptr(k_scale),
+        _ptr(q_idx), q_dtype, _ptr(w), nq, Hi, Di, _ptr(k_idx), q_dtype, k_idx.shape[0],
+        _ptr(k_scale),
         _ptr(cu_ctx), B, _ptr(q_seq), _ptr(q_vis), max_vis, _ptr(cand_blocks), n_cand, topk,
         _ptr(out_idx), _ptr(out_block_max), wp, wn, _stream(stream)))
 

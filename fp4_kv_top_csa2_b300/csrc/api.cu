@@ -48,10 +48,18 @@ struct WsCursor {
 };
 
 // Workspace layout of csa2_index_score_topk (also used to size it).
+//   Reindex: scores of the candidate slots.
+//   Full:    block maxima (unless the caller passes out_block_max, the region stays reserved),
+//            the Top-K block list, and either the score of every visible position (tensor-core
+//            path while that array stays small: the final selection reads it by position) or
+//            the scores of the positions of the selected blocks (rescored).
+constexpr int64_t kKeepScoresMax = (int64_t)1 << 27;  // elements
+
 struct ScoreWs {
   float *bm = nullptr;
   int32_t *blocks = nullptr;
-  float *scores = nullptr;
+  float *scores = nullptr;      // candidate-slot scores
+  float *pos_scores = nullptr;  // per-position scores (Full, tensor-core path)
   size_t bytes = 0;
   int64_t nb_max = 0;
   int kb = 0;
@@ -67,7 +75,10 @@ ScoreWs score_ws(void *base, int nq, int64_t max_vis, int n_cand_blocks, int top
     w.kb = (int)std::min<int64_t>(topk, w.nb_max);
     w.bm = c.take<float>((size_t)nq * w.nb_max);
     w.blocks = c.take<int32_t>((size_t)nq * w.kb);
-    w.scores = c.take<float>((size_t)nq * w.kb * kBlock);
+    if (index_mma_supported(nq) && (int64_t)nq * max_vis <= kKeepScoresMax)
+      w.pos_scores = c.take<float>((size_t)nq * max_vis);
+    else
+      w.scores = c.take<float>((size_t)nq * w.kb * kBlock);
   }
   w.bytes = c.used;
   return w;
@@ -108,13 +119,13 @@ size_t csa2_index_score_topk_workspace_size(int nq, int64_t max_vis, int n_cand_
 }
 
 int csa2_index_score_topk(const void *q_idx, int q_dtype, const float *w, int nq, int Hi, int Di,
-                          const void *k_idx, int k_dtype, const float *k_scale,
+                          const void *k_idx, int k_dtype, int64_t k_rows, const float *k_scale,
                           const int64_t *cu_ctx, int B, const int32_t *q_seq,
                           const int32_t *q_vis, int64_t max_vis, const int32_t *cand_blocks,
                           int n_cand_blocks, int topk, int32_t *out_idx, float *out_block_max,
                           void *workspace, size_t ws_bytes, void *stream) {
   if (nq < 0 || nq > 65535 || B < 1 || Hi < 1 || Hi > 16 || topk < 1 || topk > 4096 ||
-      max_vis < 0 || max_vis > (int64_t)1 << 30)
+      max_vis < 0 || max_vis > (int64_t)1 << 30 || k_rows < 0 || k_rows > INT32_MAX)
     return CSA2_ERR_INVALID_ARG;
   if (q_dtype != k_dtype) return CSA2_ERR_INVALID_ARG;
   if (!((q_dtype == CSA2_BF16 && Di == 64) || (q_dtype == CSA2_E4M3 && Di == 128)))
@@ -135,10 +146,13 @@ int csa2_index_score_topk(const void *q_idx, int q_dtype, const float *w, int nq
   if (int r = check_device()) return r;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ScoreWs ws = score_ws(workspace, nq, max_vis, n_cand_blocks, topk);
+  const bool mma = index_mma_supported(nq);
   cudaError_t e;
   if (cand_blocks) {  // Reindex: score the listed blocks, select
-    e = launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
-                          cand_blocks, n_cand_blocks, ws.scores, st);
+    e = mma ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx,
+                                    q_seq, q_vis, cand_blocks, n_cand_blocks, ws.scores, st)
+            : launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq,
+                                q_vis, cand_blocks, n_cand_blocks, ws.scores, st);
     if (e == cudaSuccess)
       e = launch_topk(ws.scores, (int64_t)n_cand_blocks * kBlock, (int64_t)n_cand_blocks * kBlock,
                       cand_blocks, n_cand_blocks, 1, q_vis, nq, topk, out_idx, st);
@@ -146,15 +160,28 @@ int csa2_index_score_topk(const void *q_idx, int q_dtype, const float *w, int nq
   }
   // Full: block maxima over every visible position; the Top-K positions lie inside the Top-K
   // blocks by block maximum (each block ahead of a selected position's block holds a position
-  // ranked ahead of it), so select those blocks first, then rescore and select their positions.
+  // ranked ahead of it), so select those blocks first, then select among their positions.
   float *bm = out_block_max ? out_block_max : ws.bm;
-  e = launch_score_scan(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
-                        max_vis, bm, ws.nb_max, st);
+  if (mma) {
+    e = launch_score_scan_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx, q_seq,
+                              q_vis, max_vis, bm, ws.nb_max, ws.pos_scores, max_vis, st);
+  } else {
+    e = launch_score_scan(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
+                          max_vis, bm, ws.nb_max, st);
+  }
   if (e == cudaSuccess)
     e = launch_topk(bm, ws.nb_max, ws.nb_max, nullptr, 0, kBlock, q_vis, nq, ws.kb, ws.blocks, st);
+  if (ws.pos_scores) {  // the scan kept every score: select among the blocks' positions
+    if (e == cudaSuccess)
+      e = launch_topk(nullptr, 0, (int64_t)ws.kb * kBlock, ws.blocks, ws.kb, 1, q_vis, nq, topk,
+                      out_idx, st, ws.pos_scores, max_vis);
+    return cuda_status(e);
+  }
   if (e == cudaSuccess)
-    e = launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
-                          ws.blocks, ws.kb, ws.scores, st);
+    e = mma ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx,
+                                    q_seq, q_vis, ws.blocks, ws.kb, ws.scores, st)
+            : launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq,
+                                q_vis, ws.blocks, ws.kb, ws.scores, st);
   if (e == cudaSuccess)
     e = launch_topk(ws.scores, (int64_t)ws.kb * kBlock, (int64_t)ws.kb * kBlock, ws.blocks,
                     ws.kb, 1, q_vis, nq, topk, out_idx, st);

@@ -3,6 +3,7 @@
 
 #include <atomic>
 
+#include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -118,9 +119,25 @@ cudaError_t launch_score_cand(const void *q_idx, int dtype, const float *w, int 
 //                   (unit = 8 for block maxima, 1 for positions);
 //   map != nullptr: element i is position map[n*map_stride + i/8]*8 + i%8, valid iff the block
 //                   id is >= 0 and the position is < q_vis[n].
+//   pos_vals != nullptr: the value of an element is pos_vals[n*pos_stride + position] instead.
 cudaError_t launch_topk(const float *vals, int64_t stride, int64_t n_elems, const int32_t *map,
                         int64_t map_stride, int unit, const int32_t *q_vis, int nq, int topk,
-                        int32_t *out, cudaStream_t st);
+                        int32_t *out, cudaStream_t st, const float *pos_vals = nullptr,
+                        int64_t pos_stride = 0);
+
+// Tensor-core indexer (index_mma.cu).
+bool index_mma_supported(int nq);
+cudaError_t launch_score_scan_mma(const void *q_idx, int dtype, const float *w, int nq, int Hi,
+                                  const void *k_idx, int64_t k_rows, const float *k_scale,
+                                  const int64_t *cu_ctx, const int32_t *q_seq,
+                                  const int32_t *q_vis, int64_t max_vis, float *bm,
+                                  int64_t bm_stride, float *scores, int64_t sc_stride,
+                                  cudaStream_t st);
+cudaError_t launch_score_cand_mma(const void *q_idx, int dtype, const float *w, int nq, int Hi,
+                                  const void *k_idx, int64_t k_rows, const float *k_scale,
+                                  const int64_t *cu_ctx, const int32_t *q_seq,
+                                  const int32_t *q_vis, const int32_t *cand, int n_cand,
+                                  float *scores, cudaStream_t st);
 
 cudaError_t launch_attn(const void *q_bf16, const uint8_t *q_codes, const uint8_t *q_sf, int nq,
                         int H, const int32_t *q_seq, const uint8_t *codes, const uint8_t *sf,

@@ -2,6 +2,7 @@
 // kernels share the device status word and the compiler sees every call).
 #include "kv_quant.cu"
 #include "index_score.cu"
+#include "index_mma.cu"
 #include "topk.cu"
 #include "attn_simt.cu"
 #include "api.cu"

@@ -20,6 +20,7 @@ constexpr int kWarps = kTopkThreads / 32;
 
 struct ElemView {
   const float *vals;
+  const float *pos_vals;  // non-null: the value of an element is pos_vals[its position]
   const int32_t *map;  // nullptr: identity
   int64_t n_elems;
   int64_t limit;       // identity: valid iff i < limit; map: valid iff pos < limit
@@ -32,7 +33,7 @@ struct ElemView {
       pos = i;
       if (i >= limit) return false;
     }
-    key = float_key(vals[i]);
+    key = float_key(pos_vals ? pos_vals[pos] : vals[i]);
     return true;
   }
 };
@@ -69,7 +70,8 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
-    const float *__restrict__ vals, int64_t stride, int64_t n_elems,
+    const float *__restrict__ vals, int64_t stride, const float *__restrict__ pos_vals,
+    int64_t pos_stride, int64_t n_elems,
     const int32_t *__restrict__ map, int64_t map_stride, int unit,
     const int32_t *__restrict__ q_vis, int topk, int32_t *__restrict__ out) {
   __shared__ uint32_t hist[2048];
@@ -79,7 +81,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
   const int n = blockIdx.x;
   const int64_t V = q_vis[n];
   ElemView ev;
-  ev.vals = vals + (int64_t)n * stride;
+  ev.vals = vals ? vals + (int64_t)n * stride : nullptr;
+  ev.pos_vals = pos_vals ? pos_vals + (int64_t)n * pos_stride : nullptr;
   ev.map = map ? map + (int64_t)n * map_stride : nullptr;
   ev.n_elems = n_elems;
   ev.limit = map ? V : (V + unit - 1) / unit;
@@ -93,10 +96,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
   const int shifts[3] = {21, 10, 0};
   const int widths[3] = {11, 11, 10};
 
+  if (threadIdx.x == 0) s_nvalid = 0;
   for (int pass = 0; pass < 3 && !done; ++pass) {
     const int shift = shifts[pass], nb = 1 << widths[pass];
     for (int i = threadIdx.x; i < nb; i += kTopkThreads) hist[i] = 0;
-    if (threadIdx.x == 0) s_nvalid = 0;
     __syncthreads();
     uint32_t local_valid = 0;
     for (int64_t i = threadIdx.x; i < n_elems; i += kTopkThreads) {
@@ -192,10 +195,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
 
 cudaError_t launch_topk(const float *vals, int64_t stride, int64_t n_elems, const int32_t *map,
                         int64_t map_stride, int unit, const int32_t *q_vis, int nq, int topk,
-                        int32_t *out, cudaStream_t st) {
+                        int32_t *out, cudaStream_t st, const float *pos_vals,
+                        int64_t pos_stride) {
   if (nq == 0) return cudaSuccess;
-  topk_kernel<<<nq, kTopkThreads, 0, st>>>(vals, stride, n_elems, map, map_stride, unit, q_vis,
-                                           topk, out);
+  topk_kernel<<<nq, kTopkThreads, 0, st>>>(vals, stride, pos_vals, pos_stride, n_elems, map,
+                                           map_stride, unit, q_vis, topk, out);
   note_launches(1);
   return cudaGetLastError();
 }

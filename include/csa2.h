@@ -103,15 +103,17 @@ int csa2_kv_quant_fp4(const void *x_bf16, int64_t n_rows, int d, const int64_t *
  * q_idx     [nq, Hi, Di] of q_dtype.            w [nq, Hi] fp32.
  * q_dtype / k_dtype  must be equal: CSA2_BF16 (then Di == 64) or CSA2_E4M3 (then Di == 128);
  *           so every index-key row is 128 bytes.  1 <= Hi <= 16.
- * k_idx     [total_rows, Di] of k_dtype, sequence b occupying rows [cu_ctx[b], cu_ctx[b+1]).
- * k_scale   NULL or [total_rows] fp32 per-key scale (> 0).
+ * k_idx     [k_rows, Di] of k_dtype, sequence b occupying rows [cu_ctx[b], cu_ctx[b+1]).
+ * k_rows    number of rows of k_idx (>= cu_ctx[B]); bounds every key-tile load.
+ * k_scale   NULL or [k_rows] fp32 per-key scale (> 0).
  * cu_ctx    [B+1] int64, non-decreasing, cu_ctx[0] == 0.
  * q_seq     [nq] int32 in [0, B).   q_vis [nq] int32, 0 <= q_vis[n] <= rows of its sequence and
  *           q_vis[n] <= max_vis.  (Decode: q_vis = L_b; chunked prefill: q_vis = P0 + i + 1.)
  * max_vis   host-side upper bound of q_vis (sizes grids and workspace).
  * cand_blocks  NULL for Full mode (all t < V are candidates).  Reindex mode: [nq, n_cand_blocks]
  *           int32 block ids; candidates are t = block_size*id + i (0 <= i < block_size), t < V,
- *           for every id >= 0 (ids must be distinct; -1 entries are ignored).  block_size = 8.
+ *           for every id >= 0; valid ids must be distinct and in ascending order (as
+ *           csa2_hier_candidate_pool writes them); -1 entries are ignored.  block_size = 8.
  * topk      1 <= topk <= 4096.
  * out_idx   [nq, topk] int32.
  * out_block_max  Full mode only: NULL, or [nq, ceil(max_vis/8)] fp32 receiving the block maxima
@@ -121,7 +123,7 @@ int csa2_kv_quant_fp4(const void *x_bf16, int64_t n_rows, int d, const int64_t *
 size_t csa2_index_score_topk_workspace_size(int nq, int64_t max_vis, int n_cand_blocks,
                                             int topk);
 int csa2_index_score_topk(const void *q_idx, int q_dtype, const float *w, int nq, int Hi, int Di,
-                          const void *k_idx, int k_dtype, const float *k_scale,
+                          const void *k_idx, int k_dtype, int64_t k_rows, const float *k_scale,
                           const int64_t *cu_ctx, int B, const int32_t *q_seq,
                           const int32_t *q_vis, int64_t max_vis, const int32_t *cand_blocks,
                           int n_cand_blocks, int topk, int32_t *out_idx, float *out_block_max,

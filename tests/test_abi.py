@@ -57,7 +57,8 @@ def test_host_validation_rejects_bad_arguments(csa2):
     assert L.csa2_kv_quant_fp4(None, 0, 512, None, None, None, None) == 0  # nothing to do
     # index score: dtype mismatch, wrong Di, topk out of range, workspace too small
     args = lambda qdt, Di, kdt, topk, ws, wsb: L.csa2_index_score_topk(
-        p, qdt, p, 1, 8, Di, p, kdt, None, p, 1, p, p, 1000, None, 0, topk, p, None, ws, wsb, None)
+        p, qdt, p, 1, 8, Di, p, kdt, 5000, None, p, 1, p, p, 1000, None, 0, topk, p, None, ws, wsb,
+        None)
     assert args(1, 128, 0, 16, p, 1 << 30) == -1
     assert args(1, 64, 1, 16, p, 1 << 30) == -1
     assert args(0, 128, 0, 16, p, 1 << 30) == -1

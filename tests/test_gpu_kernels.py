@@ -249,3 +249,41 @@ def test_prefill_attention(csa2, T, H, topk):
     ob, lh = _bits(out), lse.cpu().numpy()
     for i in range(T):
         check_attn(ob[i], lh[i], ref[i][0], ref[i][1], oracle.double_to_bf16(ref[i][0]), f"tok {i}")
+
+
+@pytest.mark.parametrize("dtype", [1, 0])
+def test_index_exact_when_scores_are_exact(csa2, dtype):
+    """Small-integer keys/queries and power-of-two head weights make every score exact in fp32,
+    so the GPU's block maxima and selection must equal the oracle's exactly -- including the
+    lower-position rule among the many exact ties this produces."""
+    g = torch.Generator().manual_seed(7 + dtype)
+    lengths = [5000, 12345]
+    Di = 128 if dtype == 1 else 64
+    kf = torch.randint(-3, 4, (sum(lengths), Di), generator=g).float()
+    qf = torch.randint(-2, 3, (2, 8 if dtype == 1 else 4, Di), generator=g).float()
+    w = torch.tensor([0.5, 0.25, 1.0, 2.0, 0.125, 4.0, 1.0, 0.5])[: qf.shape[1]].repeat(2, 1)
+    if dtype == 1:
+        k, q = kf.to(torch.float8_e4m3fn).view(torch.uint8), qf.to(torch.float8_e4m3fn).view(torch.uint8)
+        kn, qn = k.numpy(), q.numpy()
+    else:
+        k, q = kf.to(torch.bfloat16), qf.to(torch.bfloat16)
+        kn, qn = _bits(k), _bits(q)
+    cu = torch.tensor([0, lengths[0], sum(lengths)], dtype=torch.int64)
+    vis = lengths
+    nb = (max(vis) + 7) // 8
+    bm = torch.empty((2, nb), device="cuda")
+    for topk in (1000, 37):
+        got = _run_index(csa2, k, q, w, cu, vis, dtype, topk, bm=bm)
+        ref = oracle.index_score_topk(qn, dtype, w.numpy(), kn, cu.numpy(), np.arange(2),
+                                      np.array(vis), topk)
+        for n in range(2):
+            nbn = (vis[n] + 7) // 8
+            assert np.array_equal(bm.cpu().numpy()[n, :nbn], ref[n]["bm"])
+            assert np.array_equal(got[n], ref[n]["idx"])
+    # Reindex over an explicit block list: exact too
+    blocks = torch.tensor([[3, 10, 11, 200, 624, -1], [0, 5, 999, 1500, 1543, -1]], dtype=torch.int32)
+    got = _run_index(csa2, k, q, w, cu, vis, dtype, 20, cand=blocks)
+    ref = oracle.index_score_topk(qn, dtype, w.numpy(), kn, cu.numpy(), np.arange(2),
+                                  np.array(vis), 20, cand_blocks=blocks.numpy())
+    for n in range(2):
+        assert np.array_equal(got[n], ref[n]["idx"])
