@@ -44,34 +44,48 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """nvidia-smi clock / throttle samples (every 50 ms) with host timestamps, so the samples
+    that fall inside the timed window can be picked out afterwards."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.samples = []  # (host time, sm_mhz, sm_max_mhz, active reasons)
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 5.0:  # wait for the first sample
+                time.sleep(0.02)
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm, smax = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            act = [nm for nm, v in zip(self.NAMES, parts[4:8]) if v.lower().startswith("active")]
+            self.samples.append((time.time(), sm, smax, act))
 
-    def __exit__(self, *a):
+    def stop(self):
         if self.proc:
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -79,25 +93,17 @@ class ClockSampler:
                 self.proc.kill()
             self.t.join(timeout=2)
 
-    def summary(self):
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax = float(parts[1])
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        where = "timed window"
+        if not inside:  # window shorter than the sampling period: nearest samples around it
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            where = "nearest to the timed window (window shorter than the 50 ms sample period)"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = sorted({r for s in inside for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": inside[0][2],
+                "reasons": reasons, "samples": len(inside), "sampled": where}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -122,6 +128,7 @@ def run_ours(args, rank, world):
         if world > 1:
             dist.barrier()
 
+    clk = ClockSampler(dev.index).start()
     for _ in range(args.warmup):
         st.run()
     torch.cuda.synchronize()
@@ -132,15 +139,16 @@ def run_ours(args, rank, world):
           for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
-        t0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            ev[i][0].record(stream)
-            st.run()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
+    tw0 = time.time()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        st.run()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    tw1 = time.time()
     barrier()
     launches = csa2.kernel_launches() - launches0
     step_ms = [a.elapsed_time(b) for a, b in ev]
@@ -160,6 +168,7 @@ def run_ours(args, rank, world):
 
     # end to end through the C ABI with host buffers
     e2e = run_e2e(st, args.steps, dev)
+    clk.stop()
 
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 2), "unit": "tokens/s",
@@ -181,7 +190,7 @@ def run_ours(args, rank, world):
                      "ms_per_launch": round(dom_ms, 5), "algorithmic_bytes": dom_bytes},
         "breakdown_ms": {k: round(v, 5) for k, v in parts.items()},
         "e2e": e2e, "gpu_launches": launches, "wall_s_timed": round(wall, 4),
-        "clocks": clk.summary(),
+        "clocks": clk.summary(tw0, tw1),
     }
     if args.prefill and rank == 0:
         line["prefill"] = run_prefill(args, dev, peaks)
