@@ -36,6 +36,8 @@ def _load() -> ctypes.CDLL:
         "csa2_index_score_topk_workspace_size": (SZ, [I, I64, I, I]),
         "csa2_index_score_topk": (I, [P, I, P, I, I, I, P, I, I64, P, P, I, P, P, I64, P, I, I, P,
                                       P, P, SZ, P]),
+        "csa2_index_score_topk_reindex_noalloc": (I, [P, I, P, I, I, I, P, I, I64, P, P, I, P, P,
+                                                      I64, P, I, I, P, P]),
         "csa2_hier_candidate_pool_workspace_size": (SZ, [I, I64, I]),
         "csa2_hier_candidate_pool": (I, [P, I, P, I64, I, I, P, P, SZ, P]),
         "csa2_sparse_attn_decode_workspace_size": (SZ, [I, I, I]),
@@ -103,6 +105,17 @@ def csa2_index_score_topk(q_idx, q_dtype, w, k_idx, cu_ctx, q_seq, q_vis, max_vi
         _ptr(k_scale),
         _ptr(cu_ctx), B, _ptr(q_seq), _ptr(q_vis), max_vis, _ptr(cand_blocks), n_cand, topk,
         _ptr(out_idx), _ptr(out_block_max), wp, wn, _stream(stream)))
+
+
+def csa2_index_score_topk_reindex_noalloc(q_idx, q_dtype, w, k_idx, cu_ctx, q_seq, q_vis, max_vis,
+                                          topk, out_idx, cand_blocks, k_scale=None, stream=None):
+    """Reindex selection with the library's own fixed scratch (no workspace argument)."""
+    nq, Hi, Di = q_idx.shape
+    B = cu_ctx.numel() - 1
+    _check("csa2_index_score_topk_reindex_noalloc", lib.csa2_index_score_topk_reindex_noalloc(
+        _ptr(q_idx), q_dtype, _ptr(w), nq, Hi, Di, _ptr(k_idx), q_dtype, k_idx.shape[0],
+        _ptr(k_scale), _ptr(cu_ctx), B, _ptr(q_seq), _ptr(q_vis), max_vis, _ptr(cand_blocks),
+        cand_blocks.shape[1], topk, _ptr(out_idx), _stream(stream)))
 
 
 def csa2_hier_candidate_pool_workspace_size(nq, max_blocks, n_pool_blocks):

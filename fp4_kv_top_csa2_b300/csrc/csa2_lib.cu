@@ -6,3 +6,4 @@
 #include "topk.cu"
 #include "attn_simt.cu"
 #include "api.cu"
+#include "noalloc.cu"

@@ -129,6 +129,35 @@ int csa2_index_score_topk(const void *q_idx, int q_dtype, const float *w, int nq
                           int n_cand_blocks, int topk, int32_t *out_idx, float *out_block_max,
                           void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * csa2_index_score_topk_reindex_noalloc -- Reindex mode of csa2_index_score_topk that takes no
+ * workspace.  The pages have no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory when they call the library: for example a plugin running inside
+ * another engine that hands it only input and output buffers, or a process that has reserved
+ * all device memory up front, where a cudaMalloc would fail or stall the device.
+ *
+ * Arguments and results are exactly those of csa2_index_score_topk with cand_blocks non-NULL
+ * (Reindex mode) and no out_block_max, workspace or ws_bytes.  The scratch it needs -- one fp32
+ * score per candidate slot -- lives in a fixed array of 1,048,576 floats (4 MiB) inside the
+ * library, which every GPU that loads the library holds until the process exits.  Requests with
+ * nq * n_cand_blocks * 8 > 1,048,576 (e.g. more than 64 queries over a 2,048-block pool) return
+ * CSA2_ERR_WORKSPACE and enqueue nothing.  The call allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ *
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  Every call shares the
+ * one array: two calls whose work overlaps on the GPU (different streams without ordering, or
+ * different host threads on the same device) race on it and give undefined results.  Nothing in
+ * the array needs clearing between calls: each call writes every slot it reads.
+ */
+int csa2_index_score_topk_reindex_noalloc(const void *q_idx, int q_dtype, const float *w, int nq,
+                                          int Hi, int Di, const void *k_idx, int k_dtype,
+                                          int64_t k_rows, const float *k_scale,
+                                          const int64_t *cu_ctx, int B, const int32_t *q_seq,
+                                          const int32_t *q_vis, int64_t max_vis,
+                                          const int32_t *cand_blocks, int n_cand_blocks, int topk,
+                                          int32_t *out_idx, void *stream);
+
 /* ------------------------------------------------------------------------------------------ */
 /* 3. Hierarchical candidate pool                                                               */
 /* ------------------------------------------------------------------------------------------ */
