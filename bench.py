@@ -129,12 +129,14 @@ def run_ours(args, rank, world):
             dist.barrier()
 
     clk = ClockSampler(dev.index).start()
+    st.capture()  # the whole step as one CUDA graph (same C-ABI calls as Step.run)
     for _ in range(args.warmup):
-        st.run()
+        st.replay()
     torch.cuda.synchronize()
+    launches_per_step = launches_of(st)
     launches0 = csa2.kernel_launches()
 
-    # timed region: K steps, per-step events, L2 flushed between steps (outside the events)
+    # timed region: K graph replays, per-step events, L2 flushed between steps (outside events)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier()
@@ -144,13 +146,14 @@ def run_ours(args, rank, world):
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
-        st.run()
+        st.replay()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     tw1 = time.time()
     barrier()
-    launches = csa2.kernel_launches() - launches0
+    assert csa2.kernel_launches() == launches0  # replays enqueue no new host-side launches
+    launches = launches_per_step * args.steps
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = sum(step_ms) / len(step_ms)
     if world > 1:
@@ -161,13 +164,15 @@ def run_ours(args, rank, world):
     tokens_per_s = world * w.B / (ms / 1e3)
     step_gbs = by["total"] / (ms / 1e3) / 1e9
 
-    # breakdown by C-ABI call (same work, events between calls), for the dominant call's roofline
+    # per-call device times: each call captured as its own graph, replayed with events
     parts = profile_calls(st, args.steps, flush)
-    dom_name, dom_ms, dom_bytes = "csa2_index_score_topk (Full, 1,048,576 keys)", parts["full_index"], by["index_keys_full"]
+    dom_name, dom_ms, dom_bytes = ("csa2_index_score_topk (Full, 1,048,576 keys)",
+                                   parts["full_index"], by["index_keys_full"])
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
 
-    # end to end through the C ABI with host buffers
-    e2e = run_e2e(st, args.steps, dev)
+    # end to end through the C ABI with host buffers (direct calls, no graph), and with the graph
+    e2e = run_e2e(st, args.steps, dev, graph=False)
+    e2e_graph = run_e2e(st, args.steps, dev, graph=True)
     clk.stop()
 
     line = {
@@ -189,7 +194,9 @@ def run_ours(args, rank, world):
                      "peak_source": peaks["source"] + " (burst copy)", "traffic": None,
                      "ms_per_launch": round(dom_ms, 5), "algorithmic_bytes": dom_bytes},
         "breakdown_ms": {k: round(v, 5) for k, v in parts.items()},
-        "e2e": e2e, "gpu_launches": launches, "wall_s_timed": round(wall, 4),
+        "timing": "step = one CUDA-graph replay of all calls; CUDA events on the launching stream",
+        "e2e": e2e, "e2e_graph": e2e_graph, "gpu_launches": launches,
+        "gpu_launches_per_step": launches_per_step, "wall_s_timed": round(wall, 4),
         "clocks": clk.summary(tw0, tw1),
     }
     if args.prefill and rank == 0:
@@ -199,53 +206,62 @@ def run_ours(args, rank, world):
     return line
 
 
-def profile_calls(st, steps, flush):
-    """Per-call CUDA-event times of the step (same calls as Step.run)."""
+def launches_of(st):
+    """Kernels one step launches (counted by the library while enqueuing one un-captured step)."""
     import torch
     from fp4_kv_top_csa2_b300 import csa2
-    names = []
-    recs = []
-    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    a = csa2.kernel_launches()
+    st.run()
+    torch.cuda.synchronize()
+    return csa2.kernel_launches() - a
 
-    def mark(name):
-        e = torch.cuda.Event(enable_timing=True)
-        e.record(stream)
-        recs.append((name, e))
 
-    acc = {}
-    for _ in range(steps):
-        flush.zero_()
-        recs.clear()
-        mark("start")
-        st.quantize_new_rows()
-        mark("kv_quant")
-        last = None
-        for i, L in enumerate(st.layers):
-            if L["mode"] == "full":
-                st.index(L, block_max=st.bm)
-                mark("full_index")
-                csa2.csa2_hier_candidate_pool(st.bm, st.q_vis, st.w.n_pool_blocks, st.pool)
-                mark("pool")
-                last = L["idx"]
-            elif L["mode"] == "reindex":
-                st.index(L, cand=st.pool)
-                mark("reindex_index")
-                last = L["idx"]
-            st.attend(L, last)
-            mark("attention")
-        torch.cuda.synchronize()
-        for (n0, e0), (n1, e1) in zip(recs[:-1], recs[1:]):
-            acc.setdefault(n1, []).append(e0.elapsed_time(e1))
+def profile_calls(st, steps, flush):
+    """Device time of each C-ABI call of the step: every call is captured into its own CUDA graph
+    and replayed `steps` times between CUDA events (L2 flushed before each replay)."""
+    import torch
+    from fp4_kv_top_csa2_b300 import csa2
+    full = next(L for L in st.layers if L["mode"] == "full")
+    reidx = next((L for L in st.layers if L["mode"] == "reindex"), None)
+    calls = {
+        "kv_quant": lambda s: st.quantize_new_rows(stream=s),
+        "full_index": lambda s: st.index(full, block_max=st.bm, stream=s),
+        "pool": lambda s: csa2.csa2_hier_candidate_pool(st.bm, st.q_vis, st.w.n_pool_blocks,
+                                                        st.pool, ws=st.ws_pool, stream=s),
+        "attention": lambda s: st.attend(full, full["idx"], stream=s),
+    }
+    if reidx is not None:
+        calls["reindex_index"] = lambda s: st.index(reidx, cand=st.pool, stream=s)
     out = {}
-    for k, v in acc.items():  # average per call, and total per step
-        out[k] = sum(v) / len(v)
-        out[k + "_per_step"] = sum(v) / steps
+    stream = torch.cuda.current_stream()
+    for name, fn in calls.items():
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+                fn(side)
+        stream.wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize()
+        tms = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            tms.append(a.elapsed_time(b))
+        out[name] = sum(tms) / len(tms)
     return out
 
 
-def run_e2e(st, steps, dev):
+def run_e2e(st, steps, dev, graph=False):
     """Same step through the C ABI, inputs copied from pinned host memory each step and the
-    attention outputs read back, all inside the timed region."""
+    attention outputs read back, all inside the timed region.  graph=True replays the captured
+    step between the copies instead of issuing the calls one by one."""
     import torch
     host_in = {"new_x": st.new_x.cpu().pin_memory()}
     for i, L in enumerate(st.layers):
@@ -264,7 +280,10 @@ def run_e2e(st, steps, dev):
             if "q_idx" in L:
                 L["q_idx"].copy_(host_in[f"q_idx{i}"], non_blocking=True)
                 L["w"].copy_(host_in[f"w{i}"], non_blocking=True)
-        st.run()
+        if graph:
+            st.replay()
+        else:
+            st.run()
         for i, L in enumerate(st.layers):
             host_out[i].copy_(L["out"], non_blocking=True)
 
@@ -276,7 +295,8 @@ def run_e2e(st, steps, dev):
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     return {"value": round(st.w.B / dt, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 4)}
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 4),
+            "path": "graph replay" if graph else "direct C-ABI calls"}
 
 
 def run_prefill(args, dev, peaks):

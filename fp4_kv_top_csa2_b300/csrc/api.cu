@@ -60,6 +60,7 @@ struct ScoreWs {
   int32_t *blocks = nullptr;
   float *scores = nullptr;      // candidate-slot scores
   float *pos_scores = nullptr;  // per-position scores (Full, tensor-core path)
+  void *topk = nullptr;         // scratch of the Top-K selections (shared: they run in turn)
   size_t bytes = 0;
   int64_t nb_max = 0;
   int kb = 0;
@@ -70,6 +71,7 @@ ScoreWs score_ws(void *base, int nq, int64_t max_vis, int n_cand_blocks, int top
   WsCursor c(base);
   if (n_cand_blocks > 0) {
     w.scores = c.take<float>((size_t)nq * n_cand_blocks * kBlock);
+    w.topk = c.take<char>(topk_workspace_bytes(nq, (int64_t)n_cand_blocks * kBlock));
   } else {
     w.nb_max = (max_vis + kBlock - 1) / kBlock;
     w.kb = (int)std::min<int64_t>(topk, w.nb_max);
@@ -79,6 +81,8 @@ ScoreWs score_ws(void *base, int nq, int64_t max_vis, int n_cand_blocks, int top
       w.pos_scores = c.take<float>((size_t)nq * max_vis);
     else
       w.scores = c.take<float>((size_t)nq * w.kb * kBlock);
+    w.topk = c.take<char>(std::max(topk_workspace_bytes(nq, w.nb_max),
+                                   topk_workspace_bytes(nq, (int64_t)w.kb * kBlock)));
   }
   w.bytes = c.used;
   return w;
@@ -147,15 +151,18 @@ int csa2_index_score_topk(const void *q_idx, int q_dtype, const float *w, int nq
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ScoreWs ws = score_ws(workspace, nq, max_vis, n_cand_blocks, topk);
   const bool mma = index_mma_supported(nq);
+  const bool multi = !mma && index_multi_supported(nq, Hi, B);
+  const bool cand_mma = cand_mma_supported();
   cudaError_t e;
   if (cand_blocks) {  // Reindex: score the listed blocks, select
-    e = mma ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx,
+    e = cand_mma ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx,
                                     q_seq, q_vis, cand_blocks, n_cand_blocks, ws.scores, st)
             : launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq,
                                 q_vis, cand_blocks, n_cand_blocks, ws.scores, st);
     if (e == cudaSuccess)
       e = launch_topk(ws.scores, (int64_t)n_cand_blocks * kBlock, (int64_t)n_cand_blocks * kBlock,
-                      cand_blocks, n_cand_blocks, 1, q_vis, nq, topk, out_idx, st);
+                      cand_blocks, n_cand_blocks, 1, q_vis, nq, topk, out_idx, st, nullptr, 0,
+                      ws.topk);
     return cuda_status(e);
   }
   // Full: block maxima over every visible position; the Top-K positions lie inside the Top-K
@@ -165,39 +172,44 @@ int csa2_index_score_topk(const void *q_idx, int q_dtype, const float *w, int nq
   if (mma) {
     e = launch_score_scan_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx, q_seq,
                               q_vis, max_vis, bm, ws.nb_max, ws.pos_scores, max_vis, st);
+  } else if (multi) {  // chunked prefill over one sequence: 32 queries per key tile
+    e = launch_score_scan_multi(q_idx, q_dtype, w, nq, k_idx, k_rows, k_scale, q_vis, max_vis,
+                                bm, ws.nb_max, st);
   } else {
     e = launch_score_scan(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
                           max_vis, bm, ws.nb_max, st);
   }
   if (e == cudaSuccess)
-    e = launch_topk(bm, ws.nb_max, ws.nb_max, nullptr, 0, kBlock, q_vis, nq, ws.kb, ws.blocks, st);
+    e = launch_topk(bm, ws.nb_max, ws.nb_max, nullptr, 0, kBlock, q_vis, nq, ws.kb, ws.blocks, st,
+                    nullptr, 0, ws.topk);
   if (ws.pos_scores) {  // the scan kept every score: select among the blocks' positions
     if (e == cudaSuccess)
       e = launch_topk(nullptr, 0, (int64_t)ws.kb * kBlock, ws.blocks, ws.kb, 1, q_vis, nq, topk,
-                      out_idx, st, ws.pos_scores, max_vis);
+                      out_idx, st, ws.pos_scores, max_vis, ws.topk);
     return cuda_status(e);
   }
   if (e == cudaSuccess)
-    e = mma ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx,
-                                    q_seq, q_vis, ws.blocks, ws.kb, ws.scores, st)
+    e = (mma || multi) ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale,
+                                               cu_ctx, q_seq, q_vis, ws.blocks, ws.kb, ws.scores,
+                                               st)
             : launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq,
                                 q_vis, ws.blocks, ws.kb, ws.scores, st);
   if (e == cudaSuccess)
     e = launch_topk(ws.scores, (int64_t)ws.kb * kBlock, (int64_t)ws.kb * kBlock, ws.blocks,
-                    ws.kb, 1, q_vis, nq, topk, out_idx, st);
+                    ws.kb, 1, q_vis, nq, topk, out_idx, st, nullptr, 0, ws.topk);
   return cuda_status(e);
 }
 
 size_t csa2_hier_candidate_pool_workspace_size(int nq, int64_t max_blocks, int n_pool_blocks) {
-  (void)nq; (void)max_blocks; (void)n_pool_blocks;
-  return 0;
+  (void)n_pool_blocks;
+  if (nq < 0 || max_blocks < 0) return 0;
+  return align_up(topk_workspace_bytes(nq, max_blocks));
 }
 
 int csa2_hier_candidate_pool(const float *block_max, int nq, const int32_t *q_vis,
                              int64_t max_blocks, int block_size, int n_pool_blocks,
                              int32_t *out_pool_blocks, void *workspace, size_t ws_bytes,
                              void *stream) {
-  (void)workspace; (void)ws_bytes;
   if (nq < 0 || nq > 65535 || max_blocks < 0 || max_blocks > (int64_t)1 << 27 ||
       block_size != kBlock || n_pool_blocks < 1 || n_pool_blocks > 4096)
     return CSA2_ERR_INVALID_ARG;
@@ -205,15 +217,20 @@ int csa2_hier_candidate_pool(const float *block_max, int nq, const int32_t *q_vi
   if (!block_max || !q_vis || !out_pool_blocks) return CSA2_ERR_INVALID_ARG;
   if (!aligned16(block_max) || !aligned16(q_vis) || !aligned16(out_pool_blocks))
     return CSA2_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) return CSA2_ERR_INVALID_ARG;
+  const size_t need = csa2_hier_candidate_pool_workspace_size(nq, max_blocks, n_pool_blocks);
+  if (ws_bytes < need || (need && !workspace)) return CSA2_ERR_WORKSPACE;
   if (int r = check_device()) return r;
   return cuda_status(launch_topk(block_max, max_blocks, max_blocks, nullptr, 0, block_size, q_vis,
                                  nq, n_pool_blocks, out_pool_blocks,
-                                 static_cast<cudaStream_t>(stream)));
+                                 static_cast<cudaStream_t>(stream), nullptr, 0,
+                                 need ? workspace : nullptr));
 }
 
 size_t csa2_sparse_attn_decode_workspace_size(int B, int H, int topk) {
   if (B < 0 || H < 1 || topk < 1) return 0;
-  return align_up(attn_workspace_bytes(B, H, topk));
+  return align_up(attn_mma_supported(H, topk) ? attn_mma_workspace_bytes(B, H, topk)
+                                              : attn_workspace_bytes(B, H, topk));
 }
 
 static int attn_args_ok(int nq, int H, const uint8_t *codes, const uint8_t *sf,
@@ -241,16 +258,19 @@ int csa2_sparse_attn_decode(const void *q_bf16, int B, int H, const uint8_t *cod
   const size_t need = csa2_sparse_attn_decode_workspace_size(B, H, topk);
   if (ws_bytes < need || (need && !workspace)) return CSA2_ERR_WORKSPACE;
   if (int r = check_device()) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (attn_mma_supported(H, topk))
+    return cuda_status(launch_attn_mma(q_bf16, nullptr, nullptr, B, H, nullptr, codes, sf, cu_ctx,
+                                       idx, topk, softmax_scale, out_bf16, lse, workspace, st));
   return cuda_status(launch_attn(q_bf16, nullptr, nullptr, B, H, nullptr, codes, sf, cu_ctx, idx,
-                                 topk, softmax_scale, out_bf16, lse, workspace,
-                                 static_cast<cudaStream_t>(stream)));
+                                 topk, softmax_scale, out_bf16, lse, workspace, st));
 }
 
 size_t csa2_sparse_attn_prefill_workspace_size(int T, int H, int topk) {
   if (T < 0 || H < 1 || topk < 1) return 0;
   const size_t rows = (size_t)T * H;
   return align_up(rows * kCodeBytes) + align_up(rows * kSfBytes) +
-         align_up(attn_workspace_bytes(T, H, topk));
+         (attn_prefill_supported(H) ? 0 : align_up(attn_workspace_bytes(T, H, topk)));
 }
 
 int csa2_sparse_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_seq,
@@ -272,12 +292,15 @@ int csa2_sparse_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_
   const size_t rows = (size_t)T * H;
   uint8_t *q_codes = c.take<uint8_t>(rows * kCodeBytes);
   uint8_t *q_sf = c.take<uint8_t>(rows * kSfBytes);
-  void *attn_ws = c.take<char>(attn_workspace_bytes(T, H, topk));
+  const bool mma = attn_prefill_supported(H);
+  void *attn_ws = mma ? nullptr : c.take<char>(attn_workspace_bytes(T, H, topk));
   // the query is quantised per (token, head) row with the main-KV FP4 rule
   cudaError_t e = launch_kv_quant(q_bf16, (int64_t)rows, kD, nullptr, q_codes, q_sf, st);
   if (e == cudaSuccess)
-    e = launch_attn(nullptr, q_codes, q_sf, T, H, q_seq, codes, sf, cu_ctx, idx, topk,
-                    softmax_scale, out_bf16, lse, attn_ws, st);
+    e = mma ? launch_attn_prefill(q_codes, q_sf, T, H, q_seq, codes, sf, cu_ctx, idx, topk,
+                                  softmax_scale, out_bf16, lse, st)
+            : launch_attn(nullptr, q_codes, q_sf, T, H, q_seq, codes, sf, cu_ctx, idx, topk,
+                          softmax_scale, out_bf16, lse, attn_ws, st);
   return cuda_status(e);
 }
 

@@ -1,0 +1,337 @@
+// attn_prefill.cu -- sparse attention for chunked prefill on the tensor cores (tcgen05).
+//
+// Each query token has its own Top-K rows (the indexer's causal selection); the query is
+// quantised to FP4 with the main-KV rule and used exactly dequantised (fp16-exact).  One CTA
+// owns one query token (all heads, H <= 64) and walks its rows in tiles of 64 with an online
+// softmax, so no partial results leave the CTA:
+//   S   = Qhat Khat^T      kind::f16 (fp16), M=128 (heads, padded) x N=64 rows, fp32, TMEM cols 256..319
+//   O^T = Vhat^T P^T       kind::f16, M=128 channels x N=64 heads x K=16 rows per MMA, four
+//                          channel blocks -> TMEM cols 0..255 (channels on lanes, heads on
+//                          columns), accumulated over all tiles.
+// Vhat^T is the dequantised tile read as an MN-major A operand (two 64-channel atoms 8 KB
+// apart), P^T the softmax numerators as a K-major B operand in fp16 hi + lo parts.  The FP4-dequantised
+// query and rows are exact in fp16 (at most 6 significant bits, magnitudes 2^-10..2688), so
+// both products run as f16 x f16 with fp32 accumulation.
+// The softmax keeps, per head, a reference maximum m_ref; numerators are 2^(s - m_ref) and
+// m_ref moves only when a tile's maximum exceeds it by more than 2^10 -- then that head's
+// column of O^T (and its running sum) is rescaled in TMEM.  The output row is O / l in bf16,
+// lse = (m_ref + log2 l) * ln 2.
+#include "sm100.cuh"
+
+namespace csa2 {
+
+constexpr int kPfTS = 64;
+constexpr int kPfThreads = 256;
+constexpr float kPfRescale = 10.0f;  // log2 headroom before the reference maximum moves
+
+constexpr int kPfOffQ = 0;                     // 8 chunks x (64 rows x 128 B) = 64 KB (+8 KB overrun)
+constexpr int kPfOffK = 64 * 1024;             // 8 chunks x (64 rows x 128 B) = 64 KB
+constexpr int kPfOffPhi = 128 * 1024;          // 64 rows (heads) x 128 B (64 rows of the tile)
+constexpr int kPfOffPlo = 136 * 1024;
+constexpr int kPfOffRaw = 144 * 1024;          // 2 x (64 x 256 B codes + 64 x 32 B scales)
+constexpr int kPfRawBytes = kPfTS * 288;       // 18 KB
+constexpr int kPfOffLut = kPfOffRaw + 2 * kPfRawBytes;
+constexpr int kPfOffMisc = kPfOffLut + 1024;
+constexpr int kPfSmem = kPfOffMisc + 2048 + 1024;
+
+struct PfMisc {
+  uint64_t bar_g[2], bar_s, bar_o;
+  uint32_t tmem_base;
+  int any_rescale;
+  int slot_ok[2][kPfTS];
+  float factor[64];
+};
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  return (uint32_t)__half_as_ushort(__float2half_rn(lo)) |
+         ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+}
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  __half2 x = *reinterpret_cast<__half2 *>(&a);
+  __half2 y = *reinterpret_cast<__half2 *>(&b);
+  __half2 z = __hmul2(x, y);
+  return *reinterpret_cast<uint32_t *>(&z);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// MN-major 128B-swizzled operand spanning several 64-element MN atoms `atom_stride` bytes apart.
+__device__ __forceinline__ uint64_t desc_mn_sw128_atoms(uint32_t addr, uint32_t atom_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((atom_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset: next MN atom
+  d |= (uint64_t)(1024u >> 4) << 32;                    // stride byte offset: next 8 rows (K)
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void pf_gather(uint8_t *raw, PfMisc &ms, int buf, int tid,
+                                          const int32_t *idx_n, int slot0, int topk,
+                                          int64_t base, const uint8_t *codes, const uint8_t *sf) {
+  const int slot = slot0 + tid;
+  const int r = slot < topk ? idx_n[slot] : -1;
+  ms.slot_ok[buf][tid] = r >= 0;
+  uint8_t *c = raw + tid * 256;
+  uint8_t *s = raw + kPfTS * 256 + tid * 32;
+  if (r >= 0) {
+    const int64_t row = base + r;
+    sm100::mbar_arrive_expect_tx(&ms.bar_g[buf], 288);
+    bulk_g2s(c, codes + row * kCodeBytes, 256, &ms.bar_g[buf]);
+    bulk_g2s(s, sf + row * kSfBytes, 32, &ms.bar_g[buf]);
+  } else {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 16; ++i) reinterpret_cast<uint4 *>(c)[i] = z;
+    reinterpret_cast<uint4 *>(s)[0] = z;
+    reinterpret_cast<uint4 *>(s)[1] = z;
+    sm100::mbar_arrive(&ms.bar_g[buf]);
+  }
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
+    const uint8_t *__restrict__ q_codes, const uint8_t *__restrict__ q_sf, int H,
+    const int32_t *__restrict__ q_seq, const uint8_t *__restrict__ codes,
+    const uint8_t *__restrict__ sf, const int64_t *__restrict__ cu_ctx,
+    const int32_t *__restrict__ idx, int topk, float scale_log2e, uint16_t *__restrict__ out,
+    float *__restrict__ lse) {
+  using namespace sm100;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t *sm = smem_raw + ((1024 - (raw_u32 & 1023)) & 1023);
+  PfMisc &ms = *reinterpret_cast<PfMisc *>(sm + kPfOffMisc);
+  uint32_t *lut = reinterpret_cast<uint32_t *>(sm + kPfOffLut);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n = blockIdx.x;
+  const int64_t base = cu_ctx[q_seq[n]];
+  const int32_t *idx_n = idx + (int64_t)n * topk;
+  const int n_tiles = (topk + kPfTS - 1) / kPfTS;
+
+  if (tid == 0) {
+    mbar_init(&ms.bar_g[0], kPfTS);
+    mbar_init(&ms.bar_g[1], kPfTS);
+    mbar_init(&ms.bar_s, 1);
+    mbar_init(&ms.bar_o, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&ms.tmem_base, 512);
+    tmem_relinquish();
+  }
+  // byte of two E2M1 codes -> f16x2 of their values (exact)
+  lut[tid] = pack_f16x2(e2m1_to_float(tid & 15), e2m1_to_float(tid >> 4));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ms.tmem_base;
+  const uint32_t tS = tmem + 256;
+
+  if (tid < kPfTS) pf_gather(sm + kPfOffRaw, ms, 0, tid, idx_n, 0, topk, base, codes, sf);
+  // the FP4 query, exactly dequantised into the swizzled Q chunks
+  for (int v = tid; v < 64 * 64; v += kPfThreads) {
+    const int h = v >> 6, rest = v & 63, kc = rest >> 3, u = rest & 7;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (h < H) {
+      const int64_t qrow = (int64_t)n * H + h;
+      const int c0 = kc * 64 + u * 8;
+      const uint32_t cw = *reinterpret_cast<const uint32_t *>(q_codes + qrow * kCodeBytes + c0 / 2);
+      const float sc = e4m3_to_float(q_sf[qrow * kSfBytes + c0 / 16]);
+      const uint32_t s2 = pack_f16x2(sc, sc);
+      w.x = f16x2_mul(lut[cw & 0xFF], s2);
+      w.y = f16x2_mul(lut[(cw >> 8) & 0xFF], s2);
+      w.z = f16x2_mul(lut[(cw >> 16) & 0xFF], s2);
+      w.w = f16x2_mul(lut[cw >> 24], s2);
+    }
+    *reinterpret_cast<uint4 *>(sm + kPfOffQ + kc * 8192 + h * 128 + ((u ^ (h & 7)) << 4)) = w;
+  }
+
+  // per-head softmax state, owned by warps 0/1 (thread = head = TMEM lane of S)
+  float m_ref = -INFINITY, l_run = 0.0f;
+  bool ok = true;
+  for (int t = 0; t < n_tiles; ++t) {
+    const int buf = t & 1;
+    uint8_t *raw = sm + kPfOffRaw + buf * kPfRawBytes;
+    ok = mbar_wait(&ms.bar_g[buf], (t >> 1) & 1) && ok;
+    if (t > 0) ok = mbar_wait(&ms.bar_o, (t - 1) & 1) && ok;  // PV(t-1) done: K, P free
+    // prefetch the next tile's rows into the other raw buffer (consumed two steps ago)
+    if (t + 1 < n_tiles && tid < kPfTS)
+      pf_gather(sm + kPfOffRaw + (buf ^ 1) * kPfRawBytes, ms, buf ^ 1, tid, idx_n,
+                (t + 1) * kPfTS, topk, base, codes, sf);
+    for (int v = tid; v < kPfTS * 64; v += kPfThreads) {
+      const int j = v >> 6, rest = v & 63, kc = rest >> 3, u = rest & 7;
+      const int c0 = kc * 64 + u * 8;
+      const uint32_t cw = *reinterpret_cast<const uint32_t *>(raw + j * 256 + c0 / 2);
+      const float sc = e4m3_to_float(raw[kPfTS * 256 + j * 32 + c0 / 16]);
+      const uint32_t s2 = pack_f16x2(sc, sc);
+      uint4 w;
+      w.x = f16x2_mul(lut[cw & 0xFF], s2);
+      w.y = f16x2_mul(lut[(cw >> 8) & 0xFF], s2);
+      w.z = f16x2_mul(lut[(cw >> 16) & 0xFF], s2);
+      w.w = f16x2_mul(lut[cw >> 24], s2);
+      *reinterpret_cast<uint4 *>(sm + kPfOffK + kc * 8192 + j * 128 + ((u ^ (j & 7)) << 4)) = w;
+    }
+    if (tid == 0) ms.any_rescale = 0;
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {  // S = Qhat Khat^T
+      constexpr uint32_t idesc = idesc_f32acc(0, 0, 128, kPfTS);  // f16 x f16
+      const uint32_t qa = smem_u32(sm + kPfOffQ), ka = smem_u32(sm + kPfOffK);
+      for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_f16(tS, desc_k128_sw128(qa + kc * 8192 + 32 * ks),
+                  desc_k128_sw128(ka + kc * 8192 + 32 * ks), idesc, (kc | ks) != 0);
+      mma_commit(&ms.bar_s);
+    }
+    if (warp < 2) {  // softmax rows
+      ok = __all_sync(0xffffffffu, mbar_wait(&ms.bar_s, t & 1)) && ok;
+      tc_fence_after();
+      const int h = warp * 32 + lane;
+      float s[kPfTS];
+      const uint32_t la = tS + ((uint32_t)(warp * 32) << 16);
+      {
+        uint32_t r[kPfTS / 16][16];
+#pragma unroll
+        for (int c = 0; c < kPfTS / 16; ++c) tmem_ld16(la + 16 * c, r[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < kPfTS / 16; ++c)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) s[16 * c + i] = __uint_as_float(r[c][i]) * scale_log2e;
+      }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kPfTS; ++j)
+        if (ms.slot_ok[buf][j]) mt = fmaxf(mt, s[j]);
+      float factor = 1.0f;
+      if (mt > m_ref + kPfRescale) {  // (also true the first time: m_ref = -inf)
+        if (m_ref != -INFINITY) {
+          factor = exp2f(m_ref - mt);
+          atomicOr(&ms.any_rescale, 1);
+        }
+        l_run *= factor;
+        m_ref = mt;
+      }
+      ms.factor[h] = factor;
+      // numerators as fp16 hi + lo parts (p = hi + lo to ~2^-22): one fp16 operand alone
+      // (2^-12) is too coarse when large rows of opposite sign nearly cancel
+      uint32_t hi[kPfTS / 2], lo[kPfTS / 2];
+#pragma unroll
+      for (int j = 0; j < kPfTS; j += 2) {
+        const float p0 = ms.slot_ok[buf][j] ? exp2f(s[j] - m_ref) : 0.0f;
+        const float p1 = ms.slot_ok[buf][j + 1] ? exp2f(s[j + 1] - m_ref) : 0.0f;
+        l_run += p0 + p1;
+        const __half h0 = __float2half_rn(p0), h1 = __float2half_rn(p1);
+        hi[j / 2] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+        lo[j / 2] = pack_f16x2(p0 - __half2float(h0), p1 - __half2float(h1));
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int off = h * 128 + ((u ^ (h & 7)) << 4);
+        *reinterpret_cast<uint4 *>(sm + kPfOffPhi + off) =
+            make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
+        *reinterpret_cast<uint4 *>(sm + kPfOffPlo + off) =
+            make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (ms.any_rescale && warp < 4) {  // O^T[:, h] *= factor[h]: thread = channel lane
+      const uint32_t la = tmem + ((uint32_t)(warp * 32) << 16);
+      for (int c = 0; c < 256; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(la + c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          r[i] = __float_as_uint(__uint_as_float(r[i]) * ms.factor[(c + i) & 63]);
+        tmem_st16(la + c, r);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {  // O^T += Vhat^T (P_hi + P_lo)^T
+      constexpr uint32_t idesc_pv = idesc_f32acc(0, 0, 128, 64) | (1u << 15);  // f16, A MN-major
+      const uint32_t ka = smem_u32(sm + kPfOffK);
+      const uint32_t ph = smem_u32(sm + kPfOffPhi), pl = smem_u32(sm + kPfOffPlo);
+      for (int qb = 0; qb < 4; ++qb) {
+#pragma unroll
+        for (int ks = 0; ks < kPfTS / 16; ++ks) {
+          const uint64_t ad = desc_mn_sw128_atoms(ka + (2 * qb) * 8192 + ks * 16 * 128, 8192);
+          mma_f16(tmem + qb * 64, ad, desc_k128_sw128(ph + 32 * ks), idesc_pv,
+                  (t > 0 || ks > 0) ? 1u : 0u);
+          mma_f16(tmem + qb * 64, ad, desc_k128_sw128(pl + 32 * ks), idesc_pv, 1u);
+        }
+      }
+      mma_commit(&ms.bar_o);
+    }
+  }
+  // ---- epilogue: thread = channel lane; column 64*qb + h of O^T is channel 128*qb + lane'
+  ok = mbar_wait(&ms.bar_o, (n_tiles - 1) & 1) && ok;
+  if (warp < 2) {  // publish the final per-head state through shared memory
+    const int h = warp * 32 + lane;
+    ms.factor[h] = (l_run > 0.0f && ok) ? 1.0f / l_run : 0.0f;
+    if (h < H && lse)
+      lse[(int64_t)n * H + h] = (l_run > 0.0f && ok) ? (m_ref + log2f(l_run)) * 0.69314718055994531f
+                                                     : -INFINITY;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp < 4) {
+    const uint32_t la = tmem + ((uint32_t)(warp * 32) << 16);
+    const int cl = warp * 32 + lane;  // channel within a 128-channel block
+    for (int qb = 0; qb < 4; ++qb) {
+      for (int h0 = 0; h0 < 64; h0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(la + qb * 64 + h0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int h = h0 + i;
+          if (h < H)
+            out[((int64_t)n * H + h) * kD + qb * 128 + cl] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * ms.factor[h]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+bool attn_prefill_supported(int H) { return H <= 64 && encode_fn() != nullptr; }
+
+cudaError_t launch_attn_prefill(const uint8_t *q_codes, const uint8_t *q_sf, int T, int H,
+                                const int32_t *q_seq, const uint8_t *codes, const uint8_t *sf,
+                                const int64_t *cu_ctx, const int32_t *idx, int topk, float scale,
+                                void *out_bf16, float *lse, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  cudaError_t e = set_smem_once(attn_prefill_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+  if (e != cudaSuccess) return e;
+  attn_prefill_kernel<<<T, kPfThreads, kPfSmem, st>>>(
+      q_codes, q_sf, H, q_seq, codes, sf, cu_ctx, idx, topk, scale * 1.4426950408889634f,
+      static_cast<uint16_t *>(out_bf16), lse);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -259,7 +259,7 @@ cudaError_t launch_attn(const void *q_bf16, const uint8_t *q_codes, const uint8_
   float *l_part = m_part ? m_part + rows : nullptr;
   const size_t smem = sizeof(AttnSmem);
   static_assert(sizeof(AttnSmem) <= 227 * 1024, "shared memory");
-  cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel,
+  cudaError_t e = set_smem_once(attn_partial_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(ns, (H + kHG - 1) / kHG, nq);

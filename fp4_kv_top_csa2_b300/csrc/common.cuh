@@ -2,6 +2,7 @@
 #pragma once
 
 #include <atomic>
+#include <mutex>
 
 #include <algorithm>
 #include <cuda_bf16.h>
@@ -94,6 +95,33 @@ __device__ int g_csa2_status = 0;
 // ------------------------------------------------------------------------------------------
 namespace csa2 {
 
+// cudaFuncSetAttribute(kernel, attr, value) once per (kernel address, device) per process: the
+// value never changes for a kernel, and repeating the call costs host time on every launch.
+inline cudaError_t set_attr_once(const void *kernel, cudaFuncAttribute attr, int value) {
+  struct Entry { const void *k; int attr; uint64_t devs; };
+  static std::mutex mu;
+  static Entry table[64];
+  static int used = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry *ent = nullptr;
+  for (int i = 0; i < used; ++i)
+    if (table[i].k == kernel && table[i].attr == (int)attr) ent = &table[i];
+  if (ent && bit && (ent->devs & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, attr, value);
+  if (e != cudaSuccess) return e;
+  if (!ent && used < 64) ent = &table[used++], ent->k = kernel, ent->attr = (int)attr, ent->devs = 0;
+  if (ent) ent->devs |= bit;
+  return cudaSuccess;
+}
+template <class K>
+inline cudaError_t set_smem_once(K *kernel, cudaFuncAttribute attr, int value) {
+  return set_attr_once(reinterpret_cast<const void *>(kernel), attr, value);
+}
+
 // Process-wide count of kernels enqueued by the library (csa2_kernel_launches).
 inline std::atomic<uint64_t> g_kernel_launches{0};
 inline void note_launches(int n) { g_kernel_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -120,13 +148,22 @@ cudaError_t launch_score_cand(const void *q_idx, int dtype, const float *w, int 
 //   map != nullptr: element i is position map[n*map_stride + i/8]*8 + i%8, valid iff the block
 //                   id is >= 0 and the position is < q_vis[n].
 //   pos_vals != nullptr: the value of an element is pos_vals[n*pos_stride + position] instead.
+//   ws: workspace of topk_workspace_bytes(nq, n_elems) bytes (may be null when that is 0 or to
+//       force the one-CTA-per-query path).
 cudaError_t launch_topk(const float *vals, int64_t stride, int64_t n_elems, const int32_t *map,
                         int64_t map_stride, int unit, const int32_t *q_vis, int nq, int topk,
                         int32_t *out, cudaStream_t st, const float *pos_vals = nullptr,
-                        int64_t pos_stride = 0);
+                        int64_t pos_stride = 0, void *ws = nullptr);
+size_t topk_workspace_bytes(int nq, int64_t n_elems);
 
-// Tensor-core indexer (index_mma.cu).
-bool index_mma_supported(int nq);
+// Tensor-core indexer (index_mma.cu, index_multi.cu).
+bool index_mma_supported(int nq);   // single-query scan (nq <= 1024)
+bool cand_mma_supported();          // candidate scoring, any nq
+bool index_multi_supported(int nq, int Hi, int B);  // 32-query scan over one sequence
+cudaError_t launch_score_scan_multi(const void *q_idx, int dtype, const float *w, int nq,
+                                    const void *k_idx, int64_t k_rows, const float *k_scale,
+                                    const int32_t *q_vis, int64_t max_vis, float *bm,
+                                    int64_t bm_stride, cudaStream_t st);
 cudaError_t launch_score_scan_mma(const void *q_idx, int dtype, const float *w, int nq, int Hi,
                                   const void *k_idx, int64_t k_rows, const float *k_scale,
                                   const int64_t *cu_ctx, const int32_t *q_seq,
@@ -144,5 +181,21 @@ cudaError_t launch_attn(const void *q_bf16, const uint8_t *q_codes, const uint8_
                         const int64_t *cu_ctx, const int32_t *idx, int topk, float scale,
                         void *out_bf16, float *lse, void *workspace, cudaStream_t st);
 size_t attn_workspace_bytes(int nq, int H, int topk);
+
+// Tensor-core prefill attention (attn_prefill.cu): one CTA per query token, H <= 64.
+bool attn_prefill_supported(int H);
+cudaError_t launch_attn_prefill(const uint8_t *q_codes, const uint8_t *q_sf, int T, int H,
+                                const int32_t *q_seq, const uint8_t *codes, const uint8_t *sf,
+                                const int64_t *cu_ctx, const int32_t *idx, int topk, float scale,
+                                void *out_bf16, float *lse, cudaStream_t st);
+
+// Tensor-core decode attention (attn_mma.cu): H <= 64, one CTA per 64 selected rows.
+bool attn_mma_supported(int H, int topk);
+size_t attn_mma_workspace_bytes(int nq, int H, int topk);
+cudaError_t launch_attn_mma(const void *q_bf16, const uint8_t *q_codes, const uint8_t *q_sf,
+                            int nq, int H, const int32_t *q_seq, const uint8_t *codes,
+                            const uint8_t *sf, const int64_t *cu_ctx, const int32_t *idx,
+                            int topk, float scale, void *out_bf16, float *lse, void *workspace,
+                            cudaStream_t st);
 
 }  // namespace csa2

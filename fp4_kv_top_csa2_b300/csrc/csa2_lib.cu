@@ -3,7 +3,10 @@
 #include "kv_quant.cu"
 #include "index_score.cu"
 #include "index_mma.cu"
+#include "index_multi.cu"
 #include "topk.cu"
 #include "attn_simt.cu"
+#include "attn_mma.cu"
+#include "attn_prefill.cu"
 #include "api.cu"
 #include "noalloc.cu"

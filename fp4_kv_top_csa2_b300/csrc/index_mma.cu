@@ -328,7 +328,7 @@ template <int DT, int MODE>
 static cudaError_t launch_index_mma_t(const CUtensorMap &km, const CUtensorMap &qm,
                                       const IdxParams &p, int grid, cudaStream_t st) {
   const size_t smem = sizeof(IdxSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(index_mma_kernel<DT, MODE>,
+  cudaError_t e = set_smem_once(index_mma_kernel<DT, MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   index_mma_kernel<DT, MODE><<<grid, kIdxThreads, smem, st>>>(km, qm, p);
@@ -337,6 +337,7 @@ static cudaError_t launch_index_mma_t(const CUtensorMap &km, const CUtensorMap &
 }
 
 bool index_mma_supported(int nq) { return nq <= kMaxScanQueries && encode_fn() != nullptr; }
+bool cand_mma_supported() { return encode_fn() != nullptr; }
 
 // Full-mode scan on tensor cores.  scores may be null (block maxima only).
 cudaError_t launch_score_scan_mma(const void *q_idx, int dtype, const float *w, int nq, int Hi,

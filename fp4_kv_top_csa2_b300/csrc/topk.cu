@@ -5,42 +5,76 @@
 // pool ("selects blocks by their maximum index score", "DeepSeek V4.1-Flash", aiwiki.ai, section
 // "Compressed Sparse Attention 2") and Reindex selection.
 //
-// Algorithm: radix select on order-preserving 32-bit keys, most significant digit first
-// (11 + 11 + 10 bits), each digit found from a shared-memory histogram and a block-wide suffix
-// scan, stopping early once a whole bin is taken.  That yields a threshold key T and the number
-// need_eq of elements equal to T that are taken (the lowest positions among them).  A final
-// ordered pass writes the selected elements in index order: every warp owns one contiguous
-// segment, counts its selections with ballots, one block-wide scan gives each warp its output
-// offset, and a second sweep emits positions in order -- ascending output without a sort.
-// The scores live in L2; each pass keeps 16 independent loads in flight per thread.
+// Keys are order-preserving 32-bit images of the scores (key 0 = not a candidate).  The k-th
+// largest key T is built three bits per round: each round counts, in one pass, how many keys
+// are >= each of the 7 possible extensions of the current prefix, and keeps the largest one
+// with at least k keys (11 rounds, block-wide counts, no atomics).  need_eq = k - #(keys > T)
+// equal keys are taken, the lowest positions first.  The output is an ordered emission: every
+// warp owns a contiguous segment, counts its selections with ballots, one scan gives each warp
+// its offset, and a second sweep writes positions in index order (no sort).
+//
+// Where the data lives:
+//   * n <= 16,384 elements: copied once into shared memory (key, position), then everything
+//     runs there.
+//   * larger n: a strided sample of 8,192 keys gives a threshold T_est expected to keep about
+//     1.6 K elements.  One sweep appends every candidate with key >= T_est to its warp's 512
+//     shared-memory slots (index order), the slots are compacted, and the selection finishes
+//     there.  The true Top-K (ties included) is inside that set whenever it holds at least K
+//     elements; if the estimate misses (fewer than K kept, or a warp's slots overflow) the
+//     selection runs over global memory instead.
+// The three ways an element can be addressed (block maxima by index; candidate slots through
+// a block list with slot-indexed or position-indexed scores) are separate kernel instances, so
+// every global load is straight-line code with clamped indices and validity as a mask.
 #include "common.cuh"
 
 namespace csa2 {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kUnroll = 16;
+constexpr int kUnroll = 8;       // loads in flight per thread (key + position)
+constexpr int kSmemCap = 16384;  // elements held in shared memory
+constexpr int kWarpCap = kSmemCap / kTopkWarps;  // per-warp staging slots (512)
+constexpr int kSample = 8192;
+constexpr size_t kTopkSmem = (size_t)kSmemCap * 8;
 
-struct ElemView {
-  const float *vals;
-  const float *pos_vals;  // non-null: the value of an element is pos_vals[its position]
-  const int32_t *map;     // nullptr: identity
-  int64_t n_elems;
-  int64_t limit;          // identity: valid iff i < limit; map: valid iff pos < limit
-  __device__ __forceinline__ bool get(int64_t i, uint32_t &key, int32_t &pos) const {
-    if (i >= n_elems) return false;
-    int64_t p;
-    if (map) {
-      const int blk = __ldg(map + (i >> 3));
-      p = (int64_t)blk * kBlock + (i & 7);
-      if (blk < 0 || p >= limit) return false;
+enum TopkMode { kById = 0, kMapSlot = 1, kMapPos = 2 };
+
+template <int MODE>
+struct ElemView {  // elements in global memory
+  const float *vals;   // kById / kMapSlot: value of element i; kMapPos: value of position p
+  const int32_t *map;  // kMapSlot / kMapPos: element i -> position map[i/8]*8 + i%8
+  int64_t n_elems;     // >= 1
+  int64_t limit;       // kById: valid iff i < limit; mapped: valid iff position < limit
+  int64_t val_len;     // readable length of vals (>= 1)
+  __device__ __forceinline__ uint32_t get(int64_t i, int32_t &pos) const {
+    const bool in = i < n_elems;
+    const int64_t ic = in ? i : n_elems - 1;
+    int64_t p, vi;
+    bool ok;
+    if (MODE == kById) {
+      p = ic;
+      vi = ic;
+      ok = in && ic < limit;
     } else {
-      p = i;
-      if (i >= limit) return false;
+      const int blk = __ldg(map + (ic >> 3));
+      p = (int64_t)(blk < 0 ? 0 : blk) * kBlock + (ic & 7);
+      ok = in && blk >= 0 && p < limit;
+      vi = MODE == kMapSlot ? ic : (p < val_len ? p : val_len - 1);
     }
+    const float v = __ldg(vals + vi);
     pos = (int32_t)p;
-    key = float_key(pos_vals ? pos_vals[p] : vals[i]);
-    return true;
+    return ok ? float_key(v) : 0u;
+  }
+};
+
+struct SmemView {  // elements in shared memory; key 0 marks a non-candidate
+  const uint32_t *key;
+  const int32_t *pos;
+  int64_t n_elems;
+  __device__ __forceinline__ uint32_t get(int64_t i, int32_t &p) const {
+    const bool in = i < n_elems;
+    p = pos[in ? i : 0];
+    return in ? key[i] : 0u;
   }
 };
 
@@ -54,170 +88,115 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   return v;
 }
 
-// Block-wide exclusive scan of one uint32 per thread; also returns the block total.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *warp_tot,
-                                                         uint32_t &total) {
+struct TopkShared {
+  uint32_t red[2][8][kTopkWarps];
+  uint32_t seg_a[kTopkWarps], seg_b[kTopkWarps];
+  uint32_t s_a, s_b;
+};
+
+// Counts of candidates with key >= cand[j] (j < NT) over the view, block-wide.
+template <int NT, class View>
+__device__ void count_ge_n(const View &ev, int64_t n_elems, const uint32_t (&cand)[NT],
+                           uint32_t (&cnt)[NT], TopkShared &sh, int &parity) {
+  uint32_t c[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) c[j] = 0;
+  for (int64_t base = 0; base < n_elems; base += (int64_t)kTopkThreads * kUnroll) {
+    uint32_t keys[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      int32_t pos;
+      keys[u] = ev.get(base + (int64_t)u * kTopkThreads + threadIdx.x, pos);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+      for (int j = 0; j < NT; ++j) c[j] += keys[u] >= cand[j];
+  }
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const uint32_t inc = warp_incl_scan(v);
-  if (lane == 31) warp_tot[wid] = inc;
-  __syncthreads();
-  if (wid == 0) {
-    const uint32_t t = warp_tot[lane];
-    const uint32_t ti = warp_incl_scan(t);
-    warp_tot[lane] = ti - t;  // exclusive warp offsets
-    if (lane == 31) warp_tot[32] = ti;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    c[j] = __reduce_add_sync(0xffffffffu, c[j]);
+    if (lane == 0) sh.red[parity][j][wid] = c[j];
   }
   __syncthreads();
-  const uint32_t res = warp_tot[wid] + inc - v;
-  total = warp_tot[32];
-  __syncthreads();
-  return res;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) cnt[j] = __reduce_add_sync(0xffffffffu, sh.red[parity][j][lane]);
+  parity ^= 1;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(
-    const float *__restrict__ vals, int64_t stride, const float *__restrict__ pos_vals,
-    int64_t pos_stride, int64_t n_elems, const int32_t *__restrict__ map, int64_t map_stride,
-    int unit, const int32_t *__restrict__ q_vis, int topk, int32_t *__restrict__ out) {
-  __shared__ uint32_t hist[2048];
-  __shared__ uint32_t warp_tot[33];
-  __shared__ uint32_t seg_gt[kTopkWarps], seg_eq[kTopkWarps];
-  __shared__ uint32_t s_digit, s_above, s_nvalid;
+// The k-th largest key (1 <= k <= number of candidates), three bits per round.
+template <class View>
+__device__ uint32_t kth_largest(const View &ev, int64_t n_elems, uint32_t k, TopkShared &sh,
+                                int &parity) {
+  uint32_t T = 0;
+  int b = 32;
+  while (b > 0) {
+    const int w = b >= 3 ? 3 : b;
+    b -= w;
+    uint32_t cand[7], cnt[7];
+#pragma unroll
+    for (int j = 0; j < 7; ++j)  // candidates beyond this round's width never qualify
+      cand[j] = (j + 1 < (1 << w)) ? (T | ((uint32_t)(j + 1) << b)) : 0xFFFFFFFFu;
+    count_ge_n<7>(ev, n_elems, cand, cnt, sh, parity);
+    uint32_t best = 0;
+#pragma unroll
+    for (int j = 0; j < 7; ++j)
+      if (j + 1 < (1 << w) && cnt[j] >= k) best = j + 1;
+    T |= best << b;
+  }
+  return T;
+}
 
-  const int n = blockIdx.x;
+// Ordered emission of the elements with key > T, plus the first need_eq with key == T.
+template <class View>
+__device__ void ordered_emit(const View &ev, int64_t n_elems, uint32_t T, uint32_t need_eq,
+                             TopkShared &sh, int32_t *o) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int64_t V = q_vis[n];
-  ElemView ev;
-  ev.vals = vals ? vals + (int64_t)n * stride : nullptr;
-  ev.pos_vals = pos_vals ? pos_vals + (int64_t)n * pos_stride : nullptr;
-  ev.map = map ? map + (int64_t)n * map_stride : nullptr;
-  ev.n_elems = n_elems;
-  ev.limit = map ? V : (V + unit - 1) / unit;
-  int32_t *o = out + (int64_t)n * topk;
-
-  uint32_t prefix = 0;  // digits fixed so far
-  int pshift = 32;      // keys with (key >> pshift) == prefix are still in play
-  uint32_t rem = 0;     // how many still to take among them
-  uint32_t T = 0, need_eq = 0;
-  bool done = false;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-
-  if (tid == 0) s_nvalid = 0;
-  for (int pass = 0; pass < 3 && !done; ++pass) {
-    const int shift = shifts[pass], nb = 1 << widths[pass];
-    for (int i = tid; i < nb; i += kTopkThreads) hist[i] = 0;
-    __syncthreads();
-    uint32_t local_valid = 0;
-    for (int64_t base = 0; base < n_elems; base += (int64_t)kTopkThreads * kUnroll) {
-      uint32_t keys[kUnroll];
-      bool ok[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        int32_t pos;
-        ok[u] = ev.get(base + (int64_t)u * kTopkThreads + tid, keys[u], pos);
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if (!ok[u]) continue;
-        ++local_valid;
-        if (pshift == 32 || (keys[u] >> pshift) == prefix)
-          atomicAdd(&hist[(keys[u] >> shift) & (nb - 1)], 1u);
-      }
-    }
-    if (pass == 0) {
-      local_valid = __reduce_add_sync(0xffffffffu, local_valid);
-      if (lane == 0) atomicAdd(&s_nvalid, local_valid);
-    }
-    __syncthreads();
-    if (pass == 0) {
-      rem = min((uint32_t)topk, s_nvalid);
-      if (rem == 0) break;
-    }
-    // suffix scan: thread i owns bins nb-1-2i and nb-2-2i (descending digit order)
-    uint32_t c0 = 0, c1 = 0;
-    const int b0 = nb - 1 - 2 * tid, b1 = b0 - 1;
-    if (b0 >= 0) c0 = hist[b0];
-    if (b1 >= 0) c1 = hist[b1];
-    uint32_t tot;
-    const uint32_t before = block_exclusive_scan(c0 + c1, warp_tot, tot);
-    // the digit where the count from the top first reaches rem
-    if (b0 >= 0 && before < rem && before + c0 >= rem) {
-      s_digit = b0;
-      s_above = before;
-    } else if (b1 >= 0 && before + c0 < rem && before + c0 + c1 >= rem) {
-      s_digit = b1;
-      s_above = before + c0;
-    }
-    __syncthreads();
-    const uint32_t digit = s_digit;
-    const uint32_t cnt = hist[digit];
-    rem -= s_above;
-    prefix = (pshift == 32) ? digit : ((prefix << widths[pass]) | digit);
-    pshift = shift;
-    if (cnt == rem || pass == 2) {
-      if (cnt == rem) {  // every key of this bin is taken: select key >= prefix << shift
-        T = (prefix << shift) - 1u;  // prefix << shift >= 0x00800000 for finite values
-        need_eq = 0;
-      } else {
-        T = prefix;
-        need_eq = rem;
-      }
-      done = true;
-    }
-    __syncthreads();
-  }
-
-  if (!done) {  // no valid element
-    for (int i = tid; i < topk; i += kTopkThreads) o[i] = -1;
-    return;
-  }
-  const uint32_t k_eff = min((uint32_t)topk, s_nvalid);
-
-  // ordered emission: warp w owns elements [w*seg, (w+1)*seg)
   const int64_t seg = ((n_elems + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;
   const int64_t w0 = (int64_t)wid * seg, w1 = min(n_elems, w0 + seg);
   const uint32_t lt_mask = (1u << lane) - 1u;
   uint32_t ngt = 0, neq = 0;
   for (int64_t b = w0; b < w1; b += 32 * kUnroll) {
     uint32_t keys[kUnroll];
-    bool ok[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t i = b + 32 * u + lane;
       int32_t pos;
-      ok[u] = i < w1 && ev.get(i, keys[u], pos);
+      keys[u] = ev.get(i, pos);
+      if (i >= w1) keys[u] = 0u;
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      ngt += __popc(__ballot_sync(0xffffffffu, ok[u] && keys[u] > T));
-      neq += __popc(__ballot_sync(0xffffffffu, ok[u] && keys[u] == T));
+      ngt += __popc(__ballot_sync(0xffffffffu, keys[u] != 0u && keys[u] > T));
+      neq += __popc(__ballot_sync(0xffffffffu, keys[u] != 0u && keys[u] == T));
     }
   }
   if (lane == 0) {
-    seg_gt[wid] = ngt;
-    seg_eq[wid] = neq;
+    sh.seg_a[wid] = ngt;
+    sh.seg_b[wid] = neq;
   }
   __syncthreads();
   if (wid == 0) {
-    const uint32_t g = seg_gt[lane], e = seg_eq[lane];
+    const uint32_t g = sh.seg_a[lane], e = sh.seg_b[lane];
     const uint32_t gi = warp_incl_scan(g), ei = warp_incl_scan(e);
-    seg_gt[lane] = gi - g;
-    seg_eq[lane] = ei - e;
+    sh.seg_a[lane] = gi - g;
+    sh.seg_b[lane] = ei - e;
   }
   __syncthreads();
-  uint32_t gt_r = seg_gt[wid], eq_r = seg_eq[wid];
+  uint32_t gt_r = sh.seg_a[wid], eq_r = sh.seg_b[wid];
   for (int64_t b = w0; b < w1; b += 32 * kUnroll) {
     uint32_t keys[kUnroll];
     int32_t poss[kUnroll];
-    bool ok[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t i = b + 32 * u + lane;
-      ok[u] = i < w1 && ev.get(i, keys[u], poss[u]);
+      keys[u] = ev.get(i, poss[u]);
+      if (i >= w1) keys[u] = 0u;
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const bool gt = ok[u] && keys[u] > T, eq = ok[u] && keys[u] == T;
+      const bool gt = keys[u] != 0u && keys[u] > T, eq = keys[u] != 0u && keys[u] == T;
       const uint32_t bgt = __ballot_sync(0xffffffffu, gt), beq = __ballot_sync(0xffffffffu, eq);
       const uint32_t my_gt = gt_r + __popc(bgt & lt_mask), my_eq = eq_r + __popc(beq & lt_mask);
       if (gt || (eq && my_eq < need_eq)) o[my_gt + min(my_eq, need_eq)] = poss[u];
@@ -225,16 +204,465 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
       eq_r += __popc(beq);
     }
   }
-  for (int i = k_eff + tid; i < topk; i += kTopkThreads) o[i] = -1;
+}
+
+template <class View>
+__device__ void select_and_emit(const View &ev, int64_t n_elems, int topk, TopkShared &sh,
+                                int &parity, int32_t *o) {
+  uint32_t cand1[1] = {1u}, nv[1];
+  count_ge_n<1>(ev, n_elems, cand1, nv, sh, parity);
+  const uint32_t k_eff = min((uint32_t)topk, nv[0]);
+  if (k_eff > 0) {
+    const uint32_t T = kth_largest(ev, n_elems, k_eff, sh, parity);
+    uint32_t n_gt = 0;
+    if (T != 0xFFFFFFFFu) {
+      uint32_t c[1] = {T + 1u}, r[1];
+      count_ge_n<1>(ev, n_elems, c, r, sh, parity);
+      n_gt = r[0];
+    }
+    ordered_emit(ev, n_elems, T, k_eff - n_gt, sh, o);
+  }
+  for (int i = (int)k_eff + threadIdx.x; i < topk; i += kTopkThreads) o[i] = -1;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(
+    const float *__restrict__ vals, int64_t stride, int64_t n_elems,
+    const int32_t *__restrict__ map, int64_t map_stride, int unit,
+    const int32_t *__restrict__ q_vis, int topk, int32_t *__restrict__ out) {
+  extern __shared__ __align__(16) uint8_t topk_smem[];
+  uint32_t *skey = reinterpret_cast<uint32_t *>(topk_smem);
+  int32_t *spos = reinterpret_cast<int32_t *>(topk_smem + (size_t)kSmemCap * 4);
+  __shared__ TopkShared sh;
+  int parity = 0;
+
+  const int n = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int32_t *o = out + (int64_t)n * topk;
+  if (n_elems <= 0) {
+    for (int i = tid; i < topk; i += kTopkThreads) o[i] = -1;
+    return;
+  }
+  const int64_t V = q_vis[n];
+  ElemView<MODE> ev;
+  ev.vals = vals + (int64_t)n * stride;
+  ev.val_len = stride > 0 ? stride : 1;
+  ev.map = map ? map + (int64_t)n * map_stride : nullptr;
+  ev.n_elems = n_elems;
+  ev.limit = MODE == kById ? (V + unit - 1) / unit : V;
+
+  if (n_elems <= kSmemCap) {
+    // ---- small: copy everything (non-candidates -> key 0), keep index order
+    for (int64_t base = 0; base < n_elems; base += (int64_t)kTopkThreads * kUnroll) {
+      uint32_t k[kUnroll];
+      int32_t p[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) k[u] = ev.get(base + (int64_t)u * kTopkThreads + tid, p[u]);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = base + (int64_t)u * kTopkThreads + tid;
+        if (i < n_elems) {
+          skey[i] = k[u];
+          spos[i] = p[u];
+        }
+      }
+    }
+    __syncthreads();
+    SmemView sv{skey, spos, n_elems};
+    select_and_emit(sv, n_elems, topk, sh, parity, o);
+    return;
+  }
+
+  // ---- large: sample -> threshold estimate
+  const int64_t step = n_elems / kSample;  // >= 2
+  {
+    uint32_t k[kSample / kTopkThreads];
+#pragma unroll
+    for (int u = 0; u < kSample / kTopkThreads; ++u) {
+      int32_t p;
+      k[u] = ev.get((int64_t)(u * kTopkThreads + tid) * step, p);
+    }
+#pragma unroll
+    for (int u = 0; u < kSample / kTopkThreads; ++u) {
+      skey[u * kTopkThreads + tid] = k[u];
+      spos[u * kTopkThreads + tid] = 0;
+    }
+  }
+  __syncthreads();
+  SmemView smp{skey, spos, kSample};
+  const int64_t r_want = (int64_t)topk * kSample * 8 / (n_elems * 5) + 16;  // ~1.6 K kept
+  const uint32_t r = (uint32_t)(r_want < kSample ? r_want : kSample);
+  uint32_t t_est = 1u;  // every candidate key is >= 1
+  {
+    uint32_t c1[1] = {1u}, nvs[1];
+    count_ge_n<1>(smp, kSample, c1, nvs, sh, parity);
+    if (nvs[0] >= r) t_est = kth_largest(smp, kSample, r, sh, parity);
+  }
+  __syncthreads();  // the sample is no longer needed
+
+  // ---- one sweep: each warp appends its candidates >= t_est (index order) to its slots
+  const int64_t seg = ((n_elems + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;
+  const int64_t w0 = (int64_t)wid * seg, w1 = min(n_elems, w0 + seg);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint32_t nval = 0, wr = 0;
+  for (int64_t b = w0; b < w1; b += 32 * kUnroll) {
+    uint32_t keys[kUnroll];
+    int32_t poss[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = b + 32 * u + lane;
+      keys[u] = ev.get(i, poss[u]);
+      if (i >= w1) keys[u] = 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      nval += keys[u] != 0u;
+      const bool take = keys[u] >= t_est;  // t_est >= 1 excludes non-candidates
+      const uint32_t bt = __ballot_sync(0xffffffffu, take);
+      const uint32_t slot = wr + __popc(bt & lt_mask);
+      if (take && slot < (uint32_t)kWarpCap) {
+        skey[wid * kWarpCap + slot] = keys[u];
+        spos[wid * kWarpCap + slot] = poss[u];
+      }
+      wr += __popc(bt);
+    }
+  }
+  nval = __reduce_add_sync(0xffffffffu, nval);
+  if (lane == 0) {
+    sh.seg_a[wid] = nval;
+    sh.seg_b[wid] = wr;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    const uint32_t a = sh.seg_a[lane], b = sh.seg_b[lane];
+    const uint32_t ai = warp_incl_scan(a), bi = warp_incl_scan(b);
+    const uint32_t over = __ballot_sync(0xffffffffu, b > (uint32_t)kWarpCap);
+    sh.seg_b[lane] = bi - b;  // exclusive offsets of each warp's kept run
+    if (lane == 31) {
+      sh.s_a = ai;                              // candidates
+      sh.s_b = over ? (bi | 0x80000000u) : bi;  // kept (+ overflow flag)
+    }
+  }
+  __syncthreads();
+  const uint32_t total_valid = sh.s_a, kept = sh.s_b & 0x7FFFFFFFu;
+  const bool overflow = (sh.s_b & 0x80000000u) != 0u;
+  const uint32_t k_eff = min((uint32_t)topk, total_valid);
+  if (overflow || kept < k_eff) {  // the estimate missed: select over global memory
+    select_and_emit(ev, n_elems, topk, sh, parity, o);
+    return;
+  }
+  // compact the warp runs into one index-ordered array (read everything, then write)
+  {
+    const uint32_t my_cnt = wr, my_off = sh.seg_b[wid];
+    uint32_t kk[kWarpCap / 32];
+    int32_t pp[kWarpCap / 32];
+#pragma unroll
+    for (int e = 0; e < kWarpCap / 32; ++e) {
+      const uint32_t s = e * 32 + lane;
+      kk[e] = s < my_cnt ? skey[wid * kWarpCap + s] : 0u;
+      pp[e] = s < my_cnt ? spos[wid * kWarpCap + s] : 0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < kWarpCap / 32; ++e) {
+      const uint32_t s = e * 32 + lane;
+      if (s < my_cnt) {
+        skey[my_off + s] = kk[e];
+        spos[my_off + s] = pp[e];
+      }
+    }
+  }
+  __syncthreads();
+  SmemView sv{skey, spos, (int64_t)kept};
+  select_and_emit(sv, kept, topk, sh, parity, o);
+}
+
+// ------------------------------------------------------------------------------------------
+// Few queries over many elements: spread the sweep over many SMs.
+//   topk_filter_kernel  grid (chunks of 4096 elements, queries): every CTA derives the same
+//                       threshold T_est from the same strided sample of 1024 keys, then writes
+//                       its chunk's candidates with key >= T_est, in index order, to the
+//                       chunk's workspace slots, with the chunk's kept and candidate counts.
+//   topk_select_kernel  one CTA per query: gathers the kept elements of all chunks (index order)
+//                       into shared memory and selects there; if the estimate kept fewer than
+//                       K, or more than fit, it selects over global memory instead.
+// ------------------------------------------------------------------------------------------
+constexpr int kTkChunk = 4096;
+constexpr int kFilterThreads = 256;
+constexpr int kFilterSample = 1024;
+
+struct ChunkWs {  // per query: [n_chunks][kTkChunk] keys, positions, then [n_chunks] counts
+  uint32_t *keys;
+  int32_t *pos;
+  uint32_t *kept;
+  uint32_t *valid;
+};
+
+__device__ __forceinline__ ChunkWs chunk_ws(void *ws, int n, int n_chunks) {
+  const size_t per_q = (size_t)n_chunks * kTkChunk * 8 + (size_t)n_chunks * 8;
+  char *b = static_cast<char *>(ws) + (size_t)n * per_q;
+  ChunkWs c;
+  c.keys = reinterpret_cast<uint32_t *>(b);
+  c.pos = reinterpret_cast<int32_t *>(b + (size_t)n_chunks * kTkChunk * 4);
+  c.kept = reinterpret_cast<uint32_t *>(b + (size_t)n_chunks * kTkChunk * 8);
+  c.valid = c.kept + n_chunks;
+  return c;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kFilterThreads) topk_filter_kernel(
+    const float *__restrict__ vals, int64_t stride, int64_t n_elems,
+    const int32_t *__restrict__ map, int64_t map_stride, int unit,
+    const int32_t *__restrict__ q_vis, int topk, void *ws) {
+  __shared__ uint32_t ks[kFilterSample];
+  __shared__ uint32_t red[8][kFilterThreads / 32];
+  __shared__ uint32_t wcnt[kFilterThreads / 32];
+  const int c = blockIdx.x, n = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int n_chunks = gridDim.x;
+  const int64_t V = q_vis[n];
+  ElemView<MODE> ev;
+  ev.vals = vals + (int64_t)n * stride;
+  ev.val_len = stride > 0 ? stride : 1;
+  ev.map = map ? map + (int64_t)n * map_stride : nullptr;
+  ev.n_elems = n_elems;
+  ev.limit = MODE == kById ? (V + unit - 1) / unit : V;
+  // the shared threshold estimate: r-th largest of a strided sample of the whole array
+  const int64_t step = n_elems / kFilterSample;  // >= 2 (n_elems > 2 * kFilterSample)
+#pragma unroll
+  for (int u = 0; u < kFilterSample / kFilterThreads; ++u) {
+    int32_t p;
+    ks[u * kFilterThreads + tid] = ev.get((int64_t)(u * kFilterThreads + tid) * step, p);
+  }
+  __syncthreads();
+  const int64_t r_want = (int64_t)topk * kFilterSample * 8 / (n_elems * 5) + 8;
+  const uint32_t r = (uint32_t)(r_want < kFilterSample ? r_want : kFilterSample);
+  uint32_t my[kFilterSample / kFilterThreads];
+#pragma unroll
+  for (int u = 0; u < kFilterSample / kFilterThreads; ++u) my[u] = ks[u * kFilterThreads + tid];
+  auto block_counts = [&](const uint32_t (&cand)[7], uint32_t (&cnt)[7], int par) {
+    uint32_t cc[7];
+#pragma unroll
+    for (int j = 0; j < 7; ++j) {
+      cc[j] = 0;
+#pragma unroll
+      for (int u = 0; u < kFilterSample / kFilterThreads; ++u) cc[j] += my[u] >= cand[j];
+      cc[j] = __reduce_add_sync(0xffffffffu, cc[j]);
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int j = 0; j < 7; ++j) red[j][wid] = cc[j];
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 7; ++j) {
+      uint32_t t = 0;
+#pragma unroll
+      for (int w = 0; w < kFilterThreads / 32; ++w) t += red[j][w];
+      cnt[j] = t;
+    }
+    __syncthreads();
+    (void)par;
+  };
+  uint32_t t_est = 1u;
+  {
+    uint32_t cand[7], cnt[7];
+#pragma unroll
+    for (int j = 0; j < 7; ++j) cand[j] = j == 0 ? 1u : 0xFFFFFFFFu;
+    block_counts(cand, cnt, 0);
+    if (cnt[0] >= r) {
+      uint32_t T = 0;
+      int b = 32;
+      while (b > 0) {
+        const int w = b >= 3 ? 3 : b;
+        b -= w;
+#pragma unroll
+        for (int j = 0; j < 7; ++j)
+          cand[j] = (j + 1 < (1 << w)) ? (T | ((uint32_t)(j + 1) << b)) : 0xFFFFFFFFu;
+        block_counts(cand, cnt, 0);
+        uint32_t best = 0;
+#pragma unroll
+        for (int j = 0; j < 7; ++j)
+          if (j + 1 < (1 << w) && cnt[j] >= r) best = j + 1;
+        T |= best << b;
+      }
+      t_est = T;
+    }
+  }
+  // this chunk: warp w owns elements [w*512, w*512+512) of it, 16 per lane, all loads in flight
+  const int64_t c0 = (int64_t)c * kTkChunk + (int64_t)wid * (kTkChunk / 8);
+  constexpr int kPer = kTkChunk / kFilterThreads;  // 16
+  uint32_t keys[kPer];
+  int32_t poss[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) keys[u] = ev.get(c0 + 32 * u + lane, poss[u]);
+  uint32_t nval = 0, nkeep = 0;
+  uint32_t take_mask[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    nval += keys[u] != 0u;
+    take_mask[u] = __ballot_sync(0xffffffffu, keys[u] >= t_est);
+    nkeep += __popc(take_mask[u]);
+  }
+  nval = __reduce_add_sync(0xffffffffu, nval);
+  if (lane == 0) {
+    wcnt[wid] = nkeep;
+    red[0][wid] = nval;
+  }
+  __syncthreads();
+  uint32_t off = 0, tot_keep = 0, tot_val = 0;
+#pragma unroll
+  for (int w = 0; w < kFilterThreads / 32; ++w) {
+    off += (w < wid) ? wcnt[w] : 0u;
+    tot_keep += wcnt[w];
+    tot_val += red[0][w];
+  }
+  ChunkWs cw = chunk_ws(ws, n, n_chunks);
+  uint32_t *okeys = cw.keys + (size_t)c * kTkChunk;
+  int32_t *opos = cw.pos + (size_t)c * kTkChunk;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    if (keys[u] >= t_est) {
+      const uint32_t slot = off + __popc(take_mask[u] & lt_mask);
+      okeys[slot] = keys[u];
+      opos[slot] = poss[u];
+    }
+    off += __popc(take_mask[u]);
+  }
+  if (tid == 0) {
+    cw.kept[c] = tot_keep;
+    cw.valid[c] = tot_val;
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
+    const float *__restrict__ vals, int64_t stride, int64_t n_elems,
+    const int32_t *__restrict__ map, int64_t map_stride, int unit,
+    const int32_t *__restrict__ q_vis, int topk, int32_t *__restrict__ out, const void *ws,
+    int n_chunks) {
+  extern __shared__ __align__(16) uint8_t topk_smem[];
+  uint32_t *skey = reinterpret_cast<uint32_t *>(topk_smem);
+  int32_t *spos = reinterpret_cast<int32_t *>(topk_smem + (size_t)kSmemCap * 4);
+  __shared__ TopkShared sh;
+  __shared__ uint32_t coff[1025];
+  int parity = 0;
+  const int n = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int32_t *o = out + (int64_t)n * topk;
+  ChunkWs cw = chunk_ws(const_cast<void *>(ws), n, n_chunks);
+  // chunk offsets (n_chunks <= 1024): block-wide exclusive scan of the kept counts
+  const uint32_t kc = tid < n_chunks ? cw.kept[tid] : 0u;
+  const uint32_t vc = tid < n_chunks ? cw.valid[tid] : 0u;
+  const uint32_t inc = warp_incl_scan(kc);
+  const uint32_t vtot_w = __reduce_add_sync(0xffffffffu, vc);
+  if (lane == 31) sh.seg_a[wid] = inc;
+  if (lane == 0) sh.seg_b[wid] = vtot_w;
+  __syncthreads();
+  if (wid == 0) {
+    const uint32_t a = sh.seg_a[lane];
+    const uint32_t ai = warp_incl_scan(a);
+    const uint32_t vt = __reduce_add_sync(0xffffffffu, sh.seg_b[lane]);
+    sh.seg_a[lane] = ai - a;
+    if (lane == 31) {
+      sh.s_a = ai;  // kept
+      sh.s_b = vt;  // candidates
+    }
+  }
+  __syncthreads();
+  if (tid < n_chunks) coff[tid] = sh.seg_a[wid] + inc - kc;
+  const uint32_t kept = sh.s_a, total_valid = sh.s_b;
+  const uint32_t k_eff = min((uint32_t)topk, total_valid);
+  __syncthreads();
+  if (kept >= k_eff && kept <= (uint32_t)kSmemCap) {
+    for (int c = wid; c < n_chunks; c += kTopkWarps) {
+      const uint32_t cnt = cw.kept[c], base = coff[c];
+      for (uint32_t i = lane; i < cnt; i += 32) {
+        skey[base + i] = cw.keys[(size_t)c * kTkChunk + i];
+        spos[base + i] = cw.pos[(size_t)c * kTkChunk + i];
+      }
+    }
+    __syncthreads();
+    SmemView sv{skey, spos, (int64_t)kept};
+    select_and_emit(sv, kept, topk, sh, parity, o);
+    return;
+  }
+  const int64_t V = q_vis[n];  // the estimate missed: select over global memory
+  ElemView<MODE> ev;
+  ev.vals = vals + (int64_t)n * stride;
+  ev.val_len = stride > 0 ? stride : 1;
+  ev.map = map ? map + (int64_t)n * map_stride : nullptr;
+  ev.n_elems = n_elems;
+  ev.limit = MODE == kById ? (V + unit - 1) / unit : V;
+  select_and_emit(ev, n_elems, topk, sh, parity, o);
+}
+
+// The chunked two-kernel path serves few queries over many elements.
+static bool topk_use_chunks(int nq, int64_t n_elems) {
+  return nq <= 64 && n_elems > 2 * kFilterSample && (n_elems + kTkChunk - 1) / kTkChunk <= 1024;
+}
+
+size_t topk_workspace_bytes(int nq, int64_t n_elems) {
+  if (!topk_use_chunks(nq, n_elems)) return 0;
+  const size_t n_chunks = (size_t)((n_elems + kTkChunk - 1) / kTkChunk);
+  return (size_t)nq * (n_chunks * kTkChunk * 8 + n_chunks * 8);
+}
+
+template <int MODE>
+static cudaError_t launch_topk_chunked(const float *vals, int64_t stride, int64_t n_elems,
+                                       const int32_t *map, int64_t map_stride, int unit,
+                                       const int32_t *q_vis, int nq, int topk, int32_t *out,
+                                       void *ws, cudaStream_t st) {
+  const int n_chunks = (int)((n_elems + kTkChunk - 1) / kTkChunk);
+  topk_filter_kernel<MODE><<<dim3(n_chunks, nq), kFilterThreads, 0, st>>>(
+      vals, stride, n_elems, map, map_stride, unit, q_vis, topk, ws);
+  note_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = set_smem_once(topk_select_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                    (int)kTopkSmem);
+  if (e != cudaSuccess) return e;
+  topk_select_kernel<MODE><<<nq, kTopkThreads, kTopkSmem, st>>>(
+      vals, stride, n_elems, map, map_stride, unit, q_vis, topk, out, ws, n_chunks);
+  note_launches(1);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const float *vals, int64_t stride, int64_t n_elems, const int32_t *map,
                         int64_t map_stride, int unit, const int32_t *q_vis, int nq, int topk,
                         int32_t *out, cudaStream_t st, const float *pos_vals,
-                        int64_t pos_stride) {
+                        int64_t pos_stride, void *ws) {
   if (nq == 0) return cudaSuccess;
-  topk_kernel<<<nq, kTopkThreads, 0, st>>>(vals, stride, pos_vals, pos_stride, n_elems, map,
-                                           map_stride, unit, q_vis, topk, out);
+  if (ws && topk_use_chunks(nq, n_elems)) {
+    if (!map)
+      return launch_topk_chunked<kById>(vals, stride, n_elems, nullptr, 0, unit, q_vis, nq, topk,
+                                        out, ws, st);
+    if (pos_vals)
+      return launch_topk_chunked<kMapPos>(pos_vals, pos_stride, n_elems, map, map_stride, unit,
+                                          q_vis, nq, topk, out, ws, st);
+    return launch_topk_chunked<kMapSlot>(vals, stride, n_elems, map, map_stride, unit, q_vis, nq,
+                                         topk, out, ws, st);
+  }
+  cudaError_t e;
+  if (!map) {
+    e = set_smem_once(topk_kernel<kById>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                      (int)kTopkSmem);
+    if (e != cudaSuccess) return e;
+    topk_kernel<kById><<<nq, kTopkThreads, kTopkSmem, st>>>(vals, stride, n_elems, nullptr, 0,
+                                                             unit, q_vis, topk, out);
+  } else if (pos_vals) {
+    e = set_smem_once(topk_kernel<kMapPos>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                      (int)kTopkSmem);
+    if (e != cudaSuccess) return e;
+    topk_kernel<kMapPos><<<nq, kTopkThreads, kTopkSmem, st>>>(
+        pos_vals, pos_stride, n_elems, map, map_stride, unit, q_vis, topk, out);
+  } else {
+    e = set_smem_once(topk_kernel<kMapSlot>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                      (int)kTopkSmem);
+    if (e != cudaSuccess) return e;
+    topk_kernel<kMapSlot><<<nq, kTopkThreads, kTopkSmem, st>>>(vals, stride, n_elems, map,
+                                                                map_stride, unit, q_vis, topk,
+                                                                out);
+  }
   note_launches(1);
   return cudaGetLastError();
 }

@@ -64,6 +64,8 @@ class Step:
             ws = max(ws, csa2.csa2_index_score_topk_workspace_size(self.nq, self.max_vis,
                                                                    w.n_pool_blocks, w.topk))
         self.ws_index = csa2.workspace(ws, dev)
+        self.ws_pool = (csa2.workspace(csa2.csa2_hier_candidate_pool_workspace_size(
+            self.nq, nb, w.n_pool_blocks), dev) if hier else None)
         if w.kind == "prefill":
             self.ws_attn = csa2.workspace(
                 csa2.csa2_sparse_attn_prefill_workspace_size(self.nq, w.H, w.topk), dev)
@@ -103,12 +105,32 @@ class Step:
                 self.index(L, block_max=self.bm if first_full else None, stream=stream)
                 if first_full:
                     csa2.csa2_hier_candidate_pool(self.bm, self.q_vis, self.w.n_pool_blocks,
-                                                  self.pool, stream=stream)
+                                                  self.pool, ws=self.ws_pool, stream=stream)
                 last_idx = L["idx"]
             elif L["mode"] == "reindex":
                 self.index(L, cand=self.pool, stream=stream)
                 last_idx = L["idx"]
             self.attend(L, last_idx, stream=stream)
+
+    # ------------------------------------------------------------------------------------------
+    def capture(self):
+        """Record one step (the same C-ABI calls as run()) into a CUDA graph; replay() then
+        re-issues the whole step with one launch.  Inputs and outputs stay in the buffers above,
+        so a caller refreshes inputs in place between replays."""
+        self.run()  # first calls on this device: one-time set-up outside the capture
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(self.graph, stream=side, capture_error_mode="thread_local"):
+                self.run(stream=side)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
 
     # ------------------------------------------------------------------------------------------
     def algorithmic_bytes(self) -> dict:

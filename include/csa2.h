@@ -173,6 +173,8 @@ int csa2_index_score_topk_reindex_noalloc(const void *q_idx, int q_dtype, const 
  * q_vis           [nq] int32, ceil(q_vis[n]/block_size) <= max_blocks.
  * block_size      must be 8.     n_pool_blocks  1 <= n_pool_blocks <= 4096 (2048 on the pages).
  * out_pool_blocks [nq, n_pool_blocks] int32; pass it as cand_blocks to Reindex layers.
+ * workspace / ws_bytes  at least csa2_hier_candidate_pool_workspace_size(nq, max_blocks,
+ *           n_pool_blocks) bytes (0 when few blocks or many queries: one CTA per query then).
  */
 size_t csa2_hier_candidate_pool_workspace_size(int nq, int64_t max_blocks, int n_pool_blocks);
 int csa2_hier_candidate_pool(const float *block_max, int nq, const int32_t *q_vis,

@@ -112,6 +112,11 @@ def _index_case(lengths, dtype, Hi, seed, dup=0.0):
     return k, q, w, cu, kn, qn
 
 
+def _pool_ws(csa2, bm, n_pool):
+    return csa2.workspace(csa2.csa2_hier_candidate_pool_workspace_size(bm.shape[0], bm.shape[1],
+                                                                       n_pool))
+
+
 def _run_index(csa2, k, q, w, cu, vis, dtype, topk, cand=None, bm=None):
     nq = q.shape[0]
     max_vis = int(max(vis)) if len(vis) else 0
@@ -168,7 +173,7 @@ def test_pool_and_reindex(csa2):
     for n_pool in (2048, 100):
         pool = torch.empty((2, n_pool), dtype=torch.int32, device="cuda")
         csa2.csa2_hier_candidate_pool(bm, torch.tensor(vis, dtype=torch.int32, device="cuda"),
-                                      n_pool, pool)
+                                      n_pool, pool, ws=_pool_ws(csa2, bm, n_pool))
         bmh = bm.cpu().numpy()
         ref_pool = oracle.hier_candidate_pool(bmh, vis, n_pool)  # same fp32 input: exact
         for n in range(2):
@@ -176,7 +181,7 @@ def test_pool_and_reindex(csa2):
     # Reindex with new queries over the GPU pool (2048 blocks)
     pool = torch.empty((2, 2048), dtype=torch.int32, device="cuda")
     csa2.csa2_hier_candidate_pool(bm, torch.tensor(vis, dtype=torch.int32, device="cuda"), 2048,
-                                  pool)
+                                  pool, ws=_pool_ws(csa2, bm, 2048))
     g = torch.Generator().manual_seed(99)
     q2 = torch.randn(2, 8, 128, generator=g).to(torch.float8_e4m3fn).view(torch.uint8)
     w2 = torch.rand(2, 8, generator=g)
@@ -287,3 +292,57 @@ def test_index_exact_when_scores_are_exact(csa2, dtype):
                                   np.array(vis), 20, cand_blocks=blocks.numpy())
     for n in range(2):
         assert np.array_equal(got[n], ref[n]["idx"])
+
+
+@pytest.mark.parametrize("kind", ["random", "ties"])
+def test_topk_over_many_blocks(csa2, kind):
+    """Pool selection over more than 16,384 block maxima: random scores take the sampled
+    shared-memory path; heavily tied integer scores overflow it and take the global path.
+    Both must equal the oracle's selection on the same fp32 block maxima exactly."""
+    L = 300_001
+    if kind == "random":
+        k, q, w, cu, kn, qn = _index_case([L], 1, 8, 21)
+    else:
+        g = torch.Generator().manual_seed(22)
+        kf = torch.randint(-2, 3, (L, 128), generator=g).float()
+        k = kf.to(torch.float8_e4m3fn).view(torch.uint8)
+        q = torch.randint(-1, 2, (1, 8, 128), generator=g).float().to(torch.float8_e4m3fn).view(torch.uint8)
+        w = torch.full((1, 8), 0.5)
+        cu = torch.tensor([0, L], dtype=torch.int64)
+    nb = (L + 7) // 8
+    bm = torch.empty((1, nb), device="cuda")
+    vis = torch.tensor([L], dtype=torch.int32, device="cuda")
+    _run_index(csa2, k, q, w, cu, [L], 1, 2048, bm=bm)
+    bmh = bm.cpu().numpy()
+    for n_pool in (2048, 700, 4096):
+        pool = torch.empty((1, n_pool), dtype=torch.int32, device="cuda")
+        csa2.csa2_hier_candidate_pool(bm, vis, n_pool, pool, ws=_pool_ws(csa2, bm, n_pool))
+        assert np.array_equal(pool[0].cpu().numpy(), oracle.candidate_pool(bmh[0], n_pool))
+
+
+def test_prefill_indexer_many_queries(csa2):
+    """More than 1,024 queries over one sequence takes the 32-queries-per-MMA scan: causal
+    visibility per query (query i sees positions < P0 + i + 1), block maxima and Top-K."""
+    P0, T, topk = 3000, 1100, 256
+    L = P0 + T
+    k, _, _, cu, kn, _ = _index_case([L], 1, 8, 31)
+    g = torch.Generator().manual_seed(32)
+    q = torch.randn(T, 8, 128, generator=g).to(torch.float8_e4m3fn).view(torch.uint8)
+    w = torch.rand(T, 8, generator=g)
+    vis = np.arange(P0 + 1, P0 + 1 + T)
+    nb = (L + 7) // 8
+    bm = torch.full((T, nb), float("nan"), device="cuda")
+    out = torch.empty((T, topk), dtype=torch.int32, device="cuda")
+    ws = csa2.workspace(csa2.csa2_index_score_topk_workspace_size(T, L, 0, topk))
+    csa2.csa2_index_score_topk(q.cuda(), 1, w.cuda(), k.cuda(), cu.cuda(),
+                               torch.zeros(T, dtype=torch.int32, device="cuda"),
+                               torch.tensor(vis, dtype=torch.int32, device="cuda"), L, topk, out,
+                               out_block_max=bm, ws=ws)
+    got, bmh = out.cpu().numpy(), bm.cpu().numpy()
+    sample = [0, 1, 31, 32, 33, 500, 1023, 1024, 1057, T - 1]
+    ref = oracle.index_score_topk(q.numpy(), 1, w.numpy(), kn, cu.numpy(), np.zeros(T, np.int32),
+                                  vis, topk, queries=sample)
+    for n in sample:
+        check_topk(got[n], ref[n], topk, f"query {n}")
+        nbn = (vis[n] + 7) // 8
+        np.testing.assert_allclose(bmh[n, :nbn], ref[n]["bm"], rtol=2e-6, atol=1e-6)
