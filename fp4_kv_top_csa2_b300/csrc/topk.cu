@@ -125,12 +125,68 @@ __device__ void count_ge_n(const View &ev, int64_t n_elems, const uint32_t (&can
   parity ^= 1;
 }
 
+// Shared-memory specialization: only the keys are read, only the n stored elements are visited.
+template <int NT>
+__device__ void count_ge_n(const SmemView &sv, int64_t n_elems, const uint32_t (&cand)[NT],
+                           uint32_t (&cnt)[NT], TopkShared &sh, int &parity) {
+  uint32_t c[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) c[j] = 0;
+  const int n = (int)n_elems;
+  for (int i0 = threadIdx.x; i0 < n; i0 += 4 * kTopkThreads) {
+    uint32_t keys[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kTopkThreads;
+      keys[u] = i < n ? sv.key[i] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < NT; ++j) c[j] += keys[u] >= cand[j];
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    c[j] = __reduce_add_sync(0xffffffffu, c[j]);
+    if (lane == 0) sh.red[parity][j][wid] = c[j];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < NT; ++j) cnt[j] = __reduce_add_sync(0xffffffffu, sh.red[parity][j][lane]);
+  parity ^= 1;
+}
+
+// Smallest and largest candidate key of the shared-memory set (block-wide).
+__device__ __forceinline__ void key_range(const SmemView &sv, int64_t n_elems, TopkShared &sh,
+                                          int &parity, uint32_t &kmin, uint32_t &kmax) {
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int i = threadIdx.x; i < (int)n_elems; i += kTopkThreads) {
+    const uint32_t k = sv.key[i];
+    if (k != 0u) {
+      lo = min(lo, k);
+      hi = max(hi, k);
+    }
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) {
+    sh.red[parity][0][wid] = lo;
+    sh.red[parity][1][wid] = hi;
+  }
+  __syncthreads();
+  kmin = __reduce_min_sync(0xffffffffu, sh.red[parity][0][lane]);
+  kmax = __reduce_max_sync(0xffffffffu, sh.red[parity][1][lane]);
+  parity ^= 1;
+}
+
 // The k-th largest key (1 <= k <= number of candidates), three bits per round.
 template <class View>
 __device__ uint32_t kth_largest(const View &ev, int64_t n_elems, uint32_t k, TopkShared &sh,
-                                int &parity) {
-  uint32_t T = 0;
-  int b = 32;
+                                int &parity, uint32_t prefix = 0u, int b = 32) {
+  // the answer is known to start with the top (32 - b) bits of `prefix`
+  uint32_t T = b >= 32 ? 0u : (prefix & ~((1u << b) - 1u));
   while (b > 0) {
     const int w = b >= 3 ? 3 : b;
     b -= w;
@@ -207,13 +263,30 @@ __device__ void ordered_emit(const View &ev, int64_t n_elems, uint32_t T, uint32
 }
 
 template <class View>
+__device__ __forceinline__ void start_bits(const View &, int64_t, TopkShared &, int &,
+                                           uint32_t &prefix, int &b) {
+  prefix = 0u;
+  b = 32;
+}
+__device__ __forceinline__ void start_bits(const SmemView &sv, int64_t n, TopkShared &sh,
+                                           int &parity, uint32_t &prefix, int &b) {
+  uint32_t kmin, kmax;
+  key_range(sv, n, sh, parity, kmin, kmax);
+  prefix = kmax;
+  b = (kmin == kmax) ? 0 : 32 - __clz(kmin ^ kmax);  // bits below the shared leading ones
+}
+
+template <class View>
 __device__ void select_and_emit(const View &ev, int64_t n_elems, int topk, TopkShared &sh,
                                 int &parity, int32_t *o) {
   uint32_t cand1[1] = {1u}, nv[1];
   count_ge_n<1>(ev, n_elems, cand1, nv, sh, parity);
   const uint32_t k_eff = min((uint32_t)topk, nv[0]);
   if (k_eff > 0) {
-    const uint32_t T = kth_largest(ev, n_elems, k_eff, sh, parity);
+    uint32_t prefix;
+    int b0;
+    start_bits(ev, n_elems, sh, parity, prefix, b0);
+    const uint32_t T = kth_largest(ev, n_elems, k_eff, sh, parity, prefix, b0);
     uint32_t n_gt = 0;
     if (T != 0xFFFFFFFFu) {
       uint32_t c[1] = {T + 1u}, r[1];
@@ -470,8 +543,29 @@ __global__ void __launch_bounds__(kFilterThreads) topk_filter_kernel(
     for (int j = 0; j < 7; ++j) cand[j] = j == 0 ? 1u : 0xFFFFFFFFu;
     block_counts(cand, cnt, 0);
     if (cnt[0] >= r) {
-      uint32_t T = 0;
-      int b = 32;
+      // only the bits below those shared by the smallest and largest sampled key vary
+      uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+      for (int u = 0; u < kFilterSample / kFilterThreads; ++u)
+        if (my[u] != 0u) {
+          lo = min(lo, my[u]);
+          hi = max(hi, my[u]);
+        }
+      lo = __reduce_min_sync(0xffffffffu, lo);
+      hi = __reduce_max_sync(0xffffffffu, hi);
+      if (lane == 0) {
+        red[0][wid] = lo;
+        red[1][wid] = hi;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int w = 0; w < kFilterThreads / 32; ++w) {
+        lo = min(lo, red[0][w]);
+        hi = max(hi, red[1][w]);
+      }
+      __syncthreads();
+      int b = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
+      uint32_t T = b >= 32 ? 0u : (hi & ~((1u << b) - 1u));
       while (b > 0) {
         const int w = b >= 3 ? 3 : b;
         b -= w;
@@ -574,11 +668,32 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
   const uint32_t k_eff = min((uint32_t)topk, total_valid);
   __syncthreads();
   if (kept >= k_eff && kept <= (uint32_t)kSmemCap) {
-    for (int c = wid; c < n_chunks; c += kTopkWarps) {
-      const uint32_t cnt = cw.kept[c], base = coff[c];
-      for (uint32_t i = lane; i < cnt; i += 32) {
-        skey[base + i] = cw.keys[(size_t)c * kTkChunk + i];
-        spos[base + i] = cw.pos[(size_t)c * kTkChunk + i];
+    if (tid == 0) coff[n_chunks] = kept;
+    __syncthreads();
+    // flattened copy: element e of the kept set lives in the chunk c with coff[c] <= e < coff[c+1]
+    for (int e0 = tid; e0 < (int)kept; e0 += 4 * kTopkThreads) {
+      uint32_t kk[4];
+      int32_t pp[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kTopkThreads;
+        const int ec = e < (int)kept ? e : (int)kept - 1;
+        int lo = 0, hi = n_chunks - 1;  // last chunk with coff[c] <= ec
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (coff[mid] <= (uint32_t)ec) lo = mid; else hi = mid - 1;
+        }
+        const size_t src = (size_t)lo * kTkChunk + (ec - coff[lo]);
+        kk[u] = cw.keys[src];
+        pp[u] = cw.pos[src];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kTopkThreads;
+        if (e < (int)kept) {
+          skey[e] = kk[u];
+          spos[e] = pp[u];
+        }
       }
     }
     __syncthreads();
