@@ -92,6 +92,8 @@ struct TopkShared {
   uint32_t red[2][8][kTopkWarps];
   uint32_t seg_a[kTopkWarps], seg_b[kTopkWarps];
   uint32_t s_a, s_b;
+  uint32_t hist[8][256];
+  uint32_t bcast[2];
 };
 
 // Counts of candidates with key >= cand[j] (j < NT) over the view, block-wide.
@@ -262,6 +264,65 @@ __device__ void ordered_emit(const View &ev, int64_t n_elems, uint32_t T, uint32
   }
 }
 
+// k-th largest of n keys held in shared memory (key 0 = not a candidate), by radix select over
+// the low b bits (the candidates all share the bits of `prefix` above them): 8-bit digits,
+// histograms privatised per warp group (8 sub-histograms of 256 bins, summed per bin), a warp
+// scan over the 256 bins from the top.  Returns T; *need_eq = how many keys equal to T are in
+// the Top-k (k - #keys > T).  Works for any block size that is a multiple of 32 (<= 1024).
+__device__ uint32_t kth_radix(const uint32_t *keys, int n, uint32_t k, uint32_t prefix, int b,
+                              uint32_t (*hist)[256], uint32_t *bcast, uint32_t *need_eq) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int nthr = blockDim.x, nwarp = nthr >> 5;
+  const int sub = wid & 7;
+  uint32_t T = b >= 32 ? 0u : (prefix & ~((1u << b) - 1u));
+  uint32_t rem = k;
+  while (b > 0) {
+    const int w = b >= 8 ? 8 : b;
+    b -= w;
+    const int shift = b;
+    const int hi_shift = shift + w;  // keys still in play share T's bits at and above hi_shift
+    for (int i = tid; i < 8 * 256; i += nthr) (&hist[0][0])[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n; i += nthr) {
+      const uint32_t key = keys[i];
+      const bool in = key != 0u && (hi_shift >= 32 || (key >> hi_shift) == (T >> hi_shift));
+      if (in) atomicAdd(&hist[sub][(key >> shift) & ((1u << w) - 1u)], 1u);
+    }
+    __syncthreads();
+    if (wid == 0) {  // lane l owns bins 255-8l .. 248-8l (descending digit order)
+      uint32_t c[8], s = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int bin = 255 - 8 * lane - j;
+        uint32_t t = 0;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) t += hist[g][bin];
+        c[j] = t;
+        s += t;
+      }
+      const uint32_t inc = warp_incl_scan(s), before = inc - s;
+      // the lane whose bins cross rem (at most one)
+      if (before < rem && inc >= rem) {
+        uint32_t acc = before;
+        int j = 0;
+        for (; j < 8; ++j) {
+          if (acc + c[j] >= rem) break;
+          acc += c[j];
+        }
+        bcast[0] = (uint32_t)(255 - 8 * lane - j);
+        bcast[1] = acc;
+      }
+    }
+    __syncthreads();
+    T |= bcast[0] << shift;
+    rem -= bcast[1];
+    __syncthreads();
+    (void)nwarp;
+  }
+  *need_eq = rem;
+  return T;
+}
+
 template <class View>
 __device__ __forceinline__ void start_bits(const View &, int64_t, TopkShared &, int &,
                                            uint32_t &prefix, int &b) {
@@ -274,6 +335,23 @@ __device__ __forceinline__ void start_bits(const SmemView &sv, int64_t n, TopkSh
   key_range(sv, n, sh, parity, kmin, kmax);
   prefix = kmax;
   b = (kmin == kmax) ? 0 : 32 - __clz(kmin ^ kmax);  // bits below the shared leading ones
+}
+
+// Shared-memory set: k-th key by radix select, then the ordered emission.
+__device__ void select_and_emit(const SmemView &sv, int64_t n_elems, int topk, TopkShared &sh,
+                                int &parity, int32_t *o) {
+  uint32_t cand1[1] = {1u}, nv[1];
+  count_ge_n<1>(sv, n_elems, cand1, nv, sh, parity);
+  const uint32_t k_eff = min((uint32_t)topk, nv[0]);
+  if (k_eff > 0) {
+    uint32_t kmin, kmax;
+    key_range(sv, n_elems, sh, parity, kmin, kmax);
+    const int b = (kmin == kmax) ? 0 : 32 - __clz(kmin ^ kmax);
+    uint32_t need_eq;
+    const uint32_t T = kth_radix(sv.key, (int)n_elems, k_eff, kmax, b, sh.hist, sh.bcast, &need_eq);
+    ordered_emit(sv, n_elems, T, need_eq, sh, o);
+  }
+  for (int i = (int)k_eff + threadIdx.x; i < topk; i += kTopkThreads) o[i] = -1;
 }
 
 template <class View>
@@ -369,7 +447,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
   {
     uint32_t c1[1] = {1u}, nvs[1];
     count_ge_n<1>(smp, kSample, c1, nvs, sh, parity);
-    if (nvs[0] >= r) t_est = kth_largest(smp, kSample, r, sh, parity);
+    if (nvs[0] >= r) {
+      uint32_t kmin, kmax, need_eq;
+      key_range(smp, kSample, sh, parity, kmin, kmax);
+      const int b = (kmin == kmax) ? 0 : 32 - __clz(kmin ^ kmax);
+      t_est = kth_radix(skey, kSample, r, kmax, b, sh.hist, sh.bcast, &need_eq);
+    }
   }
   __syncthreads();  // the sample is no longer needed
 
@@ -490,6 +573,8 @@ __global__ void __launch_bounds__(kFilterThreads) topk_filter_kernel(
   __shared__ uint32_t ks[kFilterSample];
   __shared__ uint32_t red[8][kFilterThreads / 32];
   __shared__ uint32_t wcnt[kFilterThreads / 32];
+  __shared__ uint32_t hist[8][256];
+  __shared__ uint32_t bcast[2];
   const int c = blockIdx.x, n = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int n_chunks = gridDim.x;
@@ -510,76 +595,39 @@ __global__ void __launch_bounds__(kFilterThreads) topk_filter_kernel(
   __syncthreads();
   const int64_t r_want = (int64_t)topk * kFilterSample * 8 / (n_elems * 5) + 8;
   const uint32_t r = (uint32_t)(r_want < kFilterSample ? r_want : kFilterSample);
-  uint32_t my[kFilterSample / kFilterThreads];
-#pragma unroll
-  for (int u = 0; u < kFilterSample / kFilterThreads; ++u) my[u] = ks[u * kFilterThreads + tid];
-  auto block_counts = [&](const uint32_t (&cand)[7], uint32_t (&cnt)[7], int par) {
-    uint32_t cc[7];
-#pragma unroll
-    for (int j = 0; j < 7; ++j) {
-      cc[j] = 0;
-#pragma unroll
-      for (int u = 0; u < kFilterSample / kFilterThreads; ++u) cc[j] += my[u] >= cand[j];
-      cc[j] = __reduce_add_sync(0xffffffffu, cc[j]);
-    }
-    if (lane == 0)
-#pragma unroll
-      for (int j = 0; j < 7; ++j) red[j][wid] = cc[j];
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < 7; ++j) {
-      uint32_t t = 0;
-#pragma unroll
-      for (int w = 0; w < kFilterThreads / 32; ++w) t += red[j][w];
-      cnt[j] = t;
-    }
-    __syncthreads();
-    (void)par;
-  };
   uint32_t t_est = 1u;
   {
-    uint32_t cand[7], cnt[7];
+    // only the bits below those shared by the smallest and largest sampled key vary
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u, nz = 0u;
 #pragma unroll
-    for (int j = 0; j < 7; ++j) cand[j] = j == 0 ? 1u : 0xFFFFFFFFu;
-    block_counts(cand, cnt, 0);
-    if (cnt[0] >= r) {
-      // only the bits below those shared by the smallest and largest sampled key vary
-      uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-#pragma unroll
-      for (int u = 0; u < kFilterSample / kFilterThreads; ++u)
-        if (my[u] != 0u) {
-          lo = min(lo, my[u]);
-          hi = max(hi, my[u]);
-        }
-      lo = __reduce_min_sync(0xffffffffu, lo);
-      hi = __reduce_max_sync(0xffffffffu, hi);
-      if (lane == 0) {
-        red[0][wid] = lo;
-        red[1][wid] = hi;
+    for (int u = 0; u < kFilterSample / kFilterThreads; ++u) {
+      const uint32_t v = ks[u * kFilterThreads + tid];
+      if (v != 0u) {
+        lo = min(lo, v);
+        hi = max(hi, v);
+        ++nz;
       }
-      __syncthreads();
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    nz = __reduce_add_sync(0xffffffffu, nz);
+    if (lane == 0) {
+      red[0][wid] = lo;
+      red[1][wid] = hi;
+      red[2][wid] = nz;
+    }
+    __syncthreads();
+    nz = 0;
 #pragma unroll
-      for (int w = 0; w < kFilterThreads / 32; ++w) {
-        lo = min(lo, red[0][w]);
-        hi = max(hi, red[1][w]);
-      }
-      __syncthreads();
-      int b = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
-      uint32_t T = b >= 32 ? 0u : (hi & ~((1u << b) - 1u));
-      while (b > 0) {
-        const int w = b >= 3 ? 3 : b;
-        b -= w;
-#pragma unroll
-        for (int j = 0; j < 7; ++j)
-          cand[j] = (j + 1 < (1 << w)) ? (T | ((uint32_t)(j + 1) << b)) : 0xFFFFFFFFu;
-        block_counts(cand, cnt, 0);
-        uint32_t best = 0;
-#pragma unroll
-        for (int j = 0; j < 7; ++j)
-          if (j + 1 < (1 << w) && cnt[j] >= r) best = j + 1;
-        T |= best << b;
-      }
-      t_est = T;
+    for (int w = 0; w < kFilterThreads / 32; ++w) {
+      lo = min(lo, red[0][w]);
+      hi = max(hi, red[1][w]);
+      nz += red[2][w];
+    }
+    if (nz >= r) {
+      const int b = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
+      uint32_t need_eq;
+      t_est = kth_radix(ks, kFilterSample, r, hi, b, hist, bcast, &need_eq);
     }
   }
   // this chunk: warp w owns elements [w*512, w*512+512) of it, 16 per lane, all loads in flight
