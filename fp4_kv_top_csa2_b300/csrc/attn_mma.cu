@@ -11,12 +11,14 @@
 //   2. Every row is dequantised exactly (E2M1 x E4M3 has <= 6 significant bits) to bf16 and
 //      stored once, as eight 128B-swizzled chunks [64 rows x 64 channels].
 //   3. S = Q Khat^T: kind::f16, M=128 (heads) x N=64 (rows) x K=512, fp32 in TMEM.
-//   4. Softmax rows (exp2 domain), P split into bf16 hi + lo parts (P ~ hi + lo to 2^-17).
-//   5. O = (P_hi + P_lo) Vhat: kind::f16, the same dequantised chunks read as the MN-major B
-//      operand (channels contiguous), N=64 channels per MMA, fp32 in TMEM (512 columns; S is
-//      consumed before O overwrites its columns).
-//   6. The unnormalised O rows and the per-head (max, sum) go to workspace; a combine kernel
-//      merges the tiles of each query.
+//   4. Softmax rows (exp2 domain; four warps, two per 32-column half of S), P split into bf16
+//      hi + lo parts (P ~ hi + lo to 2^-17).
+//   5. O^T = Vhat^T (P_hi + P_lo)^T: kind::f16, the same dequantised chunks read as the
+//      MN-major A operand (channels contiguous, M=128 channels = two chunks), P as the K-major
+//      B operand (N=64 heads), fp32 in TMEM columns 0..255 (S lives in 256..319).
+//   6. Channels on TMEM lanes make the epilogue coalesced: a warp stores 32 consecutive channels
+//      of one head per instruction.  The unnormalised O rows and the per-head (max, sum) go to
+//      workspace; a combine kernel merges the tiles of each query.
 #include <cstring>
 
 #include "sm100.cuh"
@@ -26,6 +28,7 @@ namespace csa2 {
 constexpr int kAttTS = 64;          // selected rows per CTA
 constexpr int kAttThreads = 256;
 constexpr int kAttTmemCols = 512;
+constexpr int kColS = 256;          // S [heads x rows]; O^T takes columns 0..255
 
 // shared-memory layout (offsets from a 1024-byte aligned base)
 constexpr int kOffQ = 0;                         // 8 chunks x (64 rows x 128 B) = 64 KB
@@ -37,14 +40,15 @@ constexpr int kOffRawS = kOffRawC + kAttTS * 256;  // 64 rows x 32 B scales
 constexpr int kOffLut = kOffRawS + kAttTS * 32;    // 256 x u32
 constexpr int kOffMisc = kOffLut + 1024;
 constexpr int kAttSmem = kOffMisc + 1024 + 1024;  // + alignment slack
-// The M=128 operand reads of Q chunk 7 and of P_lo run 8 KB past their 64 real rows, into
-// K-chunk 0 and the raw codes respectively: readable, and only feed unused accumulator lanes.
+// The M=128 operand read of Q chunk 7 runs 8 KB past its 64 real rows, into K-chunk 0:
+// readable, and it only feeds unused accumulator lanes.
 
 struct AttMisc {
   uint64_t bar_q, bar_g, bar_s, bar_o;
   uint32_t tmem_base;
   int slot_ok[kAttTS];
-  float m2[64], l[64];
+  float m2[64];
+  float mh[2][64], lh[2][64];  // per-half row max / sum of the softmax
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -70,17 +74,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// MN-major 128B-swizzled operand: 128-byte rows along K, 64 MN-elements per row; one MN atom.
-__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr >> 4) & 0x3FFFu);
-  d |= (uint64_t)(1024u >> 4) << 16;  // leading byte offset (next MN atom; single atom here)
-  d |= (uint64_t)(1024u >> 4) << 32;  // stride byte offset: next 8 rows along K
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
 }
 
 template <bool kQfp4>
@@ -190,104 +183,106 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
     for (int kc = 0; kc < 8; ++kc)
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_f16(tmem, desc_k128_sw128(qa + kc * 8192 + 32 * ks),
+        mma_f16(tmem + kColS, desc_k128_sw128(qa + kc * 8192 + 32 * ks),
                 desc_k128_sw128(ka + kc * 8192 + 32 * ks), idesc, (kc | ks) != 0);
     mma_commit(&ms.bar_s);
   }
 
-  // ---- 4. softmax: warps 0 and 1 own TMEM lanes 0..63 = heads
-  if (warp < 2) {
+  // ---- 4. softmax: warps 0,1 and 4,5 read TMEM lanes 0..63 (= heads); warps 0,1 take the
+  //         columns (rows) 0..31 of S, warps 4,5 the columns 32..63
+  if ((warp & 3) < 2) {
     ok = __all_sync(0xffffffffu, mbar_wait(&ms.bar_s, 0)) && ok;
     tc_fence_after();
-    const int h = warp * 32 + lane;
-    float s[kAttTS];
-    const uint32_t la = tmem + ((uint32_t)(warp * 32) << 16);
+    const int h = (warp & 3) * 32 + lane;
+    const int half = warp >> 2, j0 = half * 32;
+    float s[32];
     {
-      uint32_t r[kAttTS / 16][16];
-#pragma unroll
-      for (int c = 0; c < kAttTS / 16; ++c) tmem_ld16(la + 16 * c, r[c]);  // one wait for all
+      const uint32_t la = tmem + kColS + j0 + ((uint32_t)((warp & 3) * 32) << 16);
+      uint32_t r[2][16];
+      tmem_ld16(la, r[0]);
+      tmem_ld16(la + 16, r[1]);
       tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < kAttTS / 16; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int i = 0; i < 16; ++i) s[16 * c + i] = __uint_as_float(r[c][i]) * scale_log2e;
     }
     float m = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kAttTS; ++j)
-      if (ms.slot_ok[j]) m = fmaxf(m, s[j]);
+    for (int j = 0; j < 32; ++j)
+      if (ms.slot_ok[j0 + j]) m = fmaxf(m, s[j]);
+    ms.mh[half][h] = m;
+    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps
+    m = fmaxf(ms.mh[0][h], ms.mh[1][h]);
     float l = 0.0f;
-    uint32_t hi[kAttTS / 2], lo[kAttTS / 2];
+    uint32_t hi[16], lo[16];
 #pragma unroll
-    for (int j = 0; j < kAttTS; j += 2) {
-      const float p0 = ms.slot_ok[j] ? exp2f(s[j] - m) : 0.0f;
-      const float p1 = ms.slot_ok[j + 1] ? exp2f(s[j + 1] - m) : 0.0f;
+    for (int j = 0; j < 32; j += 2) {
+      const float p0 = ms.slot_ok[j0 + j] ? exp2f(s[j] - m) : 0.0f;
+      const float p1 = ms.slot_ok[j0 + j + 1] ? exp2f(s[j + 1] - m) : 0.0f;
       l += p0 + p1;
       const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
       hi[j / 2] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
       lo[j / 2] = pack_bf16x2(p0 - __bfloat162float(h0), p1 - __bfloat162float(h1));
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int off = h * 128 + ((u ^ (h & 7)) << 4);
+    for (int u = 0; u < 4; ++u) {
+      const int off = h * 128 + (((4 * half + u) ^ (h & 7)) << 4);
       *reinterpret_cast<uint4 *>(sm + kOffPhi + off) =
           make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
       *reinterpret_cast<uint4 *>(sm + kOffPlo + off) =
           make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
     }
-    ms.m2[h] = m;
-    ms.l[h] = l;
+    if (half == 0) ms.m2[h] = m;
+    ms.lh[half][h] = l;
   }
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  // ---- 5. O = (P_hi + P_lo) Vhat, 64 channels per MMA
+  // ---- 5. O^T = Vhat^T P^T: M=128 channels (two chunks), N=64 heads, K=16 rows per MMA
   if (tid == 0) {
-    constexpr uint32_t idesc_pv = idesc_f32acc(1, 1, 128, 64) | (1u << 16);  // B MN-major
+    constexpr uint32_t idesc_pv = idesc_f32acc(1, 1, 128, 64) | (1u << 15);  // A MN-major
     const uint32_t ka = smem_u32(sm + kOffK);
     const uint32_t ph = smem_u32(sm + kOffPhi), pl = smem_u32(sm + kOffPlo);
-    for (int cc = 0; cc < 8; ++cc) {
+    for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
       for (int ks = 0; ks < kAttTS / 16; ++ks) {
-        const uint64_t bd = desc_mn_sw128(ka + cc * 8192 + ks * 16 * 128);
-        mma_f16(tmem + cc * 64, desc_k128_sw128(ph + 32 * ks), bd, idesc_pv, ks != 0);
-        mma_f16(tmem + cc * 64, desc_k128_sw128(pl + 32 * ks), bd, idesc_pv, 1);
+        const uint64_t ad = desc_mn_sw128_atoms(ka + (2 * mb) * 8192 + ks * 16 * 128, 8192);
+        mma_f16(tmem + mb * 64, ad, desc_k128_sw128(ph + 32 * ks), idesc_pv, ks != 0);
+        mma_f16(tmem + mb * 64, ad, desc_k128_sw128(pl + 32 * ks), idesc_pv, 1);
       }
     }
     mma_commit(&ms.bar_o);
   }
 
-  // ---- 6. epilogue: warps 0,1 (lanes 0..63, channels 0..255) and 4,5 (channels 256..511)
-  if ((warp & 3) < 2) {
-    ok = __all_sync(0xffffffffu, mbar_wait(&ms.bar_o, 0)) && ok;
-    tc_fence_after();
-    const int h = (warp & 3) * 32 + lane;
-    const int c_begin = (warp >= 4) ? 256 : 0;
-    const uint32_t la = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    float *orow = o_part + (((int64_t)n * n_tiles + tile) * H + h) * kD;
-    for (int c = c_begin; c < c_begin + 256; c += 32) {
+  // ---- 6. epilogue: warp w reads lanes 32(w%4).. (channels) and heads 32(w/4)..+31 of every
+  //         M block; column 64*mb + h of O^T is channel 128*mb + lane
+  ok = __all_sync(0xffffffffu, mbar_wait(&ms.bar_o, 0)) && ok;
+  tc_fence_after();
+  {
+    const int q4 = warp & 3, hh = warp >> 2;
+    const uint32_t la = tmem + ((uint32_t)(q4 * 32) << 16);
+    float *obase = o_part + ((int64_t)n * n_tiles + tile) * H * kD;
+#pragma unroll 1
+    for (int mb = 0; mb < 4; ++mb) {
       uint32_t r0[16], r1[16];
-      tmem_ld16(la + c, r0);
-      tmem_ld16(la + c + 16, r1);
+      tmem_ld16(la + mb * 64 + hh * 32, r0);
+      tmem_ld16(la + mb * 64 + hh * 32 + 16, r1);
       tmem_ld_wait();
-      if (h < H) {
-        float4 *dst = reinterpret_cast<float4 *>(orow + c);
+      float *oc = obase + mb * 128 + q4 * 32 + lane;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[i] = make_float4(__uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]),
-                               __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]));
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[4 + i] = make_float4(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]),
-                                   __uint_as_float(r1[4 * i + 2]), __uint_as_float(r1[4 * i + 3]));
+      for (int i = 0; i < 16; ++i) {
+        const int h0 = hh * 32 + i, h1 = h0 + 16;
+        if (h0 < H) oc[(int64_t)h0 * kD] = __uint_as_float(r0[i]);
+        if (h1 < H) oc[(int64_t)h1 * kD] = __uint_as_float(r1[i]);
       }
     }
-    if (warp < 2 && h < H) {
-      const int64_t pr = ((int64_t)n * n_tiles + tile) * H + h;
-      m_part[pr] = ok ? ms.m2[h] : -INFINITY;
-      l_part[pr] = ok ? ms.l[h] : 0.0f;
+    if (tid < H) {
+      const int64_t pr = ((int64_t)n * n_tiles + tile) * H + tid;
+      m_part[pr] = ok ? ms.m2[tid] : -INFINITY;
+      l_part[pr] = ok ? ms.lh[0][tid] + ms.lh[1][tid] : 0.0f;
     }
   }
   tc_fence_before();
@@ -298,78 +293,70 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
 
 // Merge the tiles of each (query, head): out = sum_t O_t 2^(m_t - M) / sum_t l_t 2^(m_t - M);
 // lse = (M + log2 L) * ln 2.  m is in the log2 domain (logits * scale * log2 e).
+// Grid (kD / 128, H, nq), 128 threads: thread = one channel.  The channel's partials of up to
+// 32 tiles are loaded at once (before the weights are known), then summed in tile order.
+constexpr int kCombBatch = 32;
 __global__ void __launch_bounds__(128) attn_mma_combine_kernel(
     int H, int n_tiles, const float *__restrict__ o_part, const float *__restrict__ m_part,
     const float *__restrict__ l_part, uint16_t *__restrict__ out, float *__restrict__ lse) {
   __shared__ float wgt[256];
-  __shared__ float red[2][4];
-  const int h = blockIdx.x, n = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  // per-tile (m, l) in parallel: thread t owns tiles t and t + 128
-  float mt[2], lt[2];
-  float M = -INFINITY;
+  __shared__ float sM, sL;
+  const int h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x, lane = tid & 31;
+  const int c = blockIdx.x * 128 + tid;
+  const int64_t tstride = (int64_t)H * kD;  // floats between consecutive tiles
+  const float *op = o_part + ((int64_t)n * n_tiles * H + h) * kD + c;
+  float o[kCombBatch];
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int t = tid + 128 * k;
-    mt[k] = -INFINITY;
-    lt[k] = 0.0f;
-    if (t < n_tiles) {
-      const int64_t pr = ((int64_t)n * n_tiles + t) * H + h;
-      lt[k] = l_part[pr];
-      mt[k] = m_part[pr];
-      if (lt[k] > 0.0f) M = fmaxf(M, mt[k]);
+  for (int u = 0; u < kCombBatch; ++u) o[u] = u < n_tiles ? op[u * tstride] : 0.0f;
+  if (tid < 32) {  // per-tile weights (n_tiles <= 256)
+    float mt[8], lt[8];
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int t = lane + 32 * k;
+      mt[k] = -INFINITY;
+      lt[k] = 0.0f;
+      if (t < n_tiles) {
+        const int64_t pr = ((int64_t)n * n_tiles + t) * H + h;
+        lt[k] = l_part[pr];
+        mt[k] = m_part[pr];
+        if (lt[k] > 0.0f) M = fmaxf(M, mt[k]);
+      }
+    }
+    M = warp_max(M);
+    float Lp = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int t = lane + 32 * k;
+      if (t < n_tiles) {
+        const float wv = (lt[k] > 0.0f) ? exp2f(mt[k] - M) : 0.0f;
+        wgt[t] = wv;
+        Lp += lt[k] * wv;
+      }
+    }
+    Lp = warp_sum(Lp);
+    if (lane == 0) {
+      sM = M;
+      sL = Lp;
     }
   }
-  M = warp_max(M);
-  if (lane == 0) red[0][wid] = M;
   __syncthreads();
-  M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
-  float Lp = 0.0f;
+  float acc = 0.0f;
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int t = tid + 128 * k;
-    if (t < n_tiles) {
-      const float wv = (lt[k] > 0.0f) ? exp2f(mt[k] - M) : 0.0f;
-      wgt[t] = wv;
-      Lp += lt[k] * wv;
-    }
-  }
-  Lp = warp_sum(Lp);
-  if (lane == 0) red[1][wid] = Lp;
-  __syncthreads();
-  const float L = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-  // O: thread = 4 channels, tiles four at a time
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4 *op = reinterpret_cast<const float4 *>(o_part) + tid;
-  const int64_t tstride = (int64_t)H * kD / 4;  // float4s between consecutive tiles
-  const int64_t base4 = (((int64_t)n * n_tiles) * H + h) * kD / 4;
-  int t = 0;
-  for (; t + 4 <= n_tiles; t += 4) {
-    float4 o[4];
+  for (int u = 0; u < kCombBatch; ++u)
+    if (u < n_tiles) acc = fmaf(o[u], wgt[u], acc);
+  for (int t0 = kCombBatch; t0 < n_tiles; t0 += kCombBatch) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) o[u] = op[base4 + (t + u) * tstride];
+    for (int u = 0; u < kCombBatch; ++u) o[u] = t0 + u < n_tiles ? op[(t0 + u) * tstride] : 0.0f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float wv = wgt[t + u];
-      acc.x = fmaf(o[u].x, wv, acc.x);
-      acc.y = fmaf(o[u].y, wv, acc.y);
-      acc.z = fmaf(o[u].z, wv, acc.z);
-      acc.w = fmaf(o[u].w, wv, acc.w);
-    }
+    for (int u = 0; u < kCombBatch; ++u)
+      if (t0 + u < n_tiles) acc = fmaf(o[u], wgt[t0 + u], acc);
   }
-  for (; t < n_tiles; ++t) {
-    const float4 o = op[base4 + t * tstride];
-    const float wv = wgt[t];
-    acc.x = fmaf(o.x, wv, acc.x);
-    acc.y = fmaf(o.y, wv, acc.y);
-    acc.z = fmaf(o.z, wv, acc.z);
-    acc.w = fmaf(o.w, wv, acc.w);
-  }
+  const float L = sL, M = sM;
   const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  uint2 pk;
-  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  reinterpret_cast<uint2 *>(out + ((int64_t)n * H + h) * kD)[tid] = pk;
-  if (tid == 0 && lse) lse[(int64_t)n * H + h] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  out[((int64_t)n * H + h) * kD + c] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv));
+  if (blockIdx.x == 0 && tid == 0 && lse)
+    lse[(int64_t)n * H + h] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -433,7 +420,7 @@ cudaError_t launch_attn_mma(const void *q_bf16, const uint8_t *q_codes, const ui
   note_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_mma_combine_kernel<<<dim3(H, nq), 128, 0, st>>>(H, n_tiles, o_part, m_part, l_part,
+  attn_mma_combine_kernel<<<dim3(kD / 128, H, nq), 128, 0, st>>>(H, n_tiles, o_part, m_part, l_part,
                                                        static_cast<uint16_t *>(out_bf16), lse);
   note_launches(1);
   return cudaGetLastError();

@@ -65,17 +65,6 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// MN-major 128B-swizzled operand spanning several 64-element MN atoms `atom_stride` bytes apart.
-__device__ __forceinline__ uint64_t desc_mn_sw128_atoms(uint32_t addr, uint32_t atom_stride) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((atom_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset: next MN atom
-  d |= (uint64_t)(1024u >> 4) << 32;                    // stride byte offset: next 8 rows (K)
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
 __device__ __forceinline__ void pf_gather(uint8_t *raw, PfMisc &ms, int buf, int tid,
                                           const int32_t *idx_n, int slot0, int topk,
                                           int64_t base, const uint8_t *codes, const uint8_t *sf) {

@@ -145,7 +145,21 @@ __device__ __forceinline__ uint64_t desc_k128_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor, dense, fp32 accumulate, both operands K-major.
+// Shared-memory matrix descriptor: MN-major operand (MN elements contiguous) stored as 128-byte
+// rows along K with the 128-byte swizzle, 8-row K groups 1024 bytes apart; an MN extent above
+// one 128-byte atom continues `atom_stride` bytes further on (leading byte offset).
+__device__ __forceinline__ uint64_t desc_mn_sw128_atoms(uint32_t addr, uint32_t atom_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((atom_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset: next MN atom
+  d |= (uint64_t)(1024u >> 4) << 32;                    // stride byte offset: next 8 rows (K)
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, dense, fp32 accumulate, both operands K-major (bit 15 / bit 16 set
+// make A / B MN-major).
 //   a_fmt/b_fmt: kind::f8f6f4 -> 0 = E4M3;  kind::f16 -> 0 = F16, 1 = BF16.
 __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t a_fmt, uint32_t b_fmt, uint32_t M,
                                                     uint32_t N) {
