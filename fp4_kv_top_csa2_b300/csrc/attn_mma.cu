@@ -92,7 +92,6 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
   uint32_t *lut = reinterpret_cast<uint32_t *>(sm + kOffLut);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile = blockIdx.x, n = blockIdx.y;
-  const int64_t base = cu_ctx[q_seq ? q_seq[n] : n];
 
   if (tid == 0) {
     mbar_init(&ms.bar_q, 1);
@@ -111,6 +110,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
+  pdl_wait();
+  pdl_trigger();
+  const int64_t base = cu_ctx[q_seq ? q_seq[n] : n];
 
   // ---- 1. loads
   if (!kQfp4 && tid == 0) {
@@ -301,6 +303,8 @@ __global__ void __launch_bounds__(128) attn_mma_combine_kernel(
     const float *__restrict__ l_part, uint16_t *__restrict__ out, float *__restrict__ lse) {
   __shared__ float wgt[256];
   __shared__ float sM, sL;
+  pdl_wait();
+  pdl_trigger();
   const int h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x, lane = tid & 31;
   const int c = blockIdx.x * 128 + tid;
   const int64_t tstride = (int64_t)H * kD;  // floats between consecutive tiles
@@ -406,24 +410,24 @@ cudaError_t launch_attn_mma(const void *q_bf16, const uint8_t *q_codes, const ui
     e = set_smem_once(attn_mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kAttSmem);
     if (e != cudaSuccess) return e;
-    attn_mma_kernel<false><<<grid, kAttThreads, kAttSmem, st>>>(
-        qm, nullptr, nullptr, H, q_seq, codes, sf, cu_ctx, idx, topk, scale_log2e, n_tiles,
-        o_part, m_part, l_part);
+    e = launch_pdl(attn_mma_kernel<false>, grid, dim3(kAttThreads), kAttSmem, st, qm,
+                   (const uint8_t *)nullptr, (const uint8_t *)nullptr, H, q_seq, codes, sf, cu_ctx,
+                   idx, topk, scale_log2e, n_tiles, o_part, m_part, l_part);
   } else {
     e = set_smem_once(attn_mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kAttSmem);
     if (e != cudaSuccess) return e;
-    attn_mma_kernel<true><<<grid, kAttThreads, kAttSmem, st>>>(
-        qm, q_codes, q_sf, H, q_seq, codes, sf, cu_ctx, idx, topk, scale_log2e, n_tiles, o_part,
-        m_part, l_part);
+    e = launch_pdl(attn_mma_kernel<true>, grid, dim3(kAttThreads), kAttSmem, st, qm, q_codes,
+                   q_sf, H, q_seq, codes, sf, cu_ctx, idx, topk, scale_log2e, n_tiles, o_part,
+                   m_part, l_part);
   }
   note_launches(1);
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_mma_combine_kernel<<<dim3(kD / 128, H, nq), 128, 0, st>>>(H, n_tiles, o_part, m_part, l_part,
-                                                       static_cast<uint16_t *>(out_bf16), lse);
+  e = launch_pdl(attn_mma_combine_kernel, dim3(kD / 128, H, nq), dim3(128), 0, st, H, n_tiles,
+                 (const float *)o_part, (const float *)m_part, (const float *)l_part,
+                 static_cast<uint16_t *>(out_bf16), lse);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa2

@@ -101,7 +101,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   uint32_t *lut = reinterpret_cast<uint32_t *>(sm + kPfOffLut);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = blockIdx.x;
-  const int64_t base = cu_ctx[q_seq[n]];
   const int32_t *idx_n = idx + (int64_t)n * topk;
   const int n_tiles = (topk + kPfTS - 1) / kPfTS;
 
@@ -123,6 +122,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
   const uint32_t tS = tmem + 256;
+  pdl_wait();
+  pdl_trigger();
+  const int64_t base = cu_ctx[q_seq[n]];
 
   if (tid < kPfTS) pf_gather(sm + kPfOffRaw, ms, 0, tid, idx_n, 0, topk, base, codes, sf);
   // the FP4 query, exactly dequantised into the swizzled Q chunks
@@ -316,11 +318,11 @@ cudaError_t launch_attn_prefill(const uint8_t *q_codes, const uint8_t *q_sf, int
   cudaError_t e = set_smem_once(attn_prefill_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
   if (e != cudaSuccess) return e;
-  attn_prefill_kernel<<<T, kPfThreads, kPfSmem, st>>>(
-      q_codes, q_sf, H, q_seq, codes, sf, cu_ctx, idx, topk, scale * 1.4426950408889634f,
-      static_cast<uint16_t *>(out_bf16), lse);
+  e = launch_pdl(attn_prefill_kernel, dim3(T), dim3(kPfThreads), kPfSmem, st, q_codes, q_sf, H,
+                 q_seq, codes, sf, cu_ctx, idx, topk, scale * 1.4426950408889634f,
+                 static_cast<uint16_t *>(out_bf16), lse);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa2

@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(kAT) attn_partial_kernel(
     const int64_t *__restrict__ cu_ctx, const int32_t *__restrict__ idx, int topk, float scale,
     int slots_per_split, int n_split, float *__restrict__ o_part, float *__restrict__ m_part,
     float *__restrict__ l_part, uint16_t *__restrict__ out, float *__restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   AttnSmem &sm = *reinterpret_cast<AttnSmem *>(smem_raw);
   const int s = blockIdx.x, hg = blockIdx.y, n = blockIdx.z;
@@ -203,6 +205,8 @@ __global__ void __launch_bounds__(kAT) attn_partial_kernel(
 __global__ void __launch_bounds__(128) attn_combine_kernel(
     int H, int n_split, const float *__restrict__ o_part, const float *__restrict__ m_part,
     const float *__restrict__ l_part, uint16_t *__restrict__ out, float *__restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
   const int h = blockIdx.x, n = blockIdx.y;
   float M = -INFINITY;
   for (int s = 0; s < n_split; ++s) M = fmaxf(M, m_part[((int64_t)n * n_split + s) * H + h]);
@@ -263,16 +267,17 @@ cudaError_t launch_attn(const void *q_bf16, const uint8_t *q_codes, const uint8_
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(ns, (H + kHG - 1) / kHG, nq);
-  attn_partial_kernel<<<grid, kAT, smem, st>>>(
-      static_cast<const uint16_t *>(q_bf16), q_codes, q_sf, H, q_seq, codes, sf, cu_ctx, idx,
-      topk, scale, sps, ns, o_part, m_part, l_part, static_cast<uint16_t *>(out_bf16), lse);
+  e = launch_pdl(attn_partial_kernel, grid, dim3(kAT), smem, st,
+                 static_cast<const uint16_t *>(q_bf16), q_codes, q_sf, H, q_seq, codes, sf,
+                 cu_ctx, idx, topk, scale, sps, ns, o_part, m_part, l_part,
+                 static_cast<uint16_t *>(out_bf16), lse);
   note_launches(1);
-  e = cudaGetLastError();
   if (e != cudaSuccess || ns == 1) return e;
-  attn_combine_kernel<<<dim3(H, nq), 128, 0, st>>>(H, ns, o_part, m_part, l_part,
-                                                   static_cast<uint16_t *>(out_bf16), lse);
+  e = launch_pdl(attn_combine_kernel, dim3(H, nq), dim3(128), 0, st, H, ns,
+                 (const float *)o_part, (const float *)m_part, (const float *)l_part,
+                 static_cast<uint16_t *>(out_bf16), lse);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa2

@@ -83,6 +83,19 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Programmatic dependent launch.  The library's kernels are enqueued with programmatic stream
+// serialisation (launch_pdl), so the CTAs of a kernel may be scheduled while the kernel before
+// it drains.  Every kernel calls pdl_wait() before its first global-memory access (read or
+// write): it returns once the previous grid has completed and its writes are visible.  A kernel
+// calls pdl_trigger() once it holds its own resources (after any TMEM allocation), which lets
+// the next kernel's CTAs start their prologue; so every CTA of an earlier grid has allocated
+// before any CTA of a later grid exists, and a later CTA only ever waits for TMEM that an
+// earlier one frees.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Per-device status word written by bounded device-side waits that ran out.  The library is
 // built as one translation unit (csa2_lib.cu), so this is its single definition.
 __device__ int g_csa2_status = 0;
@@ -120,6 +133,44 @@ inline cudaError_t set_attr_once(const void *kernel, cudaFuncAttribute attr, int
 template <class K>
 inline cudaError_t set_smem_once(K *kernel, cudaFuncAttribute attr, int value) {
   return set_attr_once(reinterpret_cast<const void *>(kernel), attr, value);
+}
+
+// Enqueue `kern` on `st` with programmatic stream serialisation (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// The same, as clusters of `cluster_x` CTAs along x (grid.x a multiple of cluster_x).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                      cudaStream_t st, int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = (unsigned)cluster_x;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
 // Process-wide count of kernels enqueued by the library (csa2_kernel_launches).

@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_mma_kernel(
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  pdl_wait();
   int total;
   if (MODE == kScan) {
     if (warp == 0) {  // chunk prefix sums over queries, 32 at a time
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_mma_kernel(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();
   if (MODE == kScan) {
     total = scan_total(sm, p.nq);
   } else {
@@ -331,9 +333,9 @@ static cudaError_t launch_index_mma_t(const CUtensorMap &km, const CUtensorMap &
   cudaError_t e = set_smem_once(index_mma_kernel<DT, MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  index_mma_kernel<DT, MODE><<<grid, kIdxThreads, smem, st>>>(km, qm, p);
+  e = launch_pdl(index_mma_kernel<DT, MODE>, dim3(grid), dim3(kIdxThreads), smem, st, km, qm, p);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 bool index_mma_supported(int nq) { return nq <= kMaxScanQueries && encode_fn() != nullptr; }

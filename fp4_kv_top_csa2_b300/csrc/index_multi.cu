@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_multi_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------------------ TMA producer
@@ -225,15 +227,15 @@ cudaError_t launch_score_scan_multi(const void *q_idx, int dtype, const float *w
     e = set_smem_once(index_multi_kernel<CSA2_E4M3>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    index_multi_kernel<CSA2_E4M3><<<grid, kMqThreads, smem, st>>>(km, qm, p);
+    e = launch_pdl(index_multi_kernel<CSA2_E4M3>, dim3(grid), dim3(kMqThreads), smem, st, km, qm, p);
   } else {
     e = set_smem_once(index_multi_kernel<CSA2_BF16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    index_multi_kernel<CSA2_BF16><<<grid, kMqThreads, smem, st>>>(km, qm, p);
+    e = launch_pdl(index_multi_kernel<CSA2_BF16>, dim3(grid), dim3(kMqThreads), smem, st, km, qm, p);
   }
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa2

@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(256) score_scan_kernel(
     const uint8_t *__restrict__ k_idx, const float *__restrict__ k_scale,
     const int64_t *__restrict__ cu_ctx, const int32_t *__restrict__ q_seq,
     const int32_t *__restrict__ q_vis, float *__restrict__ bm, int64_t bm_stride) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float qs[kMaxHi * 128];
   __shared__ float ws[kMaxHi];
   const int n = blockIdx.y;
@@ -112,6 +114,8 @@ __global__ void __launch_bounds__(256) score_cand_kernel(
     const int64_t *__restrict__ cu_ctx, const int32_t *__restrict__ q_seq,
     const int32_t *__restrict__ q_vis, const int32_t *__restrict__ cand_blocks,
     int n_cand_blocks, float *__restrict__ scores) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float qs[kMaxHi * 128];
   __shared__ float ws[kMaxHi];
   const int n = blockIdx.y;
@@ -139,14 +143,15 @@ cudaError_t launch_score_scan(const void *q_idx, int dtype, const float *w, int 
   if (nq == 0 || max_vis == 0) return cudaSuccess;
   dim3 grid((unsigned)((max_vis + 255) / 256), (unsigned)nq);
   const uint8_t *k = static_cast<const uint8_t *>(k_idx);
+  cudaError_t e;
   if (dtype == CSA2_BF16)
-    score_scan_kernel<CSA2_BF16><<<grid, 256, 0, st>>>(q_idx, w, Hi, Di, k, k_scale, cu_ctx,
-                                                       q_seq, q_vis, bm, bm_stride);
+    e = launch_pdl(score_scan_kernel<CSA2_BF16>, grid, dim3(256), 0, st, q_idx, w, Hi, Di, k,
+                   k_scale, cu_ctx, q_seq, q_vis, bm, bm_stride);
   else
-    score_scan_kernel<CSA2_E4M3><<<grid, 256, 0, st>>>(q_idx, w, Hi, Di, k, k_scale, cu_ctx,
-                                                       q_seq, q_vis, bm, bm_stride);
+    e = launch_pdl(score_scan_kernel<CSA2_E4M3>, grid, dim3(256), 0, st, q_idx, w, Hi, Di, k,
+                   k_scale, cu_ctx, q_seq, q_vis, bm, bm_stride);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_score_cand(const void *q_idx, int dtype, const float *w, int nq, int Hi,
@@ -158,16 +163,15 @@ cudaError_t launch_score_cand(const void *q_idx, int dtype, const float *w, int 
   const int64_t n_slots = (int64_t)n_cand_blocks * kBlock;
   dim3 grid((unsigned)((n_slots + 255) / 256), (unsigned)nq);
   const uint8_t *k = static_cast<const uint8_t *>(k_idx);
+  cudaError_t e;
   if (dtype == CSA2_BF16)
-    score_cand_kernel<CSA2_BF16><<<grid, 256, 0, st>>>(q_idx, w, Hi, Di, k, k_scale, cu_ctx,
-                                                       q_seq, q_vis, cand_blocks, n_cand_blocks,
-                                                       scores);
+    e = launch_pdl(score_cand_kernel<CSA2_BF16>, grid, dim3(256), 0, st, q_idx, w, Hi, Di, k,
+                   k_scale, cu_ctx, q_seq, q_vis, cand_blocks, n_cand_blocks, scores);
   else
-    score_cand_kernel<CSA2_E4M3><<<grid, 256, 0, st>>>(q_idx, w, Hi, Di, k, k_scale, cu_ctx,
-                                                       q_seq, q_vis, cand_blocks, n_cand_blocks,
-                                                       scores);
+    e = launch_pdl(score_cand_kernel<CSA2_E4M3>, grid, dim3(256), 0, st, q_idx, w, Hi, Di, k,
+                   k_scale, cu_ctx, q_seq, q_vis, cand_blocks, n_cand_blocks, scores);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa2

@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(256) kv_quant_kernel(const uint16_t *__restric
                                                        const int64_t *__restrict__ out_rows,
                                                        uint8_t *__restrict__ codes,
                                                        uint8_t *__restrict__ sf) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= n_rows) return;
@@ -62,10 +64,11 @@ cudaError_t launch_kv_quant(const void *x, int64_t n_rows, int d, const int64_t 
   if (n_rows == 0) return cudaSuccess;
   const int rows_per_cta = 8;
   const int64_t grid = (n_rows + rows_per_cta - 1) / rows_per_cta;
-  kv_quant_kernel<<<(unsigned)grid, 32 * rows_per_cta, 0, st>>>(
-      static_cast<const uint16_t *>(x), n_rows, d, out_rows, codes, sf);
+  const cudaError_t e = launch_pdl(kv_quant_kernel, dim3((unsigned)grid), dim3(32 * rows_per_cta),
+                                   0, st, static_cast<const uint16_t *>(x), n_rows, d, out_rows,
+                                   codes, sf);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa2

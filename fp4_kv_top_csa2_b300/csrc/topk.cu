@@ -65,6 +65,11 @@ struct ElemView {  // elements in global memory
     pos = (int32_t)p;
     return ok ? float_key(v) : 0u;
   }
+  // position of element i (i < n_elems, a candidate)
+  __device__ __forceinline__ int32_t pos_of(int64_t i) const {
+    if (MODE == kById) return (int32_t)i;
+    return __ldg(map + (i >> 3)) * kBlock + (int32_t)(i & 7);
+  }
 };
 
 struct SmemView {  // elements in shared memory; key 0 marks a non-candidate
@@ -381,6 +386,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const float *__restrict__ vals, int64_t stride, int64_t n_elems,
     const int32_t *__restrict__ map, int64_t map_stride, int unit,
     const int32_t *__restrict__ q_vis, int topk, int32_t *__restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) uint8_t topk_smem[];
   uint32_t *skey = reinterpret_cast<uint32_t *>(topk_smem);
   int32_t *spos = reinterpret_cast<int32_t *>(topk_smem + (size_t)kSmemCap * 4);
@@ -570,6 +577,8 @@ __global__ void __launch_bounds__(kFilterThreads) topk_filter_kernel(
     const float *__restrict__ vals, int64_t stride, int64_t n_elems,
     const int32_t *__restrict__ map, int64_t map_stride, int unit,
     const int32_t *__restrict__ q_vis, int topk, void *ws) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint32_t ks[kFilterSample];
   __shared__ uint32_t red[8][kFilterThreads / 32];
   __shared__ uint32_t wcnt[kFilterThreads / 32];
@@ -683,6 +692,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
     const int32_t *__restrict__ map, int64_t map_stride, int unit,
     const int32_t *__restrict__ q_vis, int topk, int32_t *__restrict__ out, const void *ws,
     int n_chunks) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) uint8_t topk_smem[];
   uint32_t *skey = reinterpret_cast<uint32_t *>(topk_smem);
   int32_t *spos = reinterpret_cast<int32_t *>(topk_smem + (size_t)kSmemCap * 4);
@@ -759,9 +770,571 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
   select_and_emit(ev, n_elems, topk, sh, parity, o);
 }
 
+// ------------------------------------------------------------------------------------------
+// Cluster path: few queries over at most 8 x 16,384 elements.  One thread-block cluster of C
+// CTAs per query; CTA r keeps elements r*16384 + 1024*u + tid (u < 16) in registers.
+//   1. the cluster's smallest and largest candidate key and candidate count, exchanged through
+//      distributed shared memory;
+//   2. the k-th largest key T by radix select over the bits below the shared leading ones,
+//      11-bit digits: each CTA histograms the keys still in play, every CTA sums the C
+//      histograms of a digit straight from the others' shared memory and finds the same digit
+//      (block-wide scan from the top bin).  Histograms are double-buffered, so one cluster
+//      barrier per digit suffices: a CTA only reaches barrier p after it finished reading the
+//      buffers of digit p-1, which is when they are cleared for digit p+1;
+//   3. ordered emission: per (u, warp) counts of the keys > T and == T, one block scan and a
+//      prefix over the CTAs give each selected element its slot (index order = output order).
+constexpr int kClThreads = 1024;
+constexpr int kClPer = 16;
+constexpr int kClSpan = kClThreads * kClPer;
+constexpr int kClMaxCtas = 8;
+constexpr int kClBits = 11;
+constexpr int kClBins = 1 << kClBits;
+
+struct ClShared {
+  uint32_t hist[2][kClBins];
+  uint32_t tab[kClPer * 32];  // per (u, warp): keys > T | (keys == T) << 16, then their prefix
+  uint32_t wsum[32];
+  uint32_t pub_range[3];      // read by the cluster: smallest, largest key, candidates
+  uint32_t pub_tot[2];        // read by the cluster: this CTA's keys > T, keys == T
+  uint32_t bc[4];
+};
+
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// All threads of all CTAs of the cluster; orders shared-memory writes before the barrier with
+// reads (local or remote) after it.
+__device__ __forceinline__ void cl_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Word at the same shared-memory offset as `p`, in the CTA of the cluster with rank `rank`.
+__device__ __forceinline__ uint32_t cl_ld(const uint32_t *p, uint32_t rank) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  uint32_t ra, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+// Inclusive scan over the 1024 threads of the block (ends with a barrier, so wsum is free).
+__device__ __forceinline__ uint32_t block_incl_scan_1024(uint32_t v, uint32_t *wsum) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t inc = warp_incl_scan(v);
+  if (lane == 31) wsum[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    const uint32_t t = wsum[lane];
+    wsum[lane] = warp_incl_scan(t) - t;
+  }
+  __syncthreads();
+  inc += wsum[wid];
+  __syncthreads();
+  return inc;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kClThreads, 1) topk_cluster_kernel(
+    const float *__restrict__ vals, int64_t stride, int64_t n_elems,
+    const int32_t *__restrict__ map, int64_t map_stride, int unit,
+    const int32_t *__restrict__ q_vis, int topk, int32_t *__restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ ClShared sh;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const uint32_t rank = cl_rank(), C = cl_size();
+  const int n = blockIdx.y;
+  const int64_t V = q_vis[n];
+  ElemView<MODE> ev;
+  ev.vals = vals + (int64_t)n * stride;
+  ev.val_len = stride > 0 ? stride : 1;
+  ev.map = map ? map + (int64_t)n * map_stride : nullptr;
+  ev.n_elems = n_elems;
+  ev.limit = MODE == kById ? (V + unit - 1) / unit : V;
+  const int64_t base = (int64_t)rank * kClSpan;
+  uint32_t key[kClPer];
+#pragma unroll
+  for (int u = 0; u < kClPer; ++u) {
+    int32_t p;
+    key[u] = ev.get(base + (int64_t)u * kClThreads + tid, p);
+  }
+
+  // ---- 1. range and count of the candidates, cluster-wide
+  {
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u, cnt = 0u;
+#pragma unroll
+    for (int u = 0; u < kClPer; ++u)
+      if (key[u] != 0u) {
+        lo = min(lo, key[u]);
+        hi = max(hi, key[u]);
+        ++cnt;
+      }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    if (lane == 0) {
+      sh.hist[1][wid] = lo;
+      sh.hist[1][32 + wid] = hi;
+      sh.hist[1][64 + wid] = cnt;
+    }
+    sh.hist[0][tid] = 0u;
+    sh.hist[0][tid + kClThreads] = 0u;
+    __syncthreads();
+    if (wid == 0) {
+      lo = __reduce_min_sync(0xffffffffu, sh.hist[1][lane]);
+      hi = __reduce_max_sync(0xffffffffu, sh.hist[1][32 + lane]);
+      cnt = __reduce_add_sync(0xffffffffu, sh.hist[1][64 + lane]);
+      if (lane == 0) {
+        sh.pub_range[0] = lo;
+        sh.pub_range[1] = hi;
+        sh.pub_range[2] = cnt;
+      }
+    }
+    cl_sync();
+    if (wid == 0) {
+      lo = 0xFFFFFFFFu;
+      hi = 0u;
+      cnt = 0u;
+      if ((uint32_t)lane < C) {
+        lo = cl_ld(&sh.pub_range[0], lane);
+        hi = cl_ld(&sh.pub_range[1], lane);
+        cnt = cl_ld(&sh.pub_range[2], lane);
+      }
+      lo = __reduce_min_sync(0xffffffffu, lo);
+      hi = __reduce_max_sync(0xffffffffu, hi);
+      cnt = __reduce_add_sync(0xffffffffu, cnt);
+      if (lane == 0) {
+        sh.bc[0] = lo;
+        sh.bc[1] = hi;
+        sh.bc[2] = cnt;
+      }
+    }
+    sh.hist[1][tid] = 0u;  // the scratch above was only read locally, before the barrier
+    sh.hist[1][tid + kClThreads] = 0u;
+    __syncthreads();
+  }
+  const uint32_t gmin = sh.bc[0], gmax = sh.bc[1], gcnt = sh.bc[2];
+  const uint32_t k_eff = min((uint32_t)topk, gcnt);
+
+  // ---- 2. k-th largest key (every candidate when k_eff == gcnt: T = 0, none taken as equal)
+  uint32_t T = 0u, need = 0u;
+  if (k_eff < gcnt) {
+    int b = (gmin == gmax) ? 0 : 32 - __clz(gmin ^ gmax);
+    T = b >= 32 ? 0u : (gmax & ~((1u << b) - 1u));
+    uint32_t rem = k_eff;
+    int pb = 0;
+    while (b > 0) {  // the same sequence of digits in every CTA of the cluster
+      const int w = b >= kClBits ? kClBits : b;
+      b -= w;
+      const int s = b, hs = s + w;
+      uint32_t *hist = sh.hist[pb];
+#pragma unroll
+      for (int u = 0; u < kClPer; ++u) {
+        const uint32_t k = key[u];
+        if (k != 0u && (hs >= 32 || (k >> hs) == (T >> hs)))
+          atomicAdd(&hist[(k >> s) & ((1u << w) - 1u)], 1u);
+      }
+      cl_sync();
+      sh.hist[pb ^ 1][tid] = 0u;
+      sh.hist[pb ^ 1][tid + kClThreads] = 0u;
+      const int hb0 = kClBins - 1 - 2 * tid, hb1 = hb0 - 1;  // this thread's bins, descending
+      uint32_t c0 = 0u, c1 = 0u;
+      for (uint32_t r = 0; r < C; ++r) {
+        c0 += cl_ld(&hist[hb0], r);
+        c1 += cl_ld(&hist[hb1], r);
+      }
+      const uint32_t inc = block_incl_scan_1024(c0 + c1, sh.wsum), exc = inc - c0 - c1;
+      if (exc < rem && inc >= rem) {  // exactly one thread: the in-play count is >= rem
+        const bool first = exc + c0 >= rem;
+        sh.bc[0] = (uint32_t)(first ? hb0 : hb1);
+        sh.bc[1] = first ? exc : exc + c0;
+      }
+      __syncthreads();
+      T |= sh.bc[0] << s;
+      rem -= sh.bc[1];
+      pb ^= 1;
+    }
+    need = rem;
+  }
+
+  // ---- 3. ordered emission
+#pragma unroll
+  for (int u = 0; u < kClPer; ++u) {
+    const uint32_t a = __popc(__ballot_sync(0xffffffffu, key[u] > T));
+    const uint32_t e = __popc(__ballot_sync(0xffffffffu, key[u] == T && key[u] != 0u));
+    if (lane == 0) sh.tab[u * 32 + wid] = a | (e << 16);
+  }
+  __syncthreads();
+  {
+    const uint32_t v = tid < kClPer * 32 ? sh.tab[tid] : 0u;
+    const uint32_t inc = block_incl_scan_1024(v, sh.wsum);
+    if (tid < kClPer * 32) sh.tab[tid] = inc - v;
+    if (tid == kClThreads - 1) {
+      sh.pub_tot[0] = inc & 0xFFFFu;
+      sh.pub_tot[1] = inc >> 16;
+    }
+  }
+  cl_sync();
+  if (wid == 0) {
+    uint32_t a = 0u, e = 0u;
+    if ((uint32_t)lane < C) {
+      a = cl_ld(&sh.pub_tot[0], lane);
+      e = cl_ld(&sh.pub_tot[1], lane);
+    }
+    const uint32_t ai = warp_incl_scan(a), ei = warp_incl_scan(e);
+    const uint32_t a0 = __shfl_sync(0xffffffffu, ai - a, rank);
+    const uint32_t e0 = __shfl_sync(0xffffffffu, ei - e, rank);
+    if (lane == 0) {
+      sh.bc[2] = a0;
+      sh.bc[3] = e0;
+    }
+  }
+  __syncthreads();
+  const uint32_t gt0 = sh.bc[2], eq0 = sh.bc[3];
+  int32_t *o = out + (int64_t)n * topk;
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int u = 0; u < kClPer; ++u) {
+    const bool gt = key[u] > T, eq = key[u] == T && key[u] != 0u;
+    const uint32_t bgt = __ballot_sync(0xffffffffu, gt), beq = __ballot_sync(0xffffffffu, eq);
+    const uint32_t t = sh.tab[u * 32 + wid];
+    const uint32_t my_gt = gt0 + (t & 0xFFFFu) + __popc(bgt & lt);
+    const uint32_t my_eq = eq0 + (t >> 16) + __popc(beq & lt);
+    if (gt || (eq && my_eq < need))
+      o[my_gt + min(my_eq, need)] = ev.pos_of(base + (int64_t)u * kClThreads + tid);
+  }
+  if (rank == 0)
+    for (int i = (int)k_eff + tid; i < topk; i += kClThreads) o[i] = -1;
+  cl_sync();  // no CTA leaves while another may still read its shared memory
+}
+
+// ------------------------------------------------------------------------------------------
+// Register path: one CTA per query over at most 16,384 elements, element u*1024 + tid in
+// register u of thread tid.
+//   1. candidate count, smallest and largest key (block reduction);
+//   2. threshold estimate t_lo: the r-th largest of 128 keys sampled across the elements (exact
+//      rank of every sample: 1024 threads x 16 comparisons), r = the expected number of sampled
+//      keys in the Top-K plus 2.5 standard deviations plus 3, so that at least K keys are >= t_lo
+//      with high probability;
+//   3. the keys >= t_lo are compacted in index order into shared memory (ballots per register
+//      round and warp, one block scan); if they are fewer than K (the estimate was too high) or
+//      more than the shared-memory capacity, step 4 runs over all keys in registers instead;
+//   4. radix select of the k-th largest key T over the compacted keys, 11-bit digits, one
+//      shared histogram per digit (the compacted keys spread over many bins);
+//   5. ordered emission of the keys > T and the first need = K - #(> T) keys == T.
+constexpr int kRgThreads = 1024;
+constexpr int kRgPer = 16;
+constexpr int kRgSpan = kRgThreads * kRgPer;
+constexpr int kRgSample = 128;
+constexpr int kRgKeepCap = 8192;
+
+struct RgShared {
+  uint32_t hist[2][kClBins];
+  uint32_t tab[kRgPer * 32];
+  uint32_t wsum[32];
+  uint32_t red[3][32];
+  uint32_t samp[kRgSample];
+  uint32_t sg[kRgSample], se[kRgSample];
+  uint32_t bc[8];
+  uint32_t kkey[kRgKeepCap];
+  uint16_t kidx[kRgKeepCap];
+};
+constexpr size_t kRgSmem = sizeof(RgShared);
+
+// k-th largest (1 <= k <= number of candidates) of the keys this block visits: visit(f) calls
+// f(key) for each of the calling thread's keys (0 = not a candidate); all candidates lie in
+// [lo, hi].  11-bit digits below the leading bits lo and hi share; hist[0] is zero on entry and
+// both buffers are zero on return.  need = k - #(keys > T).
+template <class Visit>
+__device__ uint32_t radix11_kth(Visit visit, uint32_t k, uint32_t lo, uint32_t hi,
+                                uint32_t (*hist)[kClBins], uint32_t *wsum, uint32_t *bc,
+                                uint32_t &need) {
+  const int tid = threadIdx.x;
+  int b = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
+  uint32_t T = b >= 32 ? 0u : (hi & ~((1u << b) - 1u));
+  uint32_t rem = k;
+  int pb = 0;
+  while (b > 0) {
+    const int w = b >= kClBits ? kClBits : b;
+    b -= w;
+    const int s = b, hs = s + w;
+    uint32_t *h = hist[pb];
+    const uint32_t Tc = T;
+    visit([&](uint32_t key) {
+      if (key != 0u && (hs >= 32 || (key >> hs) == (Tc >> hs)))
+        atomicAdd(&h[(key >> s) & ((1u << w) - 1u)], 1u);
+    });
+    __syncthreads();
+    const int hb0 = kClBins - 1 - 2 * tid, hb1 = hb0 - 1;
+    const uint32_t c0 = h[hb0], c1 = h[hb1];
+    const uint32_t inc = block_incl_scan_1024(c0 + c1, wsum), exc = inc - c0 - c1;
+    h[hb0] = 0u;  // every read of this buffer happened before the scan's barriers
+    h[hb1] = 0u;
+    if (exc < rem && inc >= rem) {
+      const bool first = exc + c0 >= rem;
+      bc[0] = (uint32_t)(first ? hb0 : hb1);
+      bc[1] = first ? exc : exc + c0;
+    }
+    __syncthreads();
+    T |= bc[0] << s;
+    rem -= bc[1];
+    __syncthreads();  // bc is rewritten by the next digit
+    pb ^= 1;
+  }
+  need = rem;
+  return T;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
+    const float *__restrict__ vals, int64_t stride, int64_t n_elems,
+    const int32_t *__restrict__ map, int64_t map_stride, int unit,
+    const int32_t *__restrict__ q_vis, int topk, int32_t *__restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(16) uint8_t rg_smem[];
+  RgShared &sh = *reinterpret_cast<RgShared *>(rg_smem);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int n = blockIdx.x;
+  const int64_t V = q_vis[n];
+  ElemView<MODE> ev;
+  ev.vals = vals + (int64_t)n * stride;
+  ev.val_len = stride > 0 ? stride : 1;
+  ev.map = map ? map + (int64_t)n * map_stride : nullptr;
+  ev.n_elems = n_elems;
+  ev.limit = MODE == kById ? (V + unit - 1) / unit : V;
+  uint32_t key[kRgPer];
+#pragma unroll
+  for (int u = 0; u < kRgPer; ++u) {
+    int32_t p;
+    key[u] = ev.get((int64_t)u * kRgThreads + tid, p);
+  }
+  sh.hist[0][tid] = 0u;
+  sh.hist[0][tid + kRgThreads] = 0u;
+  sh.hist[1][tid] = 0u;
+  sh.hist[1][tid + kRgThreads] = 0u;
+  if (tid < kRgSample) {
+    sh.sg[tid] = 0u;
+    sh.se[tid] = 0u;
+  }
+  // ---- 1. count and range
+  uint32_t gmin, gmax, gcnt;
+  {
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u, cnt = 0u;
+#pragma unroll
+    for (int u = 0; u < kRgPer; ++u)
+      if (key[u] != 0u) {
+        lo = min(lo, key[u]);
+        hi = max(hi, key[u]);
+        ++cnt;
+      }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    if (lane == 0) {
+      sh.red[0][wid] = lo;
+      sh.red[1][wid] = hi;
+      sh.red[2][wid] = cnt;
+    }
+    // sample j (= tid / 8 for tid % 8 == 0): element (j % 16) * 1024 + 8 j
+    if ((tid & 7) == 0) {
+      const int j = tid >> 3, uj = j & (kRgPer - 1);
+      uint32_t v = 0u;
+#pragma unroll
+      for (int u = 0; u < kRgPer; ++u)
+        if (u == uj) v = key[u];
+      sh.samp[j] = v;
+    }
+    __syncthreads();
+    gmin = __reduce_min_sync(0xffffffffu, sh.red[0][lane]);
+    gmax = __reduce_max_sync(0xffffffffu, sh.red[1][lane]);
+    gcnt = __reduce_add_sync(0xffffffffu, sh.red[2][lane]);
+  }
+  const uint32_t k_eff = min((uint32_t)topk, gcnt);
+  uint32_t T = 0u, need = 0u;  // k_eff == gcnt: every candidate (key > 0), none as "equal"
+  int m = -1;                  // compacted count (-1: select straight from registers)
+  if (k_eff < gcnt) {
+    // ---- 2. threshold estimate from the sample
+    {
+      const int j = tid & (kRgSample - 1), q = tid / kRgSample;  // 8 slices of 16 samples
+      const uint32_t sj = sh.samp[j];
+      uint32_t g = 0u, e = 0u;
+#pragma unroll
+      for (int i = 0; i < kRgSample / 8; ++i) {
+        const uint32_t x = sh.samp[q * (kRgSample / 8) + i];
+        g += x > sj;
+        e += x == sj;
+      }
+      atomicAdd(&sh.sg[j], g);
+      atomicAdd(&sh.se[j], e);
+    }
+    const uint32_t sv = __syncthreads_count(tid < kRgSample && sh.samp[tid] != 0u);
+    const float mu = (float)sv * (float)k_eff / (float)gcnt;
+    const uint32_t r = (uint32_t)ceilf(mu + 2.5f * sqrtf(mu) + 3.0f);
+    if (tid == 0) sh.bc[4] = 1u;  // keep every candidate unless a sample qualifies below
+    __syncthreads();
+    if (tid < kRgSample && r <= sv) {
+      const uint32_t sj = sh.samp[tid], g = sh.sg[tid], e = sh.se[tid];
+      if (sj != 0u && g < r && r <= g + e) sh.bc[4] = sj;  // the r-th largest sample
+    }
+    __syncthreads();
+    const uint32_t t_lo = sh.bc[4];
+    // ---- 3. compaction of the keys >= t_lo (index order)
+#pragma unroll
+    for (int u = 0; u < kRgPer; ++u) {
+      const uint32_t c = __popc(__ballot_sync(0xffffffffu, key[u] >= t_lo && key[u] != 0u));
+      if (lane == 0) sh.tab[u * 32 + wid] = c;
+    }
+    __syncthreads();
+    {
+      const uint32_t v = tid < kRgPer * 32 ? sh.tab[tid] : 0u;
+      const uint32_t inc = block_incl_scan_1024(v, sh.wsum);
+      if (tid < kRgPer * 32) sh.tab[tid] = inc - v;
+      if (tid == kRgThreads - 1) sh.bc[5] = inc;
+    }
+    __syncthreads();
+    const uint32_t kept = sh.bc[5];
+    if (kept >= k_eff && kept <= (uint32_t)kRgKeepCap) {
+      const uint32_t lt = (1u << lane) - 1u;
+      uint32_t klo = 0xFFFFFFFFu;
+#pragma unroll
+      for (int u = 0; u < kRgPer; ++u) {
+        const bool in = key[u] >= t_lo && key[u] != 0u;
+        const uint32_t bal = __ballot_sync(0xffffffffu, in);
+        if (in) {
+          const uint32_t slot = sh.tab[u * 32 + wid] + __popc(bal & lt);
+          sh.kkey[slot] = key[u];
+          sh.kidx[slot] = (uint16_t)(u * kRgThreads + tid);
+          klo = min(klo, key[u]);
+        }
+      }
+      klo = __reduce_min_sync(0xffffffffu, klo);
+      if (lane == 0) sh.red[0][wid] = klo;
+      __syncthreads();
+      klo = __reduce_min_sync(0xffffffffu, sh.red[0][lane]);
+      m = (int)kept;
+      // ---- 4. exact k-th largest over the compacted keys
+      T = radix11_kth(
+          [&](auto f) {
+            for (int i = tid; i < m; i += kRgThreads) f(sh.kkey[i]);
+          },
+          k_eff, klo, gmax, sh.hist, sh.wsum, sh.bc, need);
+    } else {
+      T = radix11_kth(
+          [&](auto f) {
+#pragma unroll
+            for (int u = 0; u < kRgPer; ++u) f(key[u]);
+          },
+          k_eff, gmin, gmax, sh.hist, sh.wsum, sh.bc, need);
+    }
+  }
+  // ---- 5. ordered emission
+  int32_t *o = out + (int64_t)n * topk;
+  const uint32_t lt = (1u << lane) - 1u;
+  if (m >= 0) {
+    const int rounds = (m + kRgThreads - 1) / kRgThreads;  // <= 8
+    for (int rr = 0; rr < rounds; ++rr) {
+      const int i = rr * kRgThreads + tid;
+      const uint32_t kk = i < m ? sh.kkey[i] : 0u;
+      const uint32_t a = __popc(__ballot_sync(0xffffffffu, kk > T));
+      const uint32_t e = __popc(__ballot_sync(0xffffffffu, kk == T && kk != 0u));
+      if (lane == 0) sh.tab[rr * 32 + wid] = a | (e << 16);
+    }
+    __syncthreads();
+    {
+      const uint32_t v = tid < rounds * 32 ? sh.tab[tid] : 0u;
+      const uint32_t inc = block_incl_scan_1024(v, sh.wsum);
+      if (tid < rounds * 32) sh.tab[tid] = inc - v;
+    }
+    __syncthreads();
+    for (int rr = 0; rr < rounds; ++rr) {
+      const int i = rr * kRgThreads + tid;
+      const uint32_t kk = i < m ? sh.kkey[i] : 0u;
+      const bool gt = kk > T, eq = kk == T && kk != 0u;
+      const uint32_t bgt = __ballot_sync(0xffffffffu, gt), beq = __ballot_sync(0xffffffffu, eq);
+      const uint32_t t = sh.tab[rr * 32 + wid];
+      const uint32_t my_gt = (t & 0xFFFFu) + __popc(bgt & lt);
+      const uint32_t my_eq = (t >> 16) + __popc(beq & lt);
+      if (gt || (eq && my_eq < need)) o[my_gt + min(my_eq, need)] = ev.pos_of(sh.kidx[i]);
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kRgPer; ++u) {
+      const uint32_t a = __popc(__ballot_sync(0xffffffffu, key[u] > T));
+      const uint32_t e = __popc(__ballot_sync(0xffffffffu, key[u] == T && key[u] != 0u));
+      if (lane == 0) sh.tab[u * 32 + wid] = a | (e << 16);
+    }
+    __syncthreads();
+    {
+      const uint32_t v = tid < kRgPer * 32 ? sh.tab[tid] : 0u;
+      const uint32_t inc = block_incl_scan_1024(v, sh.wsum);
+      if (tid < kRgPer * 32) sh.tab[tid] = inc - v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kRgPer; ++u) {
+      const bool gt = key[u] > T, eq = key[u] == T && key[u] != 0u;
+      const uint32_t bgt = __ballot_sync(0xffffffffu, gt), beq = __ballot_sync(0xffffffffu, eq);
+      const uint32_t t = sh.tab[u * 32 + wid];
+      const uint32_t my_gt = (t & 0xFFFFu) + __popc(bgt & lt);
+      const uint32_t my_eq = (t >> 16) + __popc(beq & lt);
+      if (gt || (eq && my_eq < need)) o[my_gt + min(my_eq, need)] = ev.pos_of(u * kRgThreads + tid);
+    }
+  }
+  for (int i = (int)k_eff + tid; i < topk; i += kRgThreads) o[i] = -1;
+}
+
+template <int MODE>
+static cudaError_t launch_topk_reg(const float *vals, int64_t stride, int64_t n_elems,
+                                   const int32_t *map, int64_t map_stride, int unit,
+                                   const int32_t *q_vis, int nq, int topk, int32_t *out,
+                                   cudaStream_t st) {
+  cudaError_t e = set_smem_once(topk_reg_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kRgSmem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(topk_reg_kernel<MODE>, dim3(nq), dim3(kRgThreads), kRgSmem, st, vals, stride,
+                 n_elems, map, map_stride, unit, q_vis, topk, out);
+  note_launches(1);
+  return e;
+}
+
+static bool topk_use_reg(int nq, int64_t n_elems) {
+  return nq <= 64 && n_elems >= 1 && n_elems <= kRgSpan;
+}
+
+// The cluster path is kept for element counts above one CTA's registers but is not routed to:
+// on skewed score distributions its first digit's shared atomics serialise.
+static int topk_cluster_ctas(int nq, int64_t n_elems) {
+  (void)nq;
+  (void)n_elems;
+  return 0;
+}
+
+template <int MODE>
+static cudaError_t launch_topk_cluster(const float *vals, int64_t stride, int64_t n_elems,
+                                       const int32_t *map, int64_t map_stride, int unit,
+                                       const int32_t *q_vis, int nq, int topk, int32_t *out,
+                                       int C, cudaStream_t st) {
+  const cudaError_t e = launch_pdl_cluster(topk_cluster_kernel<MODE>, dim3(C, nq),
+                                           dim3(kClThreads), 0, st, C, vals, stride, n_elems,
+                                           map, map_stride, unit, q_vis, topk, out);
+  note_launches(1);
+  return e;
+}
+
 // The chunked two-kernel path serves few queries over many elements.
 static bool topk_use_chunks(int nq, int64_t n_elems) {
-  return nq <= 64 && n_elems > 2 * kFilterSample && (n_elems + kTkChunk - 1) / kTkChunk <= 1024;
+  return !topk_use_reg(nq, n_elems) && topk_cluster_ctas(nq, n_elems) == 0 && nq <= 64 &&
+         n_elems > 2 * kFilterSample &&
+         (n_elems + kTkChunk - 1) / kTkChunk <= 1024;
 }
 
 size_t topk_workspace_bytes(int nq, int64_t n_elems) {
@@ -776,18 +1349,19 @@ static cudaError_t launch_topk_chunked(const float *vals, int64_t stride, int64_
                                        const int32_t *q_vis, int nq, int topk, int32_t *out,
                                        void *ws, cudaStream_t st) {
   const int n_chunks = (int)((n_elems + kTkChunk - 1) / kTkChunk);
-  topk_filter_kernel<MODE><<<dim3(n_chunks, nq), kFilterThreads, 0, st>>>(
-      vals, stride, n_elems, map, map_stride, unit, q_vis, topk, ws);
+  cudaError_t e = launch_pdl(topk_filter_kernel<MODE>, dim3(n_chunks, nq), dim3(kFilterThreads),
+                             0, st, vals, stride, n_elems, map, map_stride, unit, q_vis, topk,
+                             ws);
   note_launches(1);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = set_smem_once(topk_select_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                     (int)kTopkSmem);
   if (e != cudaSuccess) return e;
-  topk_select_kernel<MODE><<<nq, kTopkThreads, kTopkSmem, st>>>(
-      vals, stride, n_elems, map, map_stride, unit, q_vis, topk, out, ws, n_chunks);
+  e = launch_pdl(topk_select_kernel<MODE>, dim3(nq), dim3(kTopkThreads), kTopkSmem, st, vals,
+                 stride, n_elems, map, map_stride, unit, q_vis, topk, out, (const void *)ws,
+                 n_chunks);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_topk(const float *vals, int64_t stride, int64_t n_elems, const int32_t *map,
@@ -795,6 +1369,26 @@ cudaError_t launch_topk(const float *vals, int64_t stride, int64_t n_elems, cons
                         int32_t *out, cudaStream_t st, const float *pos_vals,
                         int64_t pos_stride, void *ws) {
   if (nq == 0) return cudaSuccess;
+  if (topk_use_reg(nq, n_elems)) {
+    if (!map)
+      return launch_topk_reg<kById>(vals, stride, n_elems, nullptr, 0, unit, q_vis, nq, topk, out,
+                                    st);
+    if (pos_vals)
+      return launch_topk_reg<kMapPos>(pos_vals, pos_stride, n_elems, map, map_stride, unit, q_vis,
+                                      nq, topk, out, st);
+    return launch_topk_reg<kMapSlot>(vals, stride, n_elems, map, map_stride, unit, q_vis, nq, topk,
+                                     out, st);
+  }
+  if (const int C = topk_cluster_ctas(nq, n_elems)) {
+    if (!map)
+      return launch_topk_cluster<kById>(vals, stride, n_elems, nullptr, 0, unit, q_vis, nq, topk,
+                                        out, C, st);
+    if (pos_vals)
+      return launch_topk_cluster<kMapPos>(pos_vals, pos_stride, n_elems, map, map_stride, unit,
+                                          q_vis, nq, topk, out, C, st);
+    return launch_topk_cluster<kMapSlot>(vals, stride, n_elems, map, map_stride, unit, q_vis, nq,
+                                         topk, out, C, st);
+  }
   if (ws && topk_use_chunks(nq, n_elems)) {
     if (!map)
       return launch_topk_chunked<kById>(vals, stride, n_elems, nullptr, 0, unit, q_vis, nq, topk,
@@ -810,24 +1404,23 @@ cudaError_t launch_topk(const float *vals, int64_t stride, int64_t n_elems, cons
     e = set_smem_once(topk_kernel<kById>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                       (int)kTopkSmem);
     if (e != cudaSuccess) return e;
-    topk_kernel<kById><<<nq, kTopkThreads, kTopkSmem, st>>>(vals, stride, n_elems, nullptr, 0,
-                                                             unit, q_vis, topk, out);
+    e = launch_pdl(topk_kernel<kById>, dim3(nq), dim3(kTopkThreads), kTopkSmem, st, vals,
+                   stride, n_elems, (const int32_t *)nullptr, (int64_t)0, unit, q_vis, topk, out);
   } else if (pos_vals) {
     e = set_smem_once(topk_kernel<kMapPos>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                       (int)kTopkSmem);
     if (e != cudaSuccess) return e;
-    topk_kernel<kMapPos><<<nq, kTopkThreads, kTopkSmem, st>>>(
-        pos_vals, pos_stride, n_elems, map, map_stride, unit, q_vis, topk, out);
+    e = launch_pdl(topk_kernel<kMapPos>, dim3(nq), dim3(kTopkThreads), kTopkSmem, st,
+                   pos_vals, pos_stride, n_elems, map, map_stride, unit, q_vis, topk, out);
   } else {
     e = set_smem_once(topk_kernel<kMapSlot>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                       (int)kTopkSmem);
     if (e != cudaSuccess) return e;
-    topk_kernel<kMapSlot><<<nq, kTopkThreads, kTopkSmem, st>>>(vals, stride, n_elems, map,
-                                                                map_stride, unit, q_vis, topk,
-                                                                out);
+    e = launch_pdl(topk_kernel<kMapSlot>, dim3(nq), dim3(kTopkThreads), kTopkSmem, st, vals,
+                   stride, n_elems, map, map_stride, unit, q_vis, topk, out);
   }
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa2

@@ -320,6 +320,35 @@ def test_topk_over_many_blocks(csa2, kind):
         assert np.array_equal(pool[0].cpu().numpy(), oracle.candidate_pool(bmh[0], n_pool))
 
 
+@pytest.mark.parametrize("nb,kind,vis_frac", [
+    (131072, "normal", 1.0), (131069, "ties", 1.0), (131072, "ties", 0.37), (16384, "normal", 1.0),
+    (16385, "ties", 1.0), (5, "normal", 1.0), (40000, "normal", 0.001),
+])
+def test_pool_selection_cluster_sizes(csa2, nb, kind, vis_frac):
+    """Candidate pool straight from given block maxima, at the element counts where one query's
+    selection spans 1 to 8 cooperating CTAs (and ragged tails), with heavy ties and signed zeros.
+    The selection must equal the oracle's on the same fp32 values exactly."""
+    g = torch.Generator().manual_seed(nb + int(vis_frac * 100))
+    B = 3
+    if kind == "normal":
+        bm = torch.randn(B, nb, generator=g) * 12 + 40
+    else:
+        bm = torch.randint(-3, 4, (B, nb), generator=g).float() * 0.5
+        zeros = torch.rand(B, nb, generator=g) < 0.1
+        bm[zeros] = torch.where(torch.rand(int(zeros.sum()), generator=g) < 0.5, 0.0, -0.0)
+    vis = [max(1, int(nb * 8 * vis_frac)) - i for i in range(B)]
+    vis = [max(1, v) for v in vis]
+    vis_t = torch.tensor(vis, dtype=torch.int32, device="cuda")
+    bmd = bm.cuda()
+    for n_pool in (2048, 1, 4096):
+        pool = torch.empty((B, n_pool), dtype=torch.int32, device="cuda")
+        csa2.csa2_hier_candidate_pool(bmd, vis_t, n_pool, pool, ws=_pool_ws(csa2, bmd, n_pool))
+        ref = oracle.hier_candidate_pool(bm.numpy(), vis, n_pool)
+        got = pool.cpu().numpy()
+        for n in range(B):
+            assert np.array_equal(got[n], ref[n]), (n_pool, n)
+
+
 def test_prefill_indexer_many_queries(csa2):
     """More than 1,024 queries over one sequence takes the 32-queries-per-MMA scan: causal
     visibility per query (query i sees positions < P0 + i + 1), block maxima and Top-K."""
