@@ -99,7 +99,74 @@ struct TopkShared {
   uint32_t s_a, s_b;
   uint32_t hist[8][256];
   uint32_t bcast[2];
+  uint32_t hist11[2][2048];  // radix11_kth (zero between uses)
+  uint32_t tab[512];
+  uint32_t wsum[32];
+  uint32_t bc[4];
 };
+
+constexpr int kClBits = 11;  // radix digit width of the register and shared-memory selections
+constexpr int kClBins = 1 << kClBits;
+
+// Inclusive scan over the 1024 threads of the block (ends with a barrier, so wsum is free).
+__device__ __forceinline__ uint32_t block_incl_scan_1024(uint32_t v, uint32_t *wsum) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t inc = warp_incl_scan(v);
+  if (lane == 31) wsum[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    const uint32_t t = wsum[lane];
+    wsum[lane] = warp_incl_scan(t) - t;
+  }
+  __syncthreads();
+  inc += wsum[wid];
+  __syncthreads();
+  return inc;
+}
+
+// k-th largest (1 <= k <= number of candidates) of the keys this block visits: visit(f) calls
+// f(key) for each of the calling thread's keys (0 = not a candidate); all candidates lie in
+// [lo, hi].  11-bit digits below the leading bits lo and hi share; hist[0] is zero on entry and
+// both buffers are zero on return.  need = k - #(keys > T).
+template <class Visit>
+__device__ uint32_t radix11_kth(Visit visit, uint32_t k, uint32_t lo, uint32_t hi,
+                                uint32_t (*hist)[kClBins], uint32_t *wsum, uint32_t *bc,
+                                uint32_t &need) {
+  const int tid = threadIdx.x;
+  int b = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
+  uint32_t T = b >= 32 ? 0u : (hi & ~((1u << b) - 1u));
+  uint32_t rem = k;
+  int pb = 0;
+  while (b > 0) {
+    const int w = b >= kClBits ? kClBits : b;
+    b -= w;
+    const int s = b, hs = s + w;
+    uint32_t *h = hist[pb];
+    const uint32_t Tc = T;
+    visit([&](uint32_t key) {
+      if (key != 0u && (hs >= 32 || (key >> hs) == (Tc >> hs)))
+        atomicAdd(&h[(key >> s) & ((1u << w) - 1u)], 1u);
+    });
+    __syncthreads();
+    const int hb0 = kClBins - 1 - 2 * tid, hb1 = hb0 - 1;
+    const uint32_t c0 = h[hb0], c1 = h[hb1];
+    const uint32_t inc = block_incl_scan_1024(c0 + c1, wsum), exc = inc - c0 - c1;
+    h[hb0] = 0u;  // every read of this buffer happened before the scan's barriers
+    h[hb1] = 0u;
+    if (exc < rem && inc >= rem) {
+      const bool first = exc + c0 >= rem;
+      bc[0] = (uint32_t)(first ? hb0 : hb1);
+      bc[1] = first ? exc : exc + c0;
+    }
+    __syncthreads();
+    T |= bc[0] << s;
+    rem -= bc[1];
+    __syncthreads();  // bc is rewritten by the next digit
+    pb ^= 1;
+  }
+  need = rem;
+  return T;
+}
 
 // Counts of candidates with key >= cand[j] (j < NT) over the view, block-wide.
 template <int NT, class View>
@@ -342,21 +409,71 @@ __device__ __forceinline__ void start_bits(const SmemView &sv, int64_t n, TopkSh
   b = (kmin == kmax) ? 0 : 32 - __clz(kmin ^ kmax);  // bits below the shared leading ones
 }
 
-// Shared-memory set: k-th key by radix select, then the ordered emission.
+// Shared-memory set (at most 16,384 elements in index order, 1024 threads; sh.hist11 zero on
+// entry and on return): count and range, the k-th largest key by radix11_kth, then the ordered
+// emission -- per (round, warp) counts of the keys > T and == T, one block scan, and every
+// selected element's output slot from its ballots.
 __device__ void select_and_emit(const SmemView &sv, int64_t n_elems, int topk, TopkShared &sh,
                                 int &parity, int32_t *o) {
-  uint32_t cand1[1] = {1u}, nv[1];
-  count_ge_n<1>(sv, n_elems, cand1, nv, sh, parity);
-  const uint32_t k_eff = min((uint32_t)topk, nv[0]);
-  if (k_eff > 0) {
-    uint32_t kmin, kmax;
-    key_range(sv, n_elems, sh, parity, kmin, kmax);
-    const int b = (kmin == kmax) ? 0 : 32 - __clz(kmin ^ kmax);
-    uint32_t need_eq;
-    const uint32_t T = kth_radix(sv.key, (int)n_elems, k_eff, kmax, b, sh.hist, sh.bcast, &need_eq);
-    ordered_emit(sv, n_elems, T, need_eq, sh, o);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int m = (int)n_elems;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u, cnt = 0u;
+  for (int i = tid; i < m; i += kTopkThreads) {
+    const uint32_t k = sv.key[i];
+    if (k != 0u) {
+      lo = min(lo, k);
+      hi = max(hi, k);
+      ++cnt;
+    }
   }
-  for (int i = (int)k_eff + threadIdx.x; i < topk; i += kTopkThreads) o[i] = -1;
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  if (lane == 0) {
+    sh.red[parity][0][wid] = lo;
+    sh.red[parity][1][wid] = hi;
+    sh.red[parity][2][wid] = cnt;
+  }
+  __syncthreads();
+  lo = __reduce_min_sync(0xffffffffu, sh.red[parity][0][lane]);
+  hi = __reduce_max_sync(0xffffffffu, sh.red[parity][1][lane]);
+  cnt = __reduce_add_sync(0xffffffffu, sh.red[parity][2][lane]);
+  parity ^= 1;
+  const uint32_t k_eff = min((uint32_t)topk, cnt);
+  uint32_t T = 0u, need = 0u;  // k_eff == cnt: every candidate
+  if (k_eff < cnt)
+    T = radix11_kth(
+        [&](auto f) {
+          for (int i = tid; i < m; i += kTopkThreads) f(sv.key[i]);
+        },
+        k_eff, lo, hi, sh.hist11, sh.wsum, sh.bc, need);
+  const int rounds = (m + kTopkThreads - 1) / kTopkThreads;  // <= 16
+  for (int rr = 0; rr < rounds; ++rr) {
+    const int i = rr * kTopkThreads + tid;
+    const uint32_t kk = i < m ? sv.key[i] : 0u;
+    const uint32_t a = __popc(__ballot_sync(0xffffffffu, kk > T));
+    const uint32_t e = __popc(__ballot_sync(0xffffffffu, kk == T && kk != 0u));
+    if (lane == 0) sh.tab[rr * 32 + wid] = a | (e << 16);
+  }
+  __syncthreads();
+  {
+    const uint32_t v = tid < rounds * 32 ? sh.tab[tid] : 0u;
+    const uint32_t inc = block_incl_scan_1024(v, sh.wsum);
+    if (tid < rounds * 32) sh.tab[tid] = inc - v;
+  }
+  __syncthreads();
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int rr = 0; rr < rounds; ++rr) {
+    const int i = rr * kTopkThreads + tid;
+    const uint32_t kk = i < m ? sv.key[i] : 0u;
+    const bool gt = kk > T, eq = kk == T && kk != 0u;
+    const uint32_t bgt = __ballot_sync(0xffffffffu, gt), beq = __ballot_sync(0xffffffffu, eq);
+    const uint32_t t = sh.tab[rr * 32 + wid];
+    const uint32_t my_gt = (t & 0xFFFFu) + __popc(bgt & lt);
+    const uint32_t my_eq = (t >> 16) + __popc(beq & lt);
+    if (gt || (eq && my_eq < need)) o[my_gt + min(my_eq, need)] = sv.pos[i];
+  }
+  for (int i = (int)k_eff + tid; i < topk; i += kTopkThreads) o[i] = -1;
 }
 
 template <class View>
@@ -396,6 +513,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
 
   const int n = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  for (int i = tid; i < 2 * 2048; i += kTopkThreads) (&sh.hist11[0][0])[i] = 0u;
   int32_t *o = out + (int64_t)n * topk;
   if (n_elems <= 0) {
     for (int i = tid; i < topk; i += kTopkThreads) o[i] = -1;
@@ -552,7 +670,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
 // ------------------------------------------------------------------------------------------
 constexpr int kTkChunk = 4096;
 constexpr int kFilterThreads = 256;
-constexpr int kFilterSample = 1024;
+constexpr int kFilterSample = kFilterThreads;  // one sampled key per thread
 
 struct ChunkWs {  // per query: [n_chunks][kTkChunk] keys, positions, then [n_chunks] counts
   uint32_t *keys;
@@ -582,8 +700,7 @@ __global__ void __launch_bounds__(kFilterThreads) topk_filter_kernel(
   __shared__ uint32_t ks[kFilterSample];
   __shared__ uint32_t red[8][kFilterThreads / 32];
   __shared__ uint32_t wcnt[kFilterThreads / 32];
-  __shared__ uint32_t hist[8][256];
-  __shared__ uint32_t bcast[2];
+  __shared__ uint32_t t_sh;
   const int c = blockIdx.x, n = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int n_chunks = gridDim.x;
@@ -594,51 +711,31 @@ __global__ void __launch_bounds__(kFilterThreads) topk_filter_kernel(
   ev.map = map ? map + (int64_t)n * map_stride : nullptr;
   ev.n_elems = n_elems;
   ev.limit = MODE == kById ? (V + unit - 1) / unit : V;
-  // the shared threshold estimate: r-th largest of a strided sample of the whole array
+  // the shared threshold estimate: the r-th largest of a strided sample of the whole array,
+  // found by the exact rank of every sampled key (same sample and result in every CTA);
+  // r = the expected number of sampled keys in the Top-K + 2.5 standard deviations + 3
   const int64_t step = n_elems / kFilterSample;  // >= 2 (n_elems > 2 * kFilterSample)
-#pragma unroll
-  for (int u = 0; u < kFilterSample / kFilterThreads; ++u) {
+  {
     int32_t p;
-    ks[u * kFilterThreads + tid] = ev.get((int64_t)(u * kFilterThreads + tid) * step, p);
+    ks[tid] = ev.get((int64_t)tid * step, p);
+  }
+  if (tid == 0) t_sh = 1u;  // every candidate, unless a sampled key qualifies below
+  const uint32_t sv = __syncthreads_count(ks[tid] != 0u);
+  const float mu = fminf((float)sv, (float)topk * (float)kFilterSample / (float)n_elems);
+  const uint32_t r = (uint32_t)ceilf(mu + 2.5f * sqrtf(mu) + 3.0f);
+  if (r <= sv) {
+    const uint32_t mine = ks[tid];
+    uint32_t g = 0u, e = 0u;
+#pragma unroll 16
+    for (int j = 0; j < kFilterSample; ++j) {
+      const uint32_t x = ks[j];
+      g += x > mine;
+      e += x == mine;
+    }
+    if (mine != 0u && g < r && r <= g + e) t_sh = mine;  // equal keys write the same value
   }
   __syncthreads();
-  const int64_t r_want = (int64_t)topk * kFilterSample * 8 / (n_elems * 5) + 8;
-  const uint32_t r = (uint32_t)(r_want < kFilterSample ? r_want : kFilterSample);
-  uint32_t t_est = 1u;
-  {
-    // only the bits below those shared by the smallest and largest sampled key vary
-    uint32_t lo = 0xFFFFFFFFu, hi = 0u, nz = 0u;
-#pragma unroll
-    for (int u = 0; u < kFilterSample / kFilterThreads; ++u) {
-      const uint32_t v = ks[u * kFilterThreads + tid];
-      if (v != 0u) {
-        lo = min(lo, v);
-        hi = max(hi, v);
-        ++nz;
-      }
-    }
-    lo = __reduce_min_sync(0xffffffffu, lo);
-    hi = __reduce_max_sync(0xffffffffu, hi);
-    nz = __reduce_add_sync(0xffffffffu, nz);
-    if (lane == 0) {
-      red[0][wid] = lo;
-      red[1][wid] = hi;
-      red[2][wid] = nz;
-    }
-    __syncthreads();
-    nz = 0;
-#pragma unroll
-    for (int w = 0; w < kFilterThreads / 32; ++w) {
-      lo = min(lo, red[0][w]);
-      hi = max(hi, red[1][w]);
-      nz += red[2][w];
-    }
-    if (nz >= r) {
-      const int b = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
-      uint32_t need_eq;
-      t_est = kth_radix(ks, kFilterSample, r, hi, b, hist, bcast, &need_eq);
-    }
-  }
+  const uint32_t t_est = t_sh;
   // this chunk: warp w owns elements [w*512, w*512+512) of it, 16 per lane, all loads in flight
   const int64_t c0 = (int64_t)c * kTkChunk + (int64_t)wid * (kTkChunk / 8);
   constexpr int kPer = kTkChunk / kFilterThreads;  // 16
@@ -701,6 +798,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
   __shared__ uint32_t coff[1025];
   int parity = 0;
   const int n = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  for (int i = tid; i < 2 * 2048; i += kTopkThreads) (&sh.hist11[0][0])[i] = 0u;
   int32_t *o = out + (int64_t)n * topk;
   ChunkWs cw = chunk_ws(const_cast<void *>(ws), n, n_chunks);
   // chunk offsets (n_chunks <= 1024): block-wide exclusive scan of the kept counts
@@ -729,29 +827,28 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
   if (kept >= k_eff && kept <= (uint32_t)kSmemCap) {
     if (tid == 0) coff[n_chunks] = kept;
     __syncthreads();
-    // flattened copy: element e of the kept set lives in the chunk c with coff[c] <= e < coff[c+1]
-    for (int e0 = tid; e0 < (int)kept; e0 += 4 * kTopkThreads) {
-      uint32_t kk[4];
-      int32_t pp[4];
+    // warp w copies chunks w, w + 32, ... to their offsets (index order is chunk order)
+    for (int c = wid; c < n_chunks; c += kTopkWarps) {
+      const int cnt = (int)(coff[c + 1] - coff[c]), dst = (int)coff[c];
+      const uint32_t *ck = cw.keys + (size_t)c * kTkChunk;
+      const int32_t *cp = cw.pos + (size_t)c * kTkChunk;
+      for (int j0 = 0; j0 < cnt; j0 += 32 * 4) {
+        uint32_t kk[4];
+        int32_t pp[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = e0 + u * kTopkThreads;
-        const int ec = e < (int)kept ? e : (int)kept - 1;
-        int lo = 0, hi = n_chunks - 1;  // last chunk with coff[c] <= ec
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (coff[mid] <= (uint32_t)ec) lo = mid; else hi = mid - 1;
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u * 32 + lane;
+          const int jc = j < cnt ? j : 0;
+          kk[u] = ck[jc];
+          pp[u] = cp[jc];
         }
-        const size_t src = (size_t)lo * kTkChunk + (ec - coff[lo]);
-        kk[u] = cw.keys[src];
-        pp[u] = cw.pos[src];
-      }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = e0 + u * kTopkThreads;
-        if (e < (int)kept) {
-          skey[e] = kk[u];
-          spos[e] = pp[u];
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u * 32 + lane;
+          if (j < cnt) {
+            skey[dst + j] = kk[u];
+            spos[dst + j] = pp[u];
+          }
         }
       }
     }
@@ -768,252 +865,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
   ev.n_elems = n_elems;
   ev.limit = MODE == kById ? (V + unit - 1) / unit : V;
   select_and_emit(ev, n_elems, topk, sh, parity, o);
-}
-
-// ------------------------------------------------------------------------------------------
-// Cluster path: few queries over at most 8 x 16,384 elements.  One thread-block cluster of C
-// CTAs per query; CTA r keeps elements r*16384 + 1024*u + tid (u < 16) in registers.
-//   1. the cluster's smallest and largest candidate key and candidate count, exchanged through
-//      distributed shared memory;
-//   2. the k-th largest key T by radix select over the bits below the shared leading ones,
-//      11-bit digits: each CTA histograms the keys still in play, every CTA sums the C
-//      histograms of a digit straight from the others' shared memory and finds the same digit
-//      (block-wide scan from the top bin).  Histograms are double-buffered, so one cluster
-//      barrier per digit suffices: a CTA only reaches barrier p after it finished reading the
-//      buffers of digit p-1, which is when they are cleared for digit p+1;
-//   3. ordered emission: per (u, warp) counts of the keys > T and == T, one block scan and a
-//      prefix over the CTAs give each selected element its slot (index order = output order).
-constexpr int kClThreads = 1024;
-constexpr int kClPer = 16;
-constexpr int kClSpan = kClThreads * kClPer;
-constexpr int kClMaxCtas = 8;
-constexpr int kClBits = 11;
-constexpr int kClBins = 1 << kClBits;
-
-struct ClShared {
-  uint32_t hist[2][kClBins];
-  uint32_t tab[kClPer * 32];  // per (u, warp): keys > T | (keys == T) << 16, then their prefix
-  uint32_t wsum[32];
-  uint32_t pub_range[3];      // read by the cluster: smallest, largest key, candidates
-  uint32_t pub_tot[2];        // read by the cluster: this CTA's keys > T, keys == T
-  uint32_t bc[4];
-};
-
-__device__ __forceinline__ uint32_t cl_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cl_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-// All threads of all CTAs of the cluster; orders shared-memory writes before the barrier with
-// reads (local or remote) after it.
-__device__ __forceinline__ void cl_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Word at the same shared-memory offset as `p`, in the CTA of the cluster with rank `rank`.
-__device__ __forceinline__ uint32_t cl_ld(const uint32_t *p, uint32_t rank) {
-  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-  uint32_t ra, v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
-  return v;
-}
-
-// Inclusive scan over the 1024 threads of the block (ends with a barrier, so wsum is free).
-__device__ __forceinline__ uint32_t block_incl_scan_1024(uint32_t v, uint32_t *wsum) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  uint32_t inc = warp_incl_scan(v);
-  if (lane == 31) wsum[wid] = inc;
-  __syncthreads();
-  if (wid == 0) {
-    const uint32_t t = wsum[lane];
-    wsum[lane] = warp_incl_scan(t) - t;
-  }
-  __syncthreads();
-  inc += wsum[wid];
-  __syncthreads();
-  return inc;
-}
-
-template <int MODE>
-__global__ void __launch_bounds__(kClThreads, 1) topk_cluster_kernel(
-    const float *__restrict__ vals, int64_t stride, int64_t n_elems,
-    const int32_t *__restrict__ map, int64_t map_stride, int unit,
-    const int32_t *__restrict__ q_vis, int topk, int32_t *__restrict__ out) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ ClShared sh;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const uint32_t rank = cl_rank(), C = cl_size();
-  const int n = blockIdx.y;
-  const int64_t V = q_vis[n];
-  ElemView<MODE> ev;
-  ev.vals = vals + (int64_t)n * stride;
-  ev.val_len = stride > 0 ? stride : 1;
-  ev.map = map ? map + (int64_t)n * map_stride : nullptr;
-  ev.n_elems = n_elems;
-  ev.limit = MODE == kById ? (V + unit - 1) / unit : V;
-  const int64_t base = (int64_t)rank * kClSpan;
-  uint32_t key[kClPer];
-#pragma unroll
-  for (int u = 0; u < kClPer; ++u) {
-    int32_t p;
-    key[u] = ev.get(base + (int64_t)u * kClThreads + tid, p);
-  }
-
-  // ---- 1. range and count of the candidates, cluster-wide
-  {
-    uint32_t lo = 0xFFFFFFFFu, hi = 0u, cnt = 0u;
-#pragma unroll
-    for (int u = 0; u < kClPer; ++u)
-      if (key[u] != 0u) {
-        lo = min(lo, key[u]);
-        hi = max(hi, key[u]);
-        ++cnt;
-      }
-    lo = __reduce_min_sync(0xffffffffu, lo);
-    hi = __reduce_max_sync(0xffffffffu, hi);
-    cnt = __reduce_add_sync(0xffffffffu, cnt);
-    if (lane == 0) {
-      sh.hist[1][wid] = lo;
-      sh.hist[1][32 + wid] = hi;
-      sh.hist[1][64 + wid] = cnt;
-    }
-    sh.hist[0][tid] = 0u;
-    sh.hist[0][tid + kClThreads] = 0u;
-    __syncthreads();
-    if (wid == 0) {
-      lo = __reduce_min_sync(0xffffffffu, sh.hist[1][lane]);
-      hi = __reduce_max_sync(0xffffffffu, sh.hist[1][32 + lane]);
-      cnt = __reduce_add_sync(0xffffffffu, sh.hist[1][64 + lane]);
-      if (lane == 0) {
-        sh.pub_range[0] = lo;
-        sh.pub_range[1] = hi;
-        sh.pub_range[2] = cnt;
-      }
-    }
-    cl_sync();
-    if (wid == 0) {
-      lo = 0xFFFFFFFFu;
-      hi = 0u;
-      cnt = 0u;
-      if ((uint32_t)lane < C) {
-        lo = cl_ld(&sh.pub_range[0], lane);
-        hi = cl_ld(&sh.pub_range[1], lane);
-        cnt = cl_ld(&sh.pub_range[2], lane);
-      }
-      lo = __reduce_min_sync(0xffffffffu, lo);
-      hi = __reduce_max_sync(0xffffffffu, hi);
-      cnt = __reduce_add_sync(0xffffffffu, cnt);
-      if (lane == 0) {
-        sh.bc[0] = lo;
-        sh.bc[1] = hi;
-        sh.bc[2] = cnt;
-      }
-    }
-    sh.hist[1][tid] = 0u;  // the scratch above was only read locally, before the barrier
-    sh.hist[1][tid + kClThreads] = 0u;
-    __syncthreads();
-  }
-  const uint32_t gmin = sh.bc[0], gmax = sh.bc[1], gcnt = sh.bc[2];
-  const uint32_t k_eff = min((uint32_t)topk, gcnt);
-
-  // ---- 2. k-th largest key (every candidate when k_eff == gcnt: T = 0, none taken as equal)
-  uint32_t T = 0u, need = 0u;
-  if (k_eff < gcnt) {
-    int b = (gmin == gmax) ? 0 : 32 - __clz(gmin ^ gmax);
-    T = b >= 32 ? 0u : (gmax & ~((1u << b) - 1u));
-    uint32_t rem = k_eff;
-    int pb = 0;
-    while (b > 0) {  // the same sequence of digits in every CTA of the cluster
-      const int w = b >= kClBits ? kClBits : b;
-      b -= w;
-      const int s = b, hs = s + w;
-      uint32_t *hist = sh.hist[pb];
-#pragma unroll
-      for (int u = 0; u < kClPer; ++u) {
-        const uint32_t k = key[u];
-        if (k != 0u && (hs >= 32 || (k >> hs) == (T >> hs)))
-          atomicAdd(&hist[(k >> s) & ((1u << w) - 1u)], 1u);
-      }
-      cl_sync();
-      sh.hist[pb ^ 1][tid] = 0u;
-      sh.hist[pb ^ 1][tid + kClThreads] = 0u;
-      const int hb0 = kClBins - 1 - 2 * tid, hb1 = hb0 - 1;  // this thread's bins, descending
-      uint32_t c0 = 0u, c1 = 0u;
-      for (uint32_t r = 0; r < C; ++r) {
-        c0 += cl_ld(&hist[hb0], r);
-        c1 += cl_ld(&hist[hb1], r);
-      }
-      const uint32_t inc = block_incl_scan_1024(c0 + c1, sh.wsum), exc = inc - c0 - c1;
-      if (exc < rem && inc >= rem) {  // exactly one thread: the in-play count is >= rem
-        const bool first = exc + c0 >= rem;
-        sh.bc[0] = (uint32_t)(first ? hb0 : hb1);
-        sh.bc[1] = first ? exc : exc + c0;
-      }
-      __syncthreads();
-      T |= sh.bc[0] << s;
-      rem -= sh.bc[1];
-      pb ^= 1;
-    }
-    need = rem;
-  }
-
-  // ---- 3. ordered emission
-#pragma unroll
-  for (int u = 0; u < kClPer; ++u) {
-    const uint32_t a = __popc(__ballot_sync(0xffffffffu, key[u] > T));
-    const uint32_t e = __popc(__ballot_sync(0xffffffffu, key[u] == T && key[u] != 0u));
-    if (lane == 0) sh.tab[u * 32 + wid] = a | (e << 16);
-  }
-  __syncthreads();
-  {
-    const uint32_t v = tid < kClPer * 32 ? sh.tab[tid] : 0u;
-    const uint32_t inc = block_incl_scan_1024(v, sh.wsum);
-    if (tid < kClPer * 32) sh.tab[tid] = inc - v;
-    if (tid == kClThreads - 1) {
-      sh.pub_tot[0] = inc & 0xFFFFu;
-      sh.pub_tot[1] = inc >> 16;
-    }
-  }
-  cl_sync();
-  if (wid == 0) {
-    uint32_t a = 0u, e = 0u;
-    if ((uint32_t)lane < C) {
-      a = cl_ld(&sh.pub_tot[0], lane);
-      e = cl_ld(&sh.pub_tot[1], lane);
-    }
-    const uint32_t ai = warp_incl_scan(a), ei = warp_incl_scan(e);
-    const uint32_t a0 = __shfl_sync(0xffffffffu, ai - a, rank);
-    const uint32_t e0 = __shfl_sync(0xffffffffu, ei - e, rank);
-    if (lane == 0) {
-      sh.bc[2] = a0;
-      sh.bc[3] = e0;
-    }
-  }
-  __syncthreads();
-  const uint32_t gt0 = sh.bc[2], eq0 = sh.bc[3];
-  int32_t *o = out + (int64_t)n * topk;
-  const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-  for (int u = 0; u < kClPer; ++u) {
-    const bool gt = key[u] > T, eq = key[u] == T && key[u] != 0u;
-    const uint32_t bgt = __ballot_sync(0xffffffffu, gt), beq = __ballot_sync(0xffffffffu, eq);
-    const uint32_t t = sh.tab[u * 32 + wid];
-    const uint32_t my_gt = gt0 + (t & 0xFFFFu) + __popc(bgt & lt);
-    const uint32_t my_eq = eq0 + (t >> 16) + __popc(beq & lt);
-    if (gt || (eq && my_eq < need))
-      o[my_gt + min(my_eq, need)] = ev.pos_of(base + (int64_t)u * kClThreads + tid);
-  }
-  if (rank == 0)
-    for (int i = (int)k_eff + tid; i < topk; i += kClThreads) o[i] = -1;
-  cl_sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1048,50 +899,6 @@ struct RgShared {
   uint16_t kidx[kRgKeepCap];
 };
 constexpr size_t kRgSmem = sizeof(RgShared);
-
-// k-th largest (1 <= k <= number of candidates) of the keys this block visits: visit(f) calls
-// f(key) for each of the calling thread's keys (0 = not a candidate); all candidates lie in
-// [lo, hi].  11-bit digits below the leading bits lo and hi share; hist[0] is zero on entry and
-// both buffers are zero on return.  need = k - #(keys > T).
-template <class Visit>
-__device__ uint32_t radix11_kth(Visit visit, uint32_t k, uint32_t lo, uint32_t hi,
-                                uint32_t (*hist)[kClBins], uint32_t *wsum, uint32_t *bc,
-                                uint32_t &need) {
-  const int tid = threadIdx.x;
-  int b = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
-  uint32_t T = b >= 32 ? 0u : (hi & ~((1u << b) - 1u));
-  uint32_t rem = k;
-  int pb = 0;
-  while (b > 0) {
-    const int w = b >= kClBits ? kClBits : b;
-    b -= w;
-    const int s = b, hs = s + w;
-    uint32_t *h = hist[pb];
-    const uint32_t Tc = T;
-    visit([&](uint32_t key) {
-      if (key != 0u && (hs >= 32 || (key >> hs) == (Tc >> hs)))
-        atomicAdd(&h[(key >> s) & ((1u << w) - 1u)], 1u);
-    });
-    __syncthreads();
-    const int hb0 = kClBins - 1 - 2 * tid, hb1 = hb0 - 1;
-    const uint32_t c0 = h[hb0], c1 = h[hb1];
-    const uint32_t inc = block_incl_scan_1024(c0 + c1, wsum), exc = inc - c0 - c1;
-    h[hb0] = 0u;  // every read of this buffer happened before the scan's barriers
-    h[hb1] = 0u;
-    if (exc < rem && inc >= rem) {
-      const bool first = exc + c0 >= rem;
-      bc[0] = (uint32_t)(first ? hb0 : hb1);
-      bc[1] = first ? exc : exc + c0;
-    }
-    __syncthreads();
-    T |= bc[0] << s;
-    rem -= bc[1];
-    __syncthreads();  // bc is rewritten by the next digit
-    pb ^= 1;
-  }
-  need = rem;
-  return T;
-}
 
 template <int MODE>
 __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
@@ -1310,30 +1117,9 @@ static bool topk_use_reg(int nq, int64_t n_elems) {
   return nq <= 64 && n_elems >= 1 && n_elems <= kRgSpan;
 }
 
-// The cluster path is kept for element counts above one CTA's registers but is not routed to:
-// on skewed score distributions its first digit's shared atomics serialise.
-static int topk_cluster_ctas(int nq, int64_t n_elems) {
-  (void)nq;
-  (void)n_elems;
-  return 0;
-}
-
-template <int MODE>
-static cudaError_t launch_topk_cluster(const float *vals, int64_t stride, int64_t n_elems,
-                                       const int32_t *map, int64_t map_stride, int unit,
-                                       const int32_t *q_vis, int nq, int topk, int32_t *out,
-                                       int C, cudaStream_t st) {
-  const cudaError_t e = launch_pdl_cluster(topk_cluster_kernel<MODE>, dim3(C, nq),
-                                           dim3(kClThreads), 0, st, C, vals, stride, n_elems,
-                                           map, map_stride, unit, q_vis, topk, out);
-  note_launches(1);
-  return e;
-}
-
 // The chunked two-kernel path serves few queries over many elements.
 static bool topk_use_chunks(int nq, int64_t n_elems) {
-  return !topk_use_reg(nq, n_elems) && topk_cluster_ctas(nq, n_elems) == 0 && nq <= 64 &&
-         n_elems > 2 * kFilterSample &&
+  return !topk_use_reg(nq, n_elems) && nq <= 64 && n_elems > 2 * kFilterSample &&
          (n_elems + kTkChunk - 1) / kTkChunk <= 1024;
 }
 
@@ -1378,16 +1164,6 @@ cudaError_t launch_topk(const float *vals, int64_t stride, int64_t n_elems, cons
                                       nq, topk, out, st);
     return launch_topk_reg<kMapSlot>(vals, stride, n_elems, map, map_stride, unit, q_vis, nq, topk,
                                      out, st);
-  }
-  if (const int C = topk_cluster_ctas(nq, n_elems)) {
-    if (!map)
-      return launch_topk_cluster<kById>(vals, stride, n_elems, nullptr, 0, unit, q_vis, nq, topk,
-                                        out, C, st);
-    if (pos_vals)
-      return launch_topk_cluster<kMapPos>(pos_vals, pos_stride, n_elems, map, map_stride, unit,
-                                          q_vis, nq, topk, out, C, st);
-    return launch_topk_cluster<kMapSlot>(vals, stride, n_elems, map, map_stride, unit, q_vis, nq,
-                                         topk, out, C, st);
   }
   if (ws && topk_use_chunks(nq, n_elems)) {
     if (!map)

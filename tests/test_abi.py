@@ -82,7 +82,7 @@ def test_workspace_sizes_are_host_only(csa2):
     L = csa2.lib
     assert L.csa2_index_score_topk_workspace_size(1, 1 << 20, 0, 2048) > 0
     assert L.csa2_index_score_topk_workspace_size(1, 1 << 20, 2048, 2048) >= 2048 * 8 * 4
-    assert L.csa2_hier_candidate_pool_workspace_size(1, 131072, 2048) == 0  # one cluster
-    assert L.csa2_hier_candidate_pool_workspace_size(1, 262144, 2048) >= 262144 * 8  # chunked
+    assert L.csa2_hier_candidate_pool_workspace_size(1, 16384, 2048) == 0  # one CTA, registers
+    assert L.csa2_hier_candidate_pool_workspace_size(1, 131072, 2048) >= 131072 * 8  # chunked
     assert L.csa2_hier_candidate_pool_workspace_size(4096, 33280, 2048) == 0  # one CTA per query
     assert L.csa2_sparse_attn_prefill_workspace_size(16, 64, 2048) >= 16 * 64 * 288
