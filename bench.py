@@ -166,7 +166,7 @@ def run_ours(args, rank, world):
 
     # per-call device times: each call captured as its own graph, replayed with events
     parts = profile_calls(st, args.steps, flush)
-    dom_name, dom_ms, dom_bytes = ("csa2_index_score_topk (Full, 1,048,576 keys)",
+    dom_name, dom_ms, dom_bytes = ("csa2_index_score_topk_pool (Full + pool, 1,048,576 keys)",
                                    parts["full_index"], by["index_keys_full"])
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
 
@@ -226,9 +226,9 @@ def profile_calls(st, steps, flush):
     reidx = next((L for L in st.layers if L["mode"] == "reindex"), None)
     calls = {
         "kv_quant": lambda s: st.quantize_new_rows(stream=s),
-        "full_index": lambda s: st.index(full, block_max=st.bm, stream=s),
-        "pool": lambda s: csa2.csa2_hier_candidate_pool(st.bm, st.q_vis, st.w.n_pool_blocks,
-                                                        st.pool, ws=st.ws_pool, stream=s),
+        # the step's first Full layer: with the candidate pool in the hierarchical decoder
+        "full_index": ((lambda s: st.index_with_pool(full, stream=s)) if st.pool is not None
+                       else (lambda s: st.index(full, stream=s))),
         "attention": lambda s: st.attend(full, full["idx"], stream=s),
     }
     if reidx is not None:

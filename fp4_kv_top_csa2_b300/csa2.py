@@ -38,6 +38,9 @@ def _load() -> ctypes.CDLL:
                                       P, P, SZ, P]),
         "csa2_index_score_topk_reindex_noalloc": (I, [P, I, P, I, I, I, P, I, I64, P, P, I, P, P,
                                                       I64, P, I, I, P, P]),
+        "csa2_index_score_topk_pool_workspace_size": (SZ, [I, I64, I, I]),
+        "csa2_index_score_topk_pool": (I, [P, I, P, I, I, I, P, I, I64, P, P, I, P, P, I64, I, P,
+                                           P, I, I, P, P, SZ, P]),
         "csa2_hier_candidate_pool_workspace_size": (SZ, [I, I64, I]),
         "csa2_hier_candidate_pool": (I, [P, I, P, I64, I, I, P, P, SZ, P]),
         "csa2_sparse_attn_decode_workspace_size": (SZ, [I, I, I]),
@@ -116,6 +119,24 @@ def csa2_index_score_topk_reindex_noalloc(q_idx, q_dtype, w, k_idx, cu_ctx, q_se
         _ptr(q_idx), q_dtype, _ptr(w), nq, Hi, Di, _ptr(k_idx), q_dtype, k_idx.shape[0],
         _ptr(k_scale), _ptr(cu_ctx), B, _ptr(q_seq), _ptr(q_vis), max_vis, _ptr(cand_blocks),
         cand_blocks.shape[1], topk, _ptr(out_idx), _stream(stream)))
+
+
+def csa2_index_score_topk_pool_workspace_size(nq, max_vis, topk, n_pool_blocks):
+    return lib.csa2_index_score_topk_pool_workspace_size(nq, max_vis, topk, n_pool_blocks)
+
+
+def csa2_index_score_topk_pool(q_idx, q_dtype, w, k_idx, cu_ctx, q_seq, q_vis, max_vis, topk,
+                               out_idx, n_pool_blocks, out_pool_blocks, k_scale=None,
+                               out_block_max=None, block_size=8, ws=None, stream=None):
+    """Full-mode selection and the candidate pool of the same block maxima, in one call."""
+    nq, Hi, Di = q_idx.shape
+    B = cu_ctx.numel() - 1
+    wp, wn = _ws(ws)
+    _check("csa2_index_score_topk_pool", lib.csa2_index_score_topk_pool(
+        _ptr(q_idx), q_dtype, _ptr(w), nq, Hi, Di, _ptr(k_idx), q_dtype, k_idx.shape[0],
+        _ptr(k_scale), _ptr(cu_ctx), B, _ptr(q_seq), _ptr(q_vis), max_vis, topk, _ptr(out_idx),
+        _ptr(out_block_max), block_size, n_pool_blocks, _ptr(out_pool_blocks), wp, wn,
+        _stream(stream)))
 
 
 def csa2_hier_candidate_pool_workspace_size(nq, max_blocks, n_pool_blocks):

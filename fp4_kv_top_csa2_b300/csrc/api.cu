@@ -63,10 +63,13 @@ struct ScoreWs {
   void *topk = nullptr;         // scratch of the Top-K selections (shared: they run in turn)
   size_t bytes = 0;
   int64_t nb_max = 0;
-  int kb = 0;
+  int kb = 0;         // blocks the Full selection needs: min(topk, blocks)
+  bool pool_list = false;  // Full with a pool of >= kb blocks: the pool is the block list
+  int nl = 0;         // length of the block list the positions are drawn from
 };
 
-ScoreWs score_ws(void *base, int nq, int64_t max_vis, int n_cand_blocks, int topk) {
+ScoreWs score_ws(void *base, int nq, int64_t max_vis, int n_cand_blocks, int topk,
+                 int n_pool = 0) {
   ScoreWs w;
   WsCursor c(base);
   if (n_cand_blocks > 0) {
@@ -75,17 +78,106 @@ ScoreWs score_ws(void *base, int nq, int64_t max_vis, int n_cand_blocks, int top
   } else {
     w.nb_max = (max_vis + kBlock - 1) / kBlock;
     w.kb = (int)std::min<int64_t>(topk, w.nb_max);
+    w.pool_list = n_pool > 0 && n_pool >= w.kb;
+    w.nl = w.pool_list ? n_pool : w.kb;
     w.bm = c.take<float>((size_t)nq * w.nb_max);
-    w.blocks = c.take<int32_t>((size_t)nq * w.kb);
+    if (!w.pool_list) w.blocks = c.take<int32_t>((size_t)nq * w.kb);
     if (index_mma_supported(nq) && (int64_t)nq * max_vis <= kKeepScoresMax)
       w.pos_scores = c.take<float>((size_t)nq * max_vis);
     else
-      w.scores = c.take<float>((size_t)nq * w.kb * kBlock);
+      w.scores = c.take<float>((size_t)nq * w.nl * kBlock);
     w.topk = c.take<char>(std::max(topk_workspace_bytes(nq, w.nb_max),
-                                   topk_workspace_bytes(nq, (int64_t)w.kb * kBlock)));
+                                   topk_workspace_bytes(nq, (int64_t)w.nl * kBlock)));
   }
   w.bytes = c.used;
   return w;
+}
+
+// csa2_index_score_topk and csa2_index_score_topk_pool (n_pool > 0: Full mode with the pool).
+int index_score_topk_impl(const void *q_idx, int q_dtype, const float *w, int nq, int Hi, int Di,
+                          const void *k_idx, int k_dtype, int64_t k_rows, const float *k_scale,
+                          const int64_t *cu_ctx, int B, const int32_t *q_seq,
+                          const int32_t *q_vis, int64_t max_vis, const int32_t *cand_blocks,
+                          int n_cand_blocks, int topk, int32_t *out_idx, float *out_block_max,
+                          int n_pool, int32_t *out_pool, void *workspace, size_t ws_bytes,
+                          void *stream) {
+  if (nq < 0 || nq > 65535 || B < 1 || Hi < 1 || Hi > 16 || topk < 1 || topk > 4096 ||
+      max_vis < 0 || max_vis > (int64_t)1 << 30 || k_rows < 0 || k_rows > INT32_MAX)
+    return CSA2_ERR_INVALID_ARG;
+  if (q_dtype != k_dtype) return CSA2_ERR_INVALID_ARG;
+  if (!((q_dtype == CSA2_BF16 && Di == 64) || (q_dtype == CSA2_E4M3 && Di == 128)))
+    return CSA2_ERR_INVALID_ARG;
+  if (cand_blocks ? (n_cand_blocks < 1 || n_cand_blocks > 65536 || out_block_max)
+                  : (n_cand_blocks != 0))
+    return CSA2_ERR_INVALID_ARG;
+  if (n_pool < 0 || n_pool > 4096 || (n_pool > 0 && cand_blocks)) return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  if (!q_idx || !w || !k_idx || !cu_ctx || !q_seq || !q_vis || !out_idx ||
+      (n_pool > 0 && !out_pool))
+    return CSA2_ERR_INVALID_ARG;
+  const void *ptrs[] = {q_idx, w, k_idx, k_scale, cu_ctx, q_seq, q_vis,
+                        cand_blocks, out_idx, out_block_max, out_pool};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return CSA2_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) return CSA2_ERR_INVALID_ARG;
+  ScoreWs need = score_ws(nullptr, nq, max_vis, n_cand_blocks, topk, n_pool);
+  if (ws_bytes < need.bytes || (need.bytes && !workspace)) return CSA2_ERR_WORKSPACE;
+  if (int r = check_device()) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ScoreWs ws = score_ws(workspace, nq, max_vis, n_cand_blocks, topk, n_pool);
+  const bool mma = index_mma_supported(nq);
+  const bool multi = !mma && index_multi_supported(nq, Hi, B);
+  const bool cand_mma = cand_mma_supported();
+  cudaError_t e;
+  if (cand_blocks) {  // Reindex: score the listed blocks, select
+    e = cand_mma ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx,
+                                    q_seq, q_vis, cand_blocks, n_cand_blocks, ws.scores, st)
+            : launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq,
+                                q_vis, cand_blocks, n_cand_blocks, ws.scores, st);
+    if (e == cudaSuccess)
+      e = launch_topk(ws.scores, (int64_t)n_cand_blocks * kBlock, (int64_t)n_cand_blocks * kBlock,
+                      cand_blocks, n_cand_blocks, 1, q_vis, nq, topk, out_idx, st, nullptr, 0,
+                      ws.topk);
+    return cuda_status(e);
+  }
+  // Full: block maxima over every visible position; the Top-K positions lie inside the Top-K
+  // blocks by block maximum (each block ahead of a selected position's block holds a position
+  // ranked ahead of it), so select those blocks first, then select among their positions.  A
+  // candidate pool of at least that many blocks (the top blocks by block maximum, the same
+  // selection) serves as the block list itself.
+  float *bm = out_block_max ? out_block_max : ws.bm;
+  if (mma) {
+    e = launch_score_scan_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx, q_seq,
+                              q_vis, max_vis, bm, ws.nb_max, ws.pos_scores, max_vis, st);
+  } else if (multi) {  // chunked prefill over one sequence: 32 queries per key tile
+    e = launch_score_scan_multi(q_idx, q_dtype, w, nq, k_idx, k_rows, k_scale, q_vis, max_vis,
+                                bm, ws.nb_max, st);
+  } else {
+    e = launch_score_scan(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
+                          max_vis, bm, ws.nb_max, st);
+  }
+  int32_t *list = ws.pool_list ? out_pool : ws.blocks;
+  if (e == cudaSuccess)
+    e = launch_topk(bm, ws.nb_max, ws.nb_max, nullptr, 0, kBlock, q_vis, nq, ws.nl, list, st,
+                    nullptr, 0, ws.topk);
+  if (e == cudaSuccess && n_pool > 0 && !ws.pool_list)  // a pool smaller than the block list
+    e = launch_topk(bm, ws.nb_max, ws.nb_max, nullptr, 0, kBlock, q_vis, nq, n_pool, out_pool, st,
+                    nullptr, 0, ws.topk);
+  if (ws.pos_scores) {  // the scan kept every score: select among the blocks' positions
+    if (e == cudaSuccess)
+      e = launch_topk(nullptr, 0, (int64_t)ws.nl * kBlock, list, ws.nl, 1, q_vis, nq, topk,
+                      out_idx, st, ws.pos_scores, max_vis, ws.topk);
+    return cuda_status(e);
+  }
+  if (e == cudaSuccess)
+    e = (mma || multi) ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale,
+                                               cu_ctx, q_seq, q_vis, list, ws.nl, ws.scores, st)
+            : launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq,
+                                q_vis, list, ws.nl, ws.scores, st);
+  if (e == cudaSuccess)
+    e = launch_topk(ws.scores, (int64_t)ws.nl * kBlock, (int64_t)ws.nl * kBlock, list, ws.nl, 1,
+                    q_vis, nq, topk, out_idx, st, nullptr, 0, ws.topk);
+  return cuda_status(e);
 }
 
 }  // namespace
@@ -128,76 +220,29 @@ int csa2_index_score_topk(const void *q_idx, int q_dtype, const float *w, int nq
                           const int32_t *q_vis, int64_t max_vis, const int32_t *cand_blocks,
                           int n_cand_blocks, int topk, int32_t *out_idx, float *out_block_max,
                           void *workspace, size_t ws_bytes, void *stream) {
-  if (nq < 0 || nq > 65535 || B < 1 || Hi < 1 || Hi > 16 || topk < 1 || topk > 4096 ||
-      max_vis < 0 || max_vis > (int64_t)1 << 30 || k_rows < 0 || k_rows > INT32_MAX)
-    return CSA2_ERR_INVALID_ARG;
-  if (q_dtype != k_dtype) return CSA2_ERR_INVALID_ARG;
-  if (!((q_dtype == CSA2_BF16 && Di == 64) || (q_dtype == CSA2_E4M3 && Di == 128)))
-    return CSA2_ERR_INVALID_ARG;
-  if (cand_blocks ? (n_cand_blocks < 1 || n_cand_blocks > 65536 || out_block_max)
-                  : (n_cand_blocks != 0))
-    return CSA2_ERR_INVALID_ARG;
-  if (nq == 0) return CSA2_OK;
-  if (!q_idx || !w || !k_idx || !cu_ctx || !q_seq || !q_vis || !out_idx)
-    return CSA2_ERR_INVALID_ARG;
-  const void *ptrs[] = {q_idx, w, k_idx, k_scale, cu_ctx, q_seq, q_vis,
-                        cand_blocks, out_idx, out_block_max};
-  for (const void *p : ptrs)
-    if (!aligned16(p)) return CSA2_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) return CSA2_ERR_INVALID_ARG;
-  ScoreWs need = score_ws(nullptr, nq, max_vis, n_cand_blocks, topk);
-  if (ws_bytes < need.bytes || (need.bytes && !workspace)) return CSA2_ERR_WORKSPACE;
-  if (int r = check_device()) return r;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  ScoreWs ws = score_ws(workspace, nq, max_vis, n_cand_blocks, topk);
-  const bool mma = index_mma_supported(nq);
-  const bool multi = !mma && index_multi_supported(nq, Hi, B);
-  const bool cand_mma = cand_mma_supported();
-  cudaError_t e;
-  if (cand_blocks) {  // Reindex: score the listed blocks, select
-    e = cand_mma ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx,
-                                    q_seq, q_vis, cand_blocks, n_cand_blocks, ws.scores, st)
-            : launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq,
-                                q_vis, cand_blocks, n_cand_blocks, ws.scores, st);
-    if (e == cudaSuccess)
-      e = launch_topk(ws.scores, (int64_t)n_cand_blocks * kBlock, (int64_t)n_cand_blocks * kBlock,
-                      cand_blocks, n_cand_blocks, 1, q_vis, nq, topk, out_idx, st, nullptr, 0,
-                      ws.topk);
-    return cuda_status(e);
-  }
-  // Full: block maxima over every visible position; the Top-K positions lie inside the Top-K
-  // blocks by block maximum (each block ahead of a selected position's block holds a position
-  // ranked ahead of it), so select those blocks first, then select among their positions.
-  float *bm = out_block_max ? out_block_max : ws.bm;
-  if (mma) {
-    e = launch_score_scan_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx, q_seq,
-                              q_vis, max_vis, bm, ws.nb_max, ws.pos_scores, max_vis, st);
-  } else if (multi) {  // chunked prefill over one sequence: 32 queries per key tile
-    e = launch_score_scan_multi(q_idx, q_dtype, w, nq, k_idx, k_rows, k_scale, q_vis, max_vis,
-                                bm, ws.nb_max, st);
-  } else {
-    e = launch_score_scan(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
-                          max_vis, bm, ws.nb_max, st);
-  }
-  if (e == cudaSuccess)
-    e = launch_topk(bm, ws.nb_max, ws.nb_max, nullptr, 0, kBlock, q_vis, nq, ws.kb, ws.blocks, st,
-                    nullptr, 0, ws.topk);
-  if (ws.pos_scores) {  // the scan kept every score: select among the blocks' positions
-    if (e == cudaSuccess)
-      e = launch_topk(nullptr, 0, (int64_t)ws.kb * kBlock, ws.blocks, ws.kb, 1, q_vis, nq, topk,
-                      out_idx, st, ws.pos_scores, max_vis, ws.topk);
-    return cuda_status(e);
-  }
-  if (e == cudaSuccess)
-    e = (mma || multi) ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale,
-                                               cu_ctx, q_seq, q_vis, ws.blocks, ws.kb, ws.scores,
-                                               st)
-            : launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq,
-                                q_vis, ws.blocks, ws.kb, ws.scores, st);
-  if (e == cudaSuccess)
-    e = launch_topk(ws.scores, (int64_t)ws.kb * kBlock, (int64_t)ws.kb * kBlock, ws.blocks,
-                    ws.kb, 1, q_vis, nq, topk, out_idx, st, nullptr, 0, ws.topk);
-  return cuda_status(e);
+  return index_score_topk_impl(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_dtype, k_rows, k_scale,
+                               cu_ctx, B, q_seq, q_vis, max_vis, cand_blocks, n_cand_blocks, topk,
+                               out_idx, out_block_max, 0, nullptr, workspace, ws_bytes, stream);
+}
+
+size_t csa2_index_score_topk_pool_workspace_size(int nq, int64_t max_vis, int topk,
+                                                 int n_pool_blocks) {
+  if (nq < 0 || max_vis < 0 || topk < 1 || n_pool_blocks < 1) return 0;
+  return score_ws(nullptr, nq, max_vis, 0, topk, n_pool_blocks).bytes;
+}
+
+int csa2_index_score_topk_pool(const void *q_idx, int q_dtype, const float *w, int nq, int Hi,
+                               int Di, const void *k_idx, int k_dtype, int64_t k_rows,
+                               const float *k_scale, const int64_t *cu_ctx, int B,
+                               const int32_t *q_seq, const int32_t *q_vis, int64_t max_vis,
+                               int topk, int32_t *out_idx, float *out_block_max,
+                               int block_size, int n_pool_blocks, int32_t *out_pool_blocks,
+                               void *workspace, size_t ws_bytes, void *stream) {
+  if (block_size != kBlock || n_pool_blocks < 1) return CSA2_ERR_INVALID_ARG;
+  return index_score_topk_impl(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_dtype, k_rows, k_scale,
+                               cu_ctx, B, q_seq, q_vis, max_vis, nullptr, 0, topk, out_idx,
+                               out_block_max, n_pool_blocks, out_pool_blocks, workspace, ws_bytes,
+                               stream);
 }
 
 size_t csa2_hier_candidate_pool_workspace_size(int nq, int64_t max_blocks, int n_pool_blocks) {

@@ -62,7 +62,9 @@ class Step:
         ws = csa2.csa2_index_score_topk_workspace_size(self.nq, self.max_vis, 0, w.topk)
         if hier:
             ws = max(ws, csa2.csa2_index_score_topk_workspace_size(self.nq, self.max_vis,
-                                                                   w.n_pool_blocks, w.topk))
+                                                                   w.n_pool_blocks, w.topk),
+                     csa2.csa2_index_score_topk_pool_workspace_size(self.nq, self.max_vis,
+                                                                    w.topk, w.n_pool_blocks))
         self.ws_index = csa2.workspace(ws, dev)
         self.ws_pool = (csa2.workspace(csa2.csa2_hier_candidate_pool_workspace_size(
             self.nq, nb, w.n_pool_blocks), dev) if hier else None)
@@ -94,6 +96,14 @@ class Step:
                                          self.scale, layer["out"], layer["lse"],
                                          ws=self.ws_attn, stream=stream)
 
+    def index_with_pool(self, layer, stream=None):
+        """The first Full layer of the hierarchical decoder: its selection and the candidate
+        pool in one call (csa2_index_score_topk_pool)."""
+        csa2.csa2_index_score_topk_pool(
+            layer["q_idx"], self.w.idx_dtype, layer["w"], self.k_idx, self.cu_ctx, self.q_seq,
+            self.q_vis, self.max_vis, self.w.topk, layer["idx"], self.w.n_pool_blocks, self.pool,
+            out_block_max=self.bm, ws=self.ws_index, stream=stream)
+
     def run(self, stream=None):
         """One step: quantise the new rows, then every layer in order."""
         self.quantize_new_rows(stream)
@@ -102,10 +112,10 @@ class Step:
             if L["mode"] == "full":
                 first_full = self.pool is not None and all(
                     M["mode"] != "full" for M in self.layers[:i])
-                self.index(L, block_max=self.bm if first_full else None, stream=stream)
                 if first_full:
-                    csa2.csa2_hier_candidate_pool(self.bm, self.q_vis, self.w.n_pool_blocks,
-                                                  self.pool, ws=self.ws_pool, stream=stream)
+                    self.index_with_pool(L, stream=stream)
+                else:
+                    self.index(L, stream=stream)
                 last_idx = L["idx"]
             elif L["mode"] == "reindex":
                 self.index(L, cand=self.pool, stream=stream)

@@ -182,6 +182,30 @@ int csa2_hier_candidate_pool(const float *block_max, int nq, const int32_t *q_vi
                              int32_t *out_pool_blocks, void *workspace, size_t ws_bytes,
                              void *stream);
 
+/*
+ * csa2_index_score_topk_pool -- the first Full layer of the hierarchical decoder in one call:
+ * the Full-mode selection of csa2_index_score_topk (cand_blocks NULL) and the candidate pool of
+ * csa2_hier_candidate_pool over the same block maxima ([MC] Introduction: the pool is
+ * "constructed by the first Full Mode layer").  out_idx, out_block_max (optional here too) and
+ * out_pool_blocks are exactly what csa2_index_score_topk followed by csa2_hier_candidate_pool
+ * would write.  Both selections take the top blocks by block maximum, so when n_pool_blocks >=
+ * min(topk, ceil(max_vis/8)) the pool is also the block list the Full selection draws its
+ * positions from, and one block selection serves both.
+ *
+ * Arguments as csa2_index_score_topk (Full mode) plus block_size (must be 8), n_pool_blocks
+ * (1..4096) and out_pool_blocks ([nq, n_pool_blocks] int32); workspace / ws_bytes at least
+ * csa2_index_score_topk_pool_workspace_size(nq, max_vis, topk, n_pool_blocks) bytes.
+ */
+size_t csa2_index_score_topk_pool_workspace_size(int nq, int64_t max_vis, int topk,
+                                                 int n_pool_blocks);
+int csa2_index_score_topk_pool(const void *q_idx, int q_dtype, const float *w, int nq, int Hi,
+                               int Di, const void *k_idx, int k_dtype, int64_t k_rows,
+                               const float *k_scale, const int64_t *cu_ctx, int B,
+                               const int32_t *q_seq, const int32_t *q_vis, int64_t max_vis,
+                               int topk, int32_t *out_idx, float *out_block_max,
+                               int block_size, int n_pool_blocks, int32_t *out_pool_blocks,
+                               void *workspace, size_t ws_bytes, void *stream);
+
 /* ------------------------------------------------------------------------------------------ */
 /* 4. Sparse attention, decode                                                                  */
 /* ------------------------------------------------------------------------------------------ */

@@ -66,6 +66,16 @@ def test_host_validation_rejects_bad_arguments(csa2):
     assert args(1, 128, 1, 5000, p, 1 << 30) == -1
     assert args(1, 128, 1, 16, ctypes.c_void_p(4096 + 16), 1 << 30) == -1  # ws not 256-aligned
     assert args(1, 128, 1, 16, p, 0) == -4
+    # index + pool: block size 8, pool size 1..4096, pool output required, workspace
+    pargs = lambda bs, npool, outp, wsb: L.csa2_index_score_topk_pool(
+        p, 1, p, 1, 8, 128, p, 1, 5000, None, p, 1, p, p, 1000, 16, p, None, bs, npool, outp, p,
+        wsb, None)
+    assert pargs(4, 2048, p, 1 << 30) == -1
+    assert pargs(8, 0, p, 1 << 30) == -1
+    assert pargs(8, 5000, p, 1 << 30) == -1
+    assert pargs(8, 2048, None, 1 << 30) == -1
+    assert pargs(8, 2048, odd, 1 << 30) == -1
+    assert pargs(8, 2048, p, 0) == -4
     # pool: block size must be 8
     assert L.csa2_hier_candidate_pool(p, 1, p, 100, 4, 2048, p, None, 0, None) == -1
     assert L.csa2_hier_candidate_pool(p, 1, p, 100, 8, 0, p, None, 0, None) == -1
@@ -86,3 +96,7 @@ def test_workspace_sizes_are_host_only(csa2):
     assert L.csa2_hier_candidate_pool_workspace_size(1, 131072, 2048) >= 131072 * 8  # chunked
     assert L.csa2_hier_candidate_pool_workspace_size(4096, 33280, 2048) == 0  # one CTA per query
     assert L.csa2_sparse_attn_prefill_workspace_size(16, 64, 2048) >= 16 * 64 * 288
+    # index + pool: the pool is the block list, so no separate block list is carved
+    full = L.csa2_index_score_topk_workspace_size(1, 1 << 20, 0, 2048)
+    fused = L.csa2_index_score_topk_pool_workspace_size(1, 1 << 20, 2048, 2048)
+    assert 0 < fused <= full

@@ -193,6 +193,50 @@ def test_pool_and_reindex(csa2):
             check_topk(got[n], ref[n], topk, f"reindex query {n}")
 
 
+@pytest.mark.parametrize("lengths,topk,n_pool,with_bm", [
+    ([30000, 16384 * 2 + 5], 2048, 2048, True),   # the pool is the Full block list
+    ([30000, 16384 * 2 + 5], 512, 2048, False),   # pool larger than the block list
+    ([30000, 20000], 2048, 100, True),            # pool smaller: its own selection
+    ([700, 3], 64, 4096, True),                   # pool longer than the blocks: -1 padded
+])
+def test_index_with_pool_matches_separate_calls(csa2, lengths, topk, n_pool, with_bm):
+    """csa2_index_score_topk_pool writes exactly what csa2_index_score_topk followed by
+    csa2_hier_candidate_pool writes, and both equal the oracle."""
+    k, q, w, cu, kn, qn = _index_case(lengths, 1, 8, sum(lengths) + n_pool, dup=0.05)
+    vis = list(lengths)
+    nq, max_vis = len(vis), max(vis)
+    nb = (max_vis + 7) // 8
+    qd, wd, kd, cud = q.cuda(), w.cuda(), k.cuda(), cu.cuda()
+    seq = torch.arange(nq, dtype=torch.int32, device="cuda")
+    vis_t = torch.tensor(vis, dtype=torch.int32, device="cuda")
+    # separate calls
+    bm1 = torch.empty((nq, nb), device="cuda")
+    idx1 = torch.empty((nq, topk), dtype=torch.int32, device="cuda")
+    ws = csa2.workspace(csa2.csa2_index_score_topk_workspace_size(nq, max_vis, 0, topk))
+    csa2.csa2_index_score_topk(qd, 1, wd, kd, cud, seq, vis_t, max_vis, topk, idx1,
+                               out_block_max=bm1, ws=ws)
+    pool1 = torch.empty((nq, n_pool), dtype=torch.int32, device="cuda")
+    csa2.csa2_hier_candidate_pool(bm1, vis_t, n_pool, pool1, ws=_pool_ws(csa2, bm1, n_pool))
+    # fused call
+    bm2 = torch.empty((nq, nb), device="cuda") if with_bm else None
+    idx2 = torch.full((nq, topk), -7, dtype=torch.int32, device="cuda")
+    pool2 = torch.full((nq, n_pool), -7, dtype=torch.int32, device="cuda")
+    ws2 = csa2.workspace(csa2.csa2_index_score_topk_pool_workspace_size(nq, max_vis, topk, n_pool))
+    csa2.csa2_index_score_topk_pool(qd, 1, wd, kd, cud, seq, vis_t, max_vis, topk, idx2, n_pool,
+                                    pool2, out_block_max=bm2, ws=ws2)
+    assert torch.equal(idx1, idx2)
+    assert torch.equal(pool1, pool2)
+    ref = oracle.index_score_topk(qn, 1, w.numpy(), kn, cu.numpy(), np.arange(nq), np.array(vis),
+                                  topk)
+    for n in range(nq):
+        nbn = (vis[n] + 7) // 8
+        if with_bm:
+            assert torch.equal(bm1[n, :nbn], bm2[n, :nbn])
+        check_topk(idx2[n].cpu().numpy(), ref[n], topk, f"query {n}")
+        assert np.array_equal(pool2[n].cpu().numpy(),
+                              oracle.candidate_pool(bm1[n, :nbn].cpu().numpy(), n_pool))
+
+
 # ------------------------------------------------------------------------------------------------
 # Sparse attention
 # ------------------------------------------------------------------------------------------------
