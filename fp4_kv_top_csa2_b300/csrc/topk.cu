@@ -868,37 +868,85 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
 }
 
 // ------------------------------------------------------------------------------------------
-// Register path: one CTA per query over at most 16,384 elements, element u*1024 + tid in
-// register u of thread tid.
+// Register path: one CTA per query over at most 16,384 elements.  Thread tid holds, in round v
+// (v < 4), the four consecutive elements 4096 v + 4 tid + j (j < 4): one 16-byte value load and
+// one block-list load per round (scalar loads only at a ragged end or an unaligned row).
 //   1. candidate count, smallest and largest key (block reduction);
 //   2. threshold estimate t_lo: the r-th largest of 128 keys sampled across the elements (exact
 //      rank of every sample: 1024 threads x 16 comparisons), r = the expected number of sampled
 //      keys in the Top-K plus 2.5 standard deviations plus 3, so that at least K keys are >= t_lo
 //      with high probability;
-//   3. the keys >= t_lo are compacted in index order into shared memory (ballots per register
-//      round and warp, one block scan); if they are fewer than K (the estimate was too high) or
-//      more than the shared-memory capacity, step 4 runs over all keys in registers instead;
-//   4. radix select of the k-th largest key T over the compacted keys, 11-bit digits, one
-//      shared histogram per digit (the compacted keys spread over many bins);
+//   3. the keys >= t_lo and their positions are compacted in index order into shared memory
+//      (per-round warp scans, one block scan); if they are fewer than K (the estimate was too
+//      high) or more than the shared-memory capacity, step 4 runs over all keys in registers;
+//   4. radix select of the k-th largest key T, 11-bit digits, one shared histogram per digit;
 //   5. ordered emission of the keys > T and the first need = K - #(> T) keys == T.
 constexpr int kRgThreads = 1024;
-constexpr int kRgPer = 16;
-constexpr int kRgSpan = kRgThreads * kRgPer;
+constexpr int kRgRounds = 4;
+constexpr int kRgSpan = kRgThreads * 4 * kRgRounds;  // 16,384
 constexpr int kRgSample = 128;
 constexpr int kRgKeepCap = 8192;
+static_assert(kRgKeepCap / kRgThreads >= kRgRounds, "round table");
 
 struct RgShared {
   uint32_t hist[2][kClBins];
-  uint32_t tab[kRgPer * 32];
+  uint32_t tab[(kRgKeepCap / kRgThreads) * 32];  // per (round, warp); 8 rounds of the compacted set
   uint32_t wsum[32];
   uint32_t red[3][32];
   uint32_t samp[kRgSample];
   uint32_t sg[kRgSample], se[kRgSample];
   uint32_t bc[8];
   uint32_t kkey[kRgKeepCap];
-  uint16_t kidx[kRgKeepCap];
+  int32_t kpos[kRgKeepCap];
 };
 constexpr size_t kRgSmem = sizeof(RgShared);
+
+// Keys (0 = not a candidate) and positions of elements e0 .. e0+3 (e0 = 4096 v + 4 tid).
+template <int MODE>
+__device__ __forceinline__ void load4(const ElemView<MODE> &ev, int e0, bool vec,
+                                      uint32_t (&k)[4], int32_t (&pos)[4]) {
+  const int n = (int)ev.n_elems;
+  int blk = 0;
+  if (MODE != kById) blk = e0 < n ? __ldg(ev.map + (e0 >> 3)) : -1;
+  int64_t vbase;  // value index of element e0
+  if (MODE == kMapPos) vbase = (int64_t)(blk < 0 ? 0 : blk) * kBlock + (e0 & 7);
+  else vbase = e0;
+  const bool full = e0 + 3 < n;
+  float v[4];
+  if (vec && full && (MODE != kMapPos || vbase + 3 < ev.val_len)) {
+    const float4 f = __ldg(reinterpret_cast<const float4 *>(ev.vals + vbase));
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int64_t vi = vbase + j;
+      const int64_t hi = MODE == kMapPos ? ev.val_len - 1 : (int64_t)n - 1;
+      vi = vi < hi ? vi : hi;
+      v[j] = __ldg(ev.vals + vi);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = e0 + j;
+    int64_t p;
+    bool ok;
+    if (MODE == kById) {
+      p = e;
+      ok = e < n && p < ev.limit;
+    } else {
+      p = (int64_t)blk * kBlock + (e & 7);
+      ok = e < n && blk >= 0 && p < ev.limit;
+    }
+    pos[j] = (int32_t)p;
+    k[j] = ok ? float_key(v[j]) : 0u;
+  }
+}
+
+// Exclusive offsets, in index order, of this thread's flagged elements of round v: the warp
+// scan of per-thread counts plus the block-wide prefix in tab (filled by the caller).
+__device__ __forceinline__ uint32_t warp_excl_scan(uint32_t c) {
+  return warp_incl_scan(c) - c;
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
@@ -918,11 +966,12 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
   ev.map = map ? map + (int64_t)n * map_stride : nullptr;
   ev.n_elems = n_elems;
   ev.limit = MODE == kById ? (V + unit - 1) / unit : V;
-  uint32_t key[kRgPer];
+  const bool vec = (reinterpret_cast<uintptr_t>(ev.vals) & 15u) == 0;
+  uint32_t key[kRgRounds][4];
+  {
+    int32_t pdummy[kRgRounds][4];
 #pragma unroll
-  for (int u = 0; u < kRgPer; ++u) {
-    int32_t p;
-    key[u] = ev.get((int64_t)u * kRgThreads + tid, p);
+    for (int v = 0; v < kRgRounds; ++v) load4(ev, 4096 * v + 4 * tid, vec, key[v], pdummy[v]);
   }
   sh.hist[0][tid] = 0u;
   sh.hist[0][tid + kRgThreads] = 0u;
@@ -937,12 +986,14 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
   {
     uint32_t lo = 0xFFFFFFFFu, hi = 0u, cnt = 0u;
 #pragma unroll
-    for (int u = 0; u < kRgPer; ++u)
-      if (key[u] != 0u) {
-        lo = min(lo, key[u]);
-        hi = max(hi, key[u]);
-        ++cnt;
-      }
+    for (int v = 0; v < kRgRounds; ++v)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (key[v][j] != 0u) {
+          lo = min(lo, key[v][j]);
+          hi = max(hi, key[v][j]);
+          ++cnt;
+        }
     lo = __reduce_min_sync(0xffffffffu, lo);
     hi = __reduce_max_sync(0xffffffffu, hi);
     cnt = __reduce_add_sync(0xffffffffu, cnt);
@@ -951,14 +1002,16 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
       sh.red[1][wid] = hi;
       sh.red[2][wid] = cnt;
     }
-    // sample j (= tid / 8 for tid % 8 == 0): element (j % 16) * 1024 + 8 j
+    // sample s (tid = 8 s): element 4096 ((s >> 2) & 3) + 4 tid + (s & 3)
     if ((tid & 7) == 0) {
-      const int j = tid >> 3, uj = j & (kRgPer - 1);
-      uint32_t v = 0u;
+      const int sidx = tid >> 3, vs = (sidx >> 2) & 3, js = sidx & 3;
+      uint32_t x = 0u;
 #pragma unroll
-      for (int u = 0; u < kRgPer; ++u)
-        if (u == uj) v = key[u];
-      sh.samp[j] = v;
+      for (int v = 0; v < kRgRounds; ++v)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (v == vs && j == js) x = key[v][j];
+      sh.samp[sidx] = x;
     }
     __syncthreads();
     gmin = __reduce_min_sync(0xffffffffu, sh.red[0][lane]);
@@ -995,32 +1048,52 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
     __syncthreads();
     const uint32_t t_lo = sh.bc[4];
     // ---- 3. compaction of the keys >= t_lo (index order)
+    uint32_t cnt_v[kRgRounds];
 #pragma unroll
-    for (int u = 0; u < kRgPer; ++u) {
-      const uint32_t c = __popc(__ballot_sync(0xffffffffu, key[u] >= t_lo && key[u] != 0u));
-      if (lane == 0) sh.tab[u * 32 + wid] = c;
+    for (int v = 0; v < kRgRounds; ++v) {
+      uint32_t c = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) c += key[v][j] >= t_lo && key[v][j] != 0u;
+      cnt_v[v] = c;
+      const uint32_t wt = __reduce_add_sync(0xffffffffu, c);
+      if (lane == 0) sh.tab[v * 32 + wid] = wt;
     }
     __syncthreads();
     {
-      const uint32_t v = tid < kRgPer * 32 ? sh.tab[tid] : 0u;
-      const uint32_t inc = block_incl_scan_1024(v, sh.wsum);
-      if (tid < kRgPer * 32) sh.tab[tid] = inc - v;
+      const uint32_t x = tid < kRgRounds * 32 ? sh.tab[tid] : 0u;
+      const uint32_t inc = block_incl_scan_1024(x, sh.wsum);
+      if (tid < kRgRounds * 32) sh.tab[tid] = inc - x;
       if (tid == kRgThreads - 1) sh.bc[5] = inc;
     }
     __syncthreads();
     const uint32_t kept = sh.bc[5];
     if (kept >= k_eff && kept <= (uint32_t)kRgKeepCap) {
-      const uint32_t lt = (1u << lane) - 1u;
       uint32_t klo = 0xFFFFFFFFu;
 #pragma unroll
-      for (int u = 0; u < kRgPer; ++u) {
-        const bool in = key[u] >= t_lo && key[u] != 0u;
-        const uint32_t bal = __ballot_sync(0xffffffffu, in);
-        if (in) {
-          const uint32_t slot = sh.tab[u * 32 + wid] + __popc(bal & lt);
-          sh.kkey[slot] = key[u];
-          sh.kidx[slot] = (uint16_t)(u * kRgThreads + tid);
-          klo = min(klo, key[u]);
+      for (int v = 0; v < kRgRounds; ++v) {
+        uint32_t slot = sh.tab[v * 32 + wid] + warp_excl_scan(cnt_v[v]);
+        if (cnt_v[v]) {
+          uint32_t kq[4];
+          int32_t pq[4];
+          // positions of the four elements (the block list is re-read from L1)
+          {
+            const int e0 = 4096 * v + 4 * tid;
+            int blk = 0;
+            if (MODE != kById) blk = __ldg(ev.map + (e0 >> 3));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              kq[j] = key[v][j];
+              pq[j] = MODE == kById ? e0 + j : blk * kBlock + ((e0 + j) & 7);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (kq[j] >= t_lo && kq[j] != 0u) {
+              sh.kkey[slot] = kq[j];
+              sh.kpos[slot] = pq[j];
+              ++slot;
+              klo = min(klo, kq[j]);
+            }
         }
       }
       klo = __reduce_min_sync(0xffffffffu, klo);
@@ -1038,7 +1111,9 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
       T = radix11_kth(
           [&](auto f) {
 #pragma unroll
-            for (int u = 0; u < kRgPer; ++u) f(key[u]);
+            for (int v = 0; v < kRgRounds; ++v)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) f(key[v][j]);
           },
           k_eff, gmin, gmax, sh.hist, sh.wsum, sh.bc, need);
     }
@@ -1046,7 +1121,7 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
   // ---- 5. ordered emission
   int32_t *o = out + (int64_t)n * topk;
   const uint32_t lt = (1u << lane) - 1u;
-  if (m >= 0) {
+  if (m >= 0) {  // the compacted set, element i = rr * 1024 + tid (index order)
     const int rounds = (m + kRgThreads - 1) / kRgThreads;  // <= 8
     for (int rr = 0; rr < rounds; ++rr) {
       const int i = rr * kRgThreads + tid;
@@ -1057,9 +1132,9 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
     }
     __syncthreads();
     {
-      const uint32_t v = tid < rounds * 32 ? sh.tab[tid] : 0u;
-      const uint32_t inc = block_incl_scan_1024(v, sh.wsum);
-      if (tid < rounds * 32) sh.tab[tid] = inc - v;
+      const uint32_t x = tid < rounds * 32 ? sh.tab[tid] : 0u;
+      const uint32_t inc = block_incl_scan_1024(x, sh.wsum);
+      if (tid < rounds * 32) sh.tab[tid] = inc - x;
     }
     __syncthreads();
     for (int rr = 0; rr < rounds; ++rr) {
@@ -1070,30 +1145,42 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
       const uint32_t t = sh.tab[rr * 32 + wid];
       const uint32_t my_gt = (t & 0xFFFFu) + __popc(bgt & lt);
       const uint32_t my_eq = (t >> 16) + __popc(beq & lt);
-      if (gt || (eq && my_eq < need)) o[my_gt + min(my_eq, need)] = ev.pos_of(sh.kidx[i]);
+      if (gt || (eq && my_eq < need)) o[my_gt + min(my_eq, need)] = sh.kpos[i];
     }
-  } else {
+  } else {  // straight from registers: per-round warp scans of (keys > T, keys == T) counts
+    uint32_t c_v[kRgRounds];
 #pragma unroll
-    for (int u = 0; u < kRgPer; ++u) {
-      const uint32_t a = __popc(__ballot_sync(0xffffffffu, key[u] > T));
-      const uint32_t e = __popc(__ballot_sync(0xffffffffu, key[u] == T && key[u] != 0u));
-      if (lane == 0) sh.tab[u * 32 + wid] = a | (e << 16);
+    for (int v = 0; v < kRgRounds; ++v) {
+      uint32_t a = 0u, e = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        a += key[v][j] > T;
+        e += key[v][j] == T && key[v][j] != 0u;
+      }
+      c_v[v] = a | (e << 16);
+      const uint32_t wt = __reduce_add_sync(0xffffffffu, c_v[v]);
+      if (lane == 0) sh.tab[v * 32 + wid] = wt;
     }
     __syncthreads();
     {
-      const uint32_t v = tid < kRgPer * 32 ? sh.tab[tid] : 0u;
-      const uint32_t inc = block_incl_scan_1024(v, sh.wsum);
-      if (tid < kRgPer * 32) sh.tab[tid] = inc - v;
+      const uint32_t x = tid < kRgRounds * 32 ? sh.tab[tid] : 0u;
+      const uint32_t inc = block_incl_scan_1024(x, sh.wsum);
+      if (tid < kRgRounds * 32) sh.tab[tid] = inc - x;
     }
     __syncthreads();
 #pragma unroll
-    for (int u = 0; u < kRgPer; ++u) {
-      const bool gt = key[u] > T, eq = key[u] == T && key[u] != 0u;
-      const uint32_t bgt = __ballot_sync(0xffffffffu, gt), beq = __ballot_sync(0xffffffffu, eq);
-      const uint32_t t = sh.tab[u * 32 + wid];
-      const uint32_t my_gt = (t & 0xFFFFu) + __popc(bgt & lt);
-      const uint32_t my_eq = (t >> 16) + __popc(beq & lt);
-      if (gt || (eq && my_eq < need)) o[my_gt + min(my_eq, need)] = ev.pos_of(u * kRgThreads + tid);
+    for (int v = 0; v < kRgRounds; ++v) {
+      const uint32_t base = sh.tab[v * 32 + wid] + warp_excl_scan(c_v[v]);
+      uint32_t my_gt = base & 0xFFFFu, my_eq = base >> 16;
+      const int e0 = 4096 * v + 4 * tid;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t kk = key[v][j];
+        const bool gt = kk > T, eq = kk == T && kk != 0u;
+        if (gt || (eq && my_eq < need)) o[my_gt + min(my_eq, need)] = ev.pos_of(e0 + j);
+        my_gt += gt;
+        my_eq += eq;
+      }
     }
   }
   for (int i = (int)k_eff + tid; i < topk; i += kRgThreads) o[i] = -1;
