@@ -99,10 +99,9 @@ struct TopkShared {
   uint32_t s_a, s_b;
   uint32_t hist[8][256];
   uint32_t bcast[2];
-  uint32_t hist11[2][2048];  // radix11_kth (zero between uses)
+  __align__(16) uint32_t hist11[2][2048];  // radix11_kth (zero between uses)
   uint32_t tab[512];
-  uint32_t wsum[32];
-  uint32_t bc[4];
+  uint32_t rsc[68];  // radix11_kth scratch
 };
 
 constexpr int kClBits = 11;  // radix digit width of the register and shared-memory selections
@@ -124,23 +123,83 @@ __device__ __forceinline__ uint32_t block_incl_scan_1024(uint32_t v, uint32_t *w
   return inc;
 }
 
+// Exclusive prefix of tab[0 .. count) in place (count <= 32 * MAXPER), by warp 0 alone; the sum
+// goes to *total.  Callers put a barrier before (table complete) and after (results visible).
+template <int MAXPER>
+__device__ __forceinline__ void warp0_excl_scan_table(uint32_t *tab, int count, uint32_t *total) {
+  const int lane = threadIdx.x & 31;
+  const int per = (count + 31) / 32;
+  uint32_t v[MAXPER], sum = 0u;
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i) {
+    const int idx = lane * per + i;
+    v[i] = (i < per && idx < count) ? tab[idx] : 0u;
+    sum += v[i];
+  }
+  const uint32_t inc = warp_incl_scan(sum);
+  uint32_t run = inc - sum;
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i) {
+    const int idx = lane * per + i;
+    if (i < per && idx < count) {
+      tab[idx] = run;
+      run += v[i];
+    }
+  }
+  if (lane == 31 && total) *total = inc;
+}
+
 // k-th largest (1 <= k <= number of candidates) of the keys this block visits: visit(f) calls
 // f(key) for each of the calling thread's keys (0 = not a candidate); all candidates lie in
-// [lo, hi].  11-bit digits below the leading bits lo and hi share; hist[0] is zero on entry and
-// both buffers are zero on return.  need = k - #(keys > T).
+// [lo, hi].  11-bit digits below the leading bits lo and hi share: a shared histogram per digit
+// (atomics), a block-wide scan of its 2,048 bins from the top.  Once at most 32 keys remain in
+// play, one warp ranks them directly instead of further digits.  hist[0] is zero on entry and
+// both buffers are zero on return; sc is scratch for 2 * 32 + 4 words.  need = k - #(keys > T).
+// Block size 1024.
 template <class Visit>
 __device__ uint32_t radix11_kth(Visit visit, uint32_t k, uint32_t lo, uint32_t hi,
-                                uint32_t (*hist)[kClBins], uint32_t *wsum, uint32_t *bc,
-                                uint32_t &need) {
-  const int tid = threadIdx.x;
+                                uint32_t (*hist)[kClBins], uint32_t *sc, uint32_t &need) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t *wsum = sc, *small = sc + 32, *bc = sc + 64;
   int b = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
   uint32_t T = b >= 32 ? 0u : (hi & ~((1u << b) - 1u));
   uint32_t rem = k;
+  uint32_t in_play = 0xFFFFFFFFu;  // keys in play before the digit (unknown at first)
   int pb = 0;
   while (b > 0) {
+    const int hs = b;  // keys in play share T's bits at and above hs
+    if (in_play <= 32u) {
+      // gather the (at most 32) keys in play, rank them in one warp
+      if (tid == 0) bc[3] = 0u;
+      __syncthreads();
+      const uint32_t Tc = T;
+      visit([&](uint32_t key) {
+        if (key != 0u && (hs >= 32 || (key >> hs) == (Tc >> hs))) small[atomicAdd(&bc[3], 1u)] = key;
+      });
+      __syncthreads();
+      if (tid < 32) {
+        const uint32_t cnt = bc[3];
+        const uint32_t mine = (uint32_t)lane < cnt ? small[lane] : 0u;
+        uint32_t g = 0u, e = 0u;
+        for (uint32_t j = 0; j < cnt; ++j) {
+          const uint32_t x = small[j];
+          g += x > mine;
+          e += x == mine;
+        }
+        // the key with g < rem <= g + e (equal keys agree)
+        if ((uint32_t)lane < cnt && g < rem && rem <= g + e) {
+          bc[0] = mine;
+          bc[1] = g;
+        }
+      }
+      __syncthreads();
+      T = bc[0];
+      rem -= bc[1];
+      break;
+    }
     const int w = b >= kClBits ? kClBits : b;
     b -= w;
-    const int s = b, hs = s + w;
+    const int s = b;
     uint32_t *h = hist[pb];
     const uint32_t Tc = T;
     visit([&](uint32_t key) {
@@ -153,14 +212,16 @@ __device__ uint32_t radix11_kth(Visit visit, uint32_t k, uint32_t lo, uint32_t h
     const uint32_t inc = block_incl_scan_1024(c0 + c1, wsum), exc = inc - c0 - c1;
     h[hb0] = 0u;  // every read of this buffer happened before the scan's barriers
     h[hb1] = 0u;
-    if (exc < rem && inc >= rem) {
+    if (exc < rem && inc >= rem) {  // exactly one thread: the keys in play number >= rem
       const bool first = exc + c0 >= rem;
       bc[0] = (uint32_t)(first ? hb0 : hb1);
       bc[1] = first ? exc : exc + c0;
+      bc[2] = first ? c0 : c1;
     }
     __syncthreads();
     T |= bc[0] << s;
     rem -= bc[1];
+    in_play = bc[2];
     __syncthreads();  // bc is rewritten by the next digit
     pb ^= 1;
   }
@@ -446,7 +507,7 @@ __device__ void select_and_emit(const SmemView &sv, int64_t n_elems, int topk, T
         [&](auto f) {
           for (int i = tid; i < m; i += kTopkThreads) f(sv.key[i]);
         },
-        k_eff, lo, hi, sh.hist11, sh.wsum, sh.bc, need);
+        k_eff, lo, hi, sh.hist11, sh.rsc, need);
   const int rounds = (m + kTopkThreads - 1) / kTopkThreads;  // <= 16
   for (int rr = 0; rr < rounds; ++rr) {
     const int i = rr * kTopkThreads + tid;
@@ -456,11 +517,7 @@ __device__ void select_and_emit(const SmemView &sv, int64_t n_elems, int topk, T
     if (lane == 0) sh.tab[rr * 32 + wid] = a | (e << 16);
   }
   __syncthreads();
-  {
-    const uint32_t v = tid < rounds * 32 ? sh.tab[tid] : 0u;
-    const uint32_t inc = block_incl_scan_1024(v, sh.wsum);
-    if (tid < rounds * 32) sh.tab[tid] = inc - v;
-  }
+  if (wid == 0) warp0_excl_scan_table<16>(sh.tab, rounds * 32, nullptr);
   __syncthreads();
   const uint32_t lt = (1u << lane) - 1u;
   for (int rr = 0; rr < rounds; ++rr) {
@@ -889,9 +946,9 @@ constexpr int kRgKeepCap = 8192;
 static_assert(kRgKeepCap / kRgThreads >= kRgRounds, "round table");
 
 struct RgShared {
-  uint32_t hist[2][kClBins];
+  __align__(16) uint32_t hist[2][kClBins];
   uint32_t tab[(kRgKeepCap / kRgThreads) * 32];  // per (round, warp); 8 rounds of the compacted set
-  uint32_t wsum[32];
+  uint32_t rsc[68];  // radix11_kth scratch
   uint32_t red[3][32];
   uint32_t samp[kRgSample];
   uint32_t sg[kRgSample], se[kRgSample];
@@ -1059,12 +1116,7 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
       if (lane == 0) sh.tab[v * 32 + wid] = wt;
     }
     __syncthreads();
-    {
-      const uint32_t x = tid < kRgRounds * 32 ? sh.tab[tid] : 0u;
-      const uint32_t inc = block_incl_scan_1024(x, sh.wsum);
-      if (tid < kRgRounds * 32) sh.tab[tid] = inc - x;
-      if (tid == kRgThreads - 1) sh.bc[5] = inc;
-    }
+    if (wid == 0) warp0_excl_scan_table<8>(sh.tab, kRgRounds * 32, &sh.bc[5]);
     __syncthreads();
     const uint32_t kept = sh.bc[5];
     if (kept >= k_eff && kept <= (uint32_t)kRgKeepCap) {
@@ -1106,7 +1158,7 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
           [&](auto f) {
             for (int i = tid; i < m; i += kRgThreads) f(sh.kkey[i]);
           },
-          k_eff, klo, gmax, sh.hist, sh.wsum, sh.bc, need);
+          k_eff, klo, gmax, sh.hist, sh.rsc, need);
     } else {
       T = radix11_kth(
           [&](auto f) {
@@ -1115,7 +1167,7 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
 #pragma unroll
               for (int j = 0; j < 4; ++j) f(key[v][j]);
           },
-          k_eff, gmin, gmax, sh.hist, sh.wsum, sh.bc, need);
+          k_eff, gmin, gmax, sh.hist, sh.rsc, need);
     }
   }
   // ---- 5. ordered emission
@@ -1131,11 +1183,7 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
       if (lane == 0) sh.tab[rr * 32 + wid] = a | (e << 16);
     }
     __syncthreads();
-    {
-      const uint32_t x = tid < rounds * 32 ? sh.tab[tid] : 0u;
-      const uint32_t inc = block_incl_scan_1024(x, sh.wsum);
-      if (tid < rounds * 32) sh.tab[tid] = inc - x;
-    }
+    if (wid == 0) warp0_excl_scan_table<8>(sh.tab, rounds * 32, nullptr);
     __syncthreads();
     for (int rr = 0; rr < rounds; ++rr) {
       const int i = rr * kRgThreads + tid;
@@ -1162,11 +1210,7 @@ __global__ void __launch_bounds__(kRgThreads, 1) topk_reg_kernel(
       if (lane == 0) sh.tab[v * 32 + wid] = wt;
     }
     __syncthreads();
-    {
-      const uint32_t x = tid < kRgRounds * 32 ? sh.tab[tid] : 0u;
-      const uint32_t inc = block_incl_scan_1024(x, sh.wsum);
-      if (tid < kRgRounds * 32) sh.tab[tid] = inc - x;
-    }
+    if (wid == 0) warp0_excl_scan_table<8>(sh.tab, kRgRounds * 32, nullptr);
     __syncthreads();
 #pragma unroll
     for (int v = 0; v < kRgRounds; ++v) {
