@@ -305,8 +305,8 @@ int csa2_sparse_attn_decode(const void *q_bf16, int B, int H, const uint8_t *cod
   if (int r = check_device()) return r;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (attn_mma_supported(H, topk))
-    return cuda_status(launch_attn_mma(q_bf16, nullptr, nullptr, B, H, nullptr, codes, sf, cu_ctx,
-                                       idx, topk, softmax_scale, out_bf16, lse, workspace, st));
+    return cuda_status(launch_attn_mma(q_bf16, B, H, codes, sf, cu_ctx, idx, topk, softmax_scale,
+                                       out_bf16, lse, workspace, st));
   return cuda_status(launch_attn(q_bf16, nullptr, nullptr, B, H, nullptr, codes, sf, cu_ctx, idx,
                                  topk, softmax_scale, out_bf16, lse, workspace, st));
 }

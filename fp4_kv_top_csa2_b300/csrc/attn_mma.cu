@@ -4,18 +4,19 @@
 // the same rows (K = V = the dequantised latent row; the model card's Introduction, CSA2
 // paragraph: attention reuses "Top-K sparse-attention indices" into the FP4 main KV).
 //
-// One CTA = one query (sequence) x one tile of 64 selected rows, all heads (H <= 64, padded to
-// the M=128 MMA shape).  Steps:
-//   1. Q [H x 512] bf16 arrives by TMA as eight 128B-swizzled K-chunks of 64 channels; each
-//      selected row arrives as two bulk copies (256 B of codes, 32 B of scales).
+// One CTA = one query (sequence) x one tile of 32 selected rows x one group of 32 heads (M=128
+// MMA shape, heads padded).  Small tiles keep the chain of dependent steps short and spread one
+// query over many SMs (64 x 2 CTAs for 2,048 rows and 64 heads).  Steps:
+//   1. Q [32 heads x 512] bf16 arrives by TMA as eight 128B-swizzled K-chunks of 64 channels;
+//      each selected row arrives as two bulk copies (256 B of codes, 32 B of scales).
 //   2. Every row is dequantised exactly (E2M1 x E4M3 has <= 6 significant bits) to bf16 and
-//      stored once, as eight 128B-swizzled chunks [64 rows x 64 channels].
-//   3. S = Q Khat^T: kind::f16, M=128 (heads) x N=64 (rows) x K=512, fp32 in TMEM.
-//   4. Softmax rows (exp2 domain; four warps, two per 32-column half of S), P split into bf16
+//      stored once, as eight 128B-swizzled chunks [32 rows x 64 channels].
+//   3. S = Q Khat^T: kind::f16, M=128 (heads) x N=32 (rows) x K=512, fp32 in TMEM.
+//   4. Softmax rows (exp2 domain; two warps, one per 16-column half of S), P split into bf16
 //      hi + lo parts (P ~ hi + lo to 2^-17).
 //   5. O^T = Vhat^T (P_hi + P_lo)^T: kind::f16, the same dequantised chunks read as the
 //      MN-major A operand (channels contiguous, M=128 channels = two chunks), P as the K-major
-//      B operand (N=64 heads), fp32 in TMEM columns 0..255 (S lives in 256..319).
+//      B operand (N=32 heads, K=32 rows), fp32 in TMEM columns 0..127 (S lives in 128..159).
 //   6. Channels on TMEM lanes make the epilogue coalesced: a warp stores 32 consecutive channels
 //      of one head per instruction.  The unnormalised O rows and the per-head (max, sum) go to
 //      workspace; a combine kernel merges the tiles of each query.
@@ -25,30 +26,35 @@
 
 namespace csa2 {
 
-constexpr int kAttTS = 64;          // selected rows per CTA
+constexpr int kAttTS = 32;          // selected rows per CTA
+constexpr int kAttHG = 32;          // heads per CTA
 constexpr int kAttThreads = 256;
-constexpr int kAttTmemCols = 512;
-constexpr int kColS = 256;          // S [heads x rows]; O^T takes columns 0..255
+constexpr int kAttTmemCols = 256;
+constexpr int kColS = 128;          // S [heads x rows]; O^T takes columns 0..127
+constexpr int kChunkBytes = kAttTS * 128;  // one 64-channel chunk of the row tile (4 KB)
+constexpr int kQChunkBytes = kAttHG * 128;  // one 64-channel chunk of Q (4 KB)
 
 // shared-memory layout (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;                         // 8 chunks x (64 rows x 128 B) = 64 KB
-constexpr int kOffK = 64 * 1024;                 // 8 chunks x (64 rows x 128 B) = 64 KB
-constexpr int kOffPhi = 128 * 1024;              // 64 rows x 128 B
-constexpr int kOffPlo = 136 * 1024;              // 64 rows x 128 B
-constexpr int kOffRawC = 144 * 1024;             // 64 rows x 256 B codes
-constexpr int kOffRawS = kOffRawC + kAttTS * 256;  // 64 rows x 32 B scales
-constexpr int kOffLut = kOffRawS + kAttTS * 32;    // 256 x u32
+constexpr int kOffQ = 0;                              // 8 chunks x (32 heads x 128 B) = 32 KB
+constexpr int kOffK = 8 * kQChunkBytes;               // 8 chunks x (32 rows x 128 B) = 32 KB
+constexpr int kOffPhi = kOffK + 8 * kChunkBytes;      // 32 heads x 128 B (64 B used)
+constexpr int kOffPlo = kOffPhi + 4096;
+constexpr int kOffRawC = kOffPlo + 4096;              // 32 rows x 256 B codes
+constexpr int kOffRawS = kOffRawC + kAttTS * 256;     // 32 rows x 32 B scales
+constexpr int kOffLut = kOffRawS + kAttTS * 32;       // 256 x u32
 constexpr int kOffMisc = kOffLut + 1024;
-constexpr int kAttSmem = kOffMisc + 1024 + 1024;  // + alignment slack
-// The M=128 operand read of Q chunk 7 runs 8 KB past its 64 real rows, into K-chunk 0:
-// readable, and it only feeds unused accumulator lanes.
+constexpr int kAttSmem = kOffMisc + 1024 + 1024;      // + alignment slack
+// The M=128 operand read of a Q chunk covers 128 rows of 128 B from the chunk's start, i.e. up
+// to 12 KB past its 32 real rows (into the following chunks and the row tile): readable, and it
+// only feeds unused accumulator lanes.
+static_assert(kOffQ + 7 * kQChunkBytes + 128 * 128 <= kOffMisc, "Q over-read stays in smem");
 
 struct AttMisc {
   uint64_t bar_q, bar_g, bar_s, bar_o;
   uint32_t tmem_base;
   int slot_ok[kAttTS];
-  float m2[64];
-  float mh[2][64], lh[2][64];  // per-half row max / sum of the softmax
+  float m2[kAttHG];
+  float mh[2][kAttHG], lh[2][kAttHG];  // per-half row max / sum of the softmax
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -76,14 +82,11 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <bool kQfp4>
 __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
-    const __grid_constant__ CUtensorMap qmap, const uint8_t *__restrict__ q_codes,
-    const uint8_t *__restrict__ q_sf, int H, const int32_t *__restrict__ q_seq,
-    const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf,
-    const int64_t *__restrict__ cu_ctx, const int32_t *__restrict__ idx, int topk,
-    float scale_log2e, int n_tiles, float *__restrict__ o_part, float *__restrict__ m_part,
-    float *__restrict__ l_part) {
+    const __grid_constant__ CUtensorMap qmap, int H, const uint8_t *__restrict__ codes,
+    const uint8_t *__restrict__ sf, const int64_t *__restrict__ cu_ctx,
+    const int32_t *__restrict__ idx, int topk, float scale_log2e, int n_tiles,
+    float *__restrict__ o_part, float *__restrict__ m_part, float *__restrict__ l_part) {
   using namespace sm100;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -91,7 +94,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
   AttMisc &ms = *reinterpret_cast<AttMisc *>(sm + kOffMisc);
   uint32_t *lut = reinterpret_cast<uint32_t *>(sm + kOffLut);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x, n = blockIdx.y;
+  const int tile = blockIdx.x, hg = blockIdx.y, n = blockIdx.z;
+  const int h0 = hg * kAttHG;  // first head of this CTA
 
   if (tid == 0) {
     mbar_init(&ms.bar_q, 1);
@@ -99,6 +103,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
     mbar_init(&ms.bar_s, 1);
     mbar_init(&ms.bar_o, 1);
     fence_barrier_init();
+    prefetch_tensormap(&qmap);
   }
   if (warp == 0) {
     tmem_alloc(&ms.tmem_base, kAttTmemCols);
@@ -112,12 +117,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
   const uint32_t tmem = ms.tmem_base;
   pdl_wait();
   pdl_trigger();
-  const int64_t base = cu_ctx[q_seq ? q_seq[n] : n];
+  const int64_t base = cu_ctx[n];
 
   // ---- 1. loads
-  if (!kQfp4 && tid == 0) {
-    mbar_arrive_expect_tx(&ms.bar_q, 8 * 64 * 128);
-    for (int kc = 0; kc < 8; ++kc) tma_load_2d(sm + kOffQ + kc * 8192, &qmap, &ms.bar_q, kc * 64, n * H);
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&ms.bar_q, 8 * kQChunkBytes);
+    for (int kc = 0; kc < 8; ++kc)
+      tma_load_2d(sm + kOffQ + kc * kQChunkBytes, &qmap, &ms.bar_q, kc * 64, n * H + h0);
   }
   if (tid < kAttTS) {
     const int slot = tile * kAttTS + tid;
@@ -138,27 +144,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
       mbar_arrive(&ms.bar_g);
     }
   }
-  if (kQfp4) {  // prefill: exactly dequantised FP4 query rows into the swizzled Q chunks
-    for (int v = tid; v < 64 * 64; v += kAttThreads) {
-      const int h = v >> 6, rest = v & 63, kc = rest >> 3, u = rest & 7;
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if (h < H) {
-        const int64_t qrow = (int64_t)n * H + h;
-        const int c0 = kc * 64 + u * 8;
-        const uint32_t cw = *reinterpret_cast<const uint32_t *>(q_codes + qrow * kCodeBytes + c0 / 2);
-        const float sc = e4m3_to_float(q_sf[qrow * kSfBytes + c0 / 16]);
-        const uint32_t s2 = pack_bf16x2(sc, sc);
-        w.x = bf16x2_mul(lut[cw & 0xFF], s2);
-        w.y = bf16x2_mul(lut[(cw >> 8) & 0xFF], s2);
-        w.z = bf16x2_mul(lut[(cw >> 16) & 0xFF], s2);
-        w.w = bf16x2_mul(lut[cw >> 24], s2);
-      }
-      *reinterpret_cast<uint4 *>(sm + kOffQ + kc * 8192 + h * 128 + ((u ^ (h & 7)) << 4)) = w;
-    }
-  }
   bool ok = mbar_wait(&ms.bar_g, 0);
 
-  // ---- 2. dequantise the rows once: chunk kc holds channels 64kc..64kc+63 of all 64 rows
+  // ---- 2. dequantise the rows once: chunk kc holds channels 64kc..64kc+63 of all 32 rows
   for (int v = tid; v < kAttTS * 64; v += kAttThreads) {
     const int j = v >> 6, rest = v & 63, kc = rest >> 3, u = rest & 7;
     const int c0 = kc * 64 + u * 8;
@@ -170,7 +158,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
     w.y = bf16x2_mul(lut[(cw >> 8) & 0xFF], s2);
     w.z = bf16x2_mul(lut[(cw >> 16) & 0xFF], s2);
     w.w = bf16x2_mul(lut[cw >> 24], s2);
-    *reinterpret_cast<uint4 *>(sm + kOffK + kc * 8192 + j * 128 + ((u ^ (j & 7)) << 4)) = w;
+    *reinterpret_cast<uint4 *>(sm + kOffK + kc * kChunkBytes + j * 128 + ((u ^ (j & 7)) << 4)) =
+        w;
   }
   fence_async_smem();
   tc_fence_before();
@@ -179,57 +168,53 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
 
   // ---- 3. S = Q Khat^T
   if (tid == 0) {
-    if (!kQfp4) ok = ok && mbar_wait(&ms.bar_q, 0);
+    ok = ok && mbar_wait(&ms.bar_q, 0);
     constexpr uint32_t idesc = idesc_f32acc(1, 1, 128, kAttTS);
     const uint32_t qa = smem_u32(sm + kOffQ), ka = smem_u32(sm + kOffK);
     for (int kc = 0; kc < 8; ++kc)
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_f16(tmem + kColS, desc_k128_sw128(qa + kc * 8192 + 32 * ks),
-                desc_k128_sw128(ka + kc * 8192 + 32 * ks), idesc, (kc | ks) != 0);
+        mma_f16(tmem + kColS, desc_k128_sw128(qa + kc * kQChunkBytes + 32 * ks),
+                desc_k128_sw128(ka + kc * kChunkBytes + 32 * ks), idesc, (kc | ks) != 0);
     mma_commit(&ms.bar_s);
   }
 
-  // ---- 4. softmax: warps 0,1 and 4,5 read TMEM lanes 0..63 (= heads); warps 0,1 take the
-  //         columns (rows) 0..31 of S, warps 4,5 the columns 32..63
-  if ((warp & 3) < 2) {
+  // ---- 4. softmax: warps 0 and 4 read TMEM lanes 0..31 (= heads); warp 0 takes the columns
+  //         (rows) 0..15 of S, warp 4 the columns 16..31
+  if ((warp & 3) == 0) {
     ok = __all_sync(0xffffffffu, mbar_wait(&ms.bar_s, 0)) && ok;
     tc_fence_after();
-    const int h = (warp & 3) * 32 + lane;
-    const int half = warp >> 2, j0 = half * 32;
-    float s[32];
+    const int h = lane;
+    const int half = warp >> 2, j0 = half * 16;
+    float s[16];
     {
-      const uint32_t la = tmem + kColS + j0 + ((uint32_t)((warp & 3) * 32) << 16);
-      uint32_t r[2][16];
-      tmem_ld16(la, r[0]);
-      tmem_ld16(la + 16, r[1]);
+      uint32_t r[16];
+      tmem_ld16(tmem + kColS + j0, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) s[16 * c + i] = __uint_as_float(r[c][i]) * scale_log2e;
+      for (int i = 0; i < 16; ++i) s[i] = __uint_as_float(r[i]) * scale_log2e;
     }
     float m = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
+    for (int j = 0; j < 16; ++j)
       if (ms.slot_ok[j0 + j]) m = fmaxf(m, s[j]);
     ms.mh[half][h] = m;
-    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps
+    asm volatile("bar.sync 1, 64;" ::: "memory");  // the two softmax warps
     m = fmaxf(ms.mh[0][h], ms.mh[1][h]);
     float l = 0.0f;
-    uint32_t hi[16], lo[16];
+    uint32_t hi[8], lo[8];
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
+    for (int j = 0; j < 16; j += 2) {
       const float p0 = ms.slot_ok[j0 + j] ? exp2f(s[j] - m) : 0.0f;
       const float p1 = ms.slot_ok[j0 + j + 1] ? exp2f(s[j + 1] - m) : 0.0f;
       l += p0 + p1;
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
-      hi[j / 2] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-      lo[j / 2] = pack_bf16x2(p0 - __bfloat162float(h0), p1 - __bfloat162float(h1));
+      const __nv_bfloat16 b0 = __float2bfloat16_rn(p0), b1 = __float2bfloat16_rn(p1);
+      hi[j / 2] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
+      lo[j / 2] = pack_bf16x2(p0 - __bfloat162float(b0), p1 - __bfloat162float(b1));
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int off = h * 128 + (((4 * half + u) ^ (h & 7)) << 4);
+    for (int u = 0; u < 2; ++u) {
+      const int off = h * 128 + (((2 * half + u) ^ (h & 7)) << 4);
       *reinterpret_cast<uint4 *>(sm + kOffPhi + off) =
           make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
       *reinterpret_cast<uint4 *>(sm + kOffPlo + off) =
@@ -243,46 +228,47 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
   __syncthreads();
   tc_fence_after();
 
-  // ---- 5. O^T = Vhat^T P^T: M=128 channels (two chunks), N=64 heads, K=16 rows per MMA
+  // ---- 5. O^T = Vhat^T P^T: M=128 channels (two chunks), N=32 heads, K=16 rows per MMA
   if (tid == 0) {
-    constexpr uint32_t idesc_pv = idesc_f32acc(1, 1, 128, 64) | (1u << 15);  // A MN-major
+    constexpr uint32_t idesc_pv = idesc_f32acc(1, 1, 128, kAttHG) | (1u << 15);  // A MN-major
     const uint32_t ka = smem_u32(sm + kOffK);
     const uint32_t ph = smem_u32(sm + kOffPhi), pl = smem_u32(sm + kOffPlo);
     for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
       for (int ks = 0; ks < kAttTS / 16; ++ks) {
-        const uint64_t ad = desc_mn_sw128_atoms(ka + (2 * mb) * 8192 + ks * 16 * 128, 8192);
-        mma_f16(tmem + mb * 64, ad, desc_k128_sw128(ph + 32 * ks), idesc_pv, ks != 0);
-        mma_f16(tmem + mb * 64, ad, desc_k128_sw128(pl + 32 * ks), idesc_pv, 1);
+        const uint64_t ad =
+            desc_mn_sw128_atoms(ka + (2 * mb) * kChunkBytes + ks * 16 * 128, kChunkBytes);
+        mma_f16(tmem + mb * kAttHG, ad, desc_k128_sw128(ph + 32 * ks), idesc_pv, ks != 0);
+        mma_f16(tmem + mb * kAttHG, ad, desc_k128_sw128(pl + 32 * ks), idesc_pv, 1);
       }
     }
     mma_commit(&ms.bar_o);
   }
 
-  // ---- 6. epilogue: warp w reads lanes 32(w%4).. (channels) and heads 32(w/4)..+31 of every
-  //         M block; column 64*mb + h of O^T is channel 128*mb + lane
+  // ---- 6. epilogue: warp w reads lanes 32(w%4).. (channels) of M blocks 2(w/4), 2(w/4)+1;
+  //         column 32*mb + h of O^T is channel 128*mb + lane
   ok = __all_sync(0xffffffffu, mbar_wait(&ms.bar_o, 0)) && ok;
   tc_fence_after();
   {
-    const int q4 = warp & 3, hh = warp >> 2;
+    const int q4 = warp & 3, mb0 = (warp >> 2) * 2;
     const uint32_t la = tmem + ((uint32_t)(q4 * 32) << 16);
-    float *obase = o_part + ((int64_t)n * n_tiles + tile) * H * kD;
+    float *obase = o_part + (((int64_t)n * n_tiles + tile) * H + h0) * kD;
+    const int hn = min(kAttHG, H - h0);  // real heads of this group
 #pragma unroll 1
-    for (int mb = 0; mb < 4; ++mb) {
+    for (int mb = mb0; mb < mb0 + 2; ++mb) {
       uint32_t r0[16], r1[16];
-      tmem_ld16(la + mb * 64 + hh * 32, r0);
-      tmem_ld16(la + mb * 64 + hh * 32 + 16, r1);
+      tmem_ld16(la + mb * kAttHG, r0);
+      tmem_ld16(la + mb * kAttHG + 16, r1);
       tmem_ld_wait();
       float *oc = obase + mb * 128 + q4 * 32 + lane;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const int h0 = hh * 32 + i, h1 = h0 + 16;
-        if (h0 < H) oc[(int64_t)h0 * kD] = __uint_as_float(r0[i]);
-        if (h1 < H) oc[(int64_t)h1 * kD] = __uint_as_float(r1[i]);
+        if (i < hn) oc[(int64_t)i * kD] = __uint_as_float(r0[i]);
+        if (i + 16 < hn) oc[(int64_t)(i + 16) * kD] = __uint_as_float(r1[i]);
       }
     }
-    if (tid < H) {
-      const int64_t pr = ((int64_t)n * n_tiles + tile) * H + tid;
+    if (tid < hn) {
+      const int64_t pr = ((int64_t)n * n_tiles + tile) * H + h0 + tid;
       m_part[pr] = ok ? ms.m2[tid] : -INFINITY;
       l_part[pr] = ok ? ms.lh[0][tid] + ms.lh[1][tid] : 0.0f;
     }
@@ -295,63 +281,64 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
 
 // Merge the tiles of each (query, head): out = sum_t O_t 2^(m_t - M) / sum_t l_t 2^(m_t - M);
 // lse = (M + log2 L) * ln 2.  m is in the log2 domain (logits * scale * log2 e).
-// Grid (kD / 128, H, nq), 128 threads: thread = one channel.  The channel's partials of up to
-// 32 tiles are loaded at once (before the weights are known), then summed in tile order.
+// Grid (kD / 128, H, nq), 128 threads: thread = one channel.  The channel's partials are read 32
+// tiles at a time with unconditional loads (indices clamped, so all 32 are in flight at once;
+// the first batch before the weights are known), then summed in tile order.
 constexpr int kCombBatch = 32;
 __global__ void __launch_bounds__(128) attn_mma_combine_kernel(
     int H, int n_tiles, const float *__restrict__ o_part, const float *__restrict__ m_part,
     const float *__restrict__ l_part, uint16_t *__restrict__ out, float *__restrict__ lse) {
-  __shared__ float wgt[256];
-  __shared__ float sM, sL;
   pdl_wait();
   pdl_trigger();
+  __shared__ float wgt[256];
+  __shared__ float sM, sL;
   const int h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x, lane = tid & 31;
   const int c = blockIdx.x * 128 + tid;
   const int64_t tstride = (int64_t)H * kD;  // floats between consecutive tiles
   const float *op = o_part + ((int64_t)n * n_tiles * H + h) * kD + c;
-  float o[kCombBatch];
-#pragma unroll
-  for (int u = 0; u < kCombBatch; ++u) o[u] = u < n_tiles ? op[u * tstride] : 0.0f;
-  if (tid < 32) {  // per-tile weights (n_tiles <= 256)
-    float mt[8], lt[8];
-    float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int t = lane + 32 * k;
-      mt[k] = -INFINITY;
-      lt[k] = 0.0f;
-      if (t < n_tiles) {
-        const int64_t pr = ((int64_t)n * n_tiles + t) * H + h;
-        lt[k] = l_part[pr];
-        mt[k] = m_part[pr];
-        if (lt[k] > 0.0f) M = fmaxf(M, mt[k]);
-      }
-    }
-    M = warp_max(M);
-    float Lp = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int t = lane + 32 * k;
-      if (t < n_tiles) {
-        const float wv = (lt[k] > 0.0f) ? exp2f(mt[k] - M) : 0.0f;
-        wgt[t] = wv;
-        Lp += lt[k] * wv;
-      }
-    }
-    Lp = warp_sum(Lp);
-    if (lane == 0) {
-      sM = M;
-      sL = Lp;
-    }
-  }
-  __syncthreads();
   float acc = 0.0f;
+  for (int t0 = 0; t0 < n_tiles; t0 += kCombBatch) {
+    float o[kCombBatch];
 #pragma unroll
-  for (int u = 0; u < kCombBatch; ++u)
-    if (u < n_tiles) acc = fmaf(o[u], wgt[u], acc);
-  for (int t0 = kCombBatch; t0 < n_tiles; t0 += kCombBatch) {
+    for (int u = 0; u < kCombBatch; ++u) {
+      const int t = min(t0 + u, n_tiles - 1);
+      o[u] = op[t * tstride];
+    }
+    if (t0 == 0) {
+      if (tid < 32) {  // per-tile weights (n_tiles <= 256)
+        float mt[8], lt[8];
+        float M = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < kCombBatch; ++u) o[u] = t0 + u < n_tiles ? op[(t0 + u) * tstride] : 0.0f;
+        for (int k = 0; k < 8; ++k) {
+          const int t = lane + 32 * k;
+          mt[k] = -INFINITY;
+          lt[k] = 0.0f;
+          if (t < n_tiles) {
+            const int64_t pr = ((int64_t)n * n_tiles + t) * H + h;
+            lt[k] = l_part[pr];
+            mt[k] = m_part[pr];
+            if (lt[k] > 0.0f) M = fmaxf(M, mt[k]);
+          }
+        }
+        M = warp_max(M);
+        float Lp = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int t = lane + 32 * k;
+          if (t < n_tiles) {
+            const float wv = (lt[k] > 0.0f) ? exp2f(mt[k] - M) : 0.0f;
+            wgt[t] = wv;
+            Lp += lt[k] * wv;
+          }
+        }
+        Lp = warp_sum(Lp);
+        if (lane == 0) {
+          sM = M;
+          sL = Lp;
+        }
+      }
+      __syncthreads();
+    }
 #pragma unroll
     for (int u = 0; u < kCombBatch; ++u)
       if (t0 + u < n_tiles) acc = fmaf(o[u], wgt[t0 + u], acc);
@@ -381,7 +368,7 @@ static bool make_q_map(CUtensorMap *m, const void *q, int64_t rows) {
   if (!enc || rows <= 0) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, kAttHG};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -389,8 +376,7 @@ static bool make_q_map(CUtensorMap *m, const void *q, int64_t rows) {
          CUDA_SUCCESS;
 }
 
-cudaError_t launch_attn_mma(const void *q_bf16, const uint8_t *q_codes, const uint8_t *q_sf,
-                            int nq, int H, const int32_t *q_seq, const uint8_t *codes,
+cudaError_t launch_attn_mma(const void *q_bf16, int nq, int H, const uint8_t *codes,
                             const uint8_t *sf, const int64_t *cu_ctx, const int32_t *idx,
                             int topk, float scale, void *out_bf16, float *lse, void *workspace,
                             cudaStream_t st) {
@@ -402,25 +388,15 @@ cudaError_t launch_attn_mma(const void *q_bf16, const uint8_t *q_codes, const ui
   float *l_part = m_part + rows;
   CUtensorMap qm;
   memset(&qm, 0, sizeof(qm));
-  if (q_bf16 && !make_q_map(&qm, q_bf16, (int64_t)nq * H)) return cudaErrorInvalidValue;
+  if (!make_q_map(&qm, q_bf16, (int64_t)nq * H)) return cudaErrorInvalidValue;
   const float scale_log2e = scale * 1.4426950408889634f;
-  dim3 grid(n_tiles, nq);
-  cudaError_t e;
-  if (q_bf16) {
-    e = set_smem_once(attn_mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kAttSmem);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(attn_mma_kernel<false>, grid, dim3(kAttThreads), kAttSmem, st, qm,
-                   (const uint8_t *)nullptr, (const uint8_t *)nullptr, H, q_seq, codes, sf, cu_ctx,
-                   idx, topk, scale_log2e, n_tiles, o_part, m_part, l_part);
-  } else {
-    e = set_smem_once(attn_mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kAttSmem);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(attn_mma_kernel<true>, grid, dim3(kAttThreads), kAttSmem, st, qm, q_codes,
-                   q_sf, H, q_seq, codes, sf, cu_ctx, idx, topk, scale_log2e, n_tiles, o_part,
-                   m_part, l_part);
-  }
+  const int n_hg = (H + kAttHG - 1) / kAttHG;
+  cudaError_t e = set_smem_once(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kAttSmem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(attn_mma_kernel, dim3(n_tiles, n_hg, nq), dim3(kAttThreads), (size_t)kAttSmem,
+                 st, qm, H, codes, sf, cu_ctx, idx, topk, scale_log2e, n_tiles, o_part, m_part,
+                 l_part);
   note_launches(1);
   if (e != cudaSuccess) return e;
   e = launch_pdl(attn_mma_combine_kernel, dim3(kD / 128, H, nq), dim3(128), 0, st, H, n_tiles,

@@ -219,11 +219,11 @@ cudaError_t launch_attn_prefill(const uint8_t *q_codes, const uint8_t *q_sf, int
                                 const int64_t *cu_ctx, const int32_t *idx, int topk, float scale,
                                 void *out_bf16, float *lse, cudaStream_t st);
 
-// Tensor-core decode attention (attn_mma.cu): H <= 64, one CTA per 64 selected rows.
+// Tensor-core decode attention (attn_mma.cu): H <= 64, one CTA per 32 selected rows and 32
+// heads.
 bool attn_mma_supported(int H, int topk);
 size_t attn_mma_workspace_bytes(int nq, int H, int topk);
-cudaError_t launch_attn_mma(const void *q_bf16, const uint8_t *q_codes, const uint8_t *q_sf,
-                            int nq, int H, const int32_t *q_seq, const uint8_t *codes,
+cudaError_t launch_attn_mma(const void *q_bf16, int nq, int H, const uint8_t *codes,
                             const uint8_t *sf, const int64_t *cu_ctx, const int32_t *idx,
                             int topk, float scale, void *out_bf16, float *lse, void *workspace,
                             cudaStream_t st);
