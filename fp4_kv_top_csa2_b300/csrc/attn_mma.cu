@@ -146,37 +146,38 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
   }
   bool ok = mbar_wait(&ms.bar_g, 0);
 
-  // ---- 2. dequantise the rows once: chunk kc holds channels 64kc..64kc+63 of all 32 rows
-  for (int v = tid; v < kAttTS * 64; v += kAttThreads) {
-    const int j = v >> 6, rest = v & 63, kc = rest >> 3, u = rest & 7;
-    const int c0 = kc * 64 + u * 8;
-    const uint32_t cw = *reinterpret_cast<const uint32_t *>(sm + kOffRawC + j * 256 + c0 / 2);
-    const float sc = e4m3_to_float(sm[kOffRawS + j * 32 + c0 / 16]);
-    const uint32_t s2 = pack_bf16x2(sc, sc);
-    uint4 w;
-    w.x = bf16x2_mul(lut[cw & 0xFF], s2);
-    w.y = bf16x2_mul(lut[(cw >> 8) & 0xFF], s2);
-    w.z = bf16x2_mul(lut[(cw >> 16) & 0xFF], s2);
-    w.w = bf16x2_mul(lut[cw >> 24], s2);
-    *reinterpret_cast<uint4 *>(sm + kOffK + kc * kChunkBytes + j * 128 + ((u ^ (j & 7)) << 4)) =
-        w;
-  }
-  fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
-  // ---- 3. S = Q Khat^T
-  if (tid == 0) {
-    ok = ok && mbar_wait(&ms.bar_q, 0);
-    constexpr uint32_t idesc = idesc_f32acc(1, 1, 128, kAttTS);
-    const uint32_t qa = smem_u32(sm + kOffQ), ka = smem_u32(sm + kOffK);
-    for (int kc = 0; kc < 8; ++kc)
+  // ---- 2./3. dequantise the rows once (chunk kc holds channels 64kc..64kc+63 of all 32 rows)
+  //           and S = Q Khat^T: the MMAs over chunks 0..3 run while chunks 4..7 are dequantised
+  constexpr uint32_t idesc = idesc_f32acc(1, 1, 128, kAttTS);
+  for (int half = 0; half < 2; ++half) {
+    for (int v = tid; v < kAttTS * 32; v += kAttThreads) {
+      const int j = v >> 5, rest = v & 31, kc = half * 4 + (rest >> 3), u = rest & 7;
+      const int c0 = kc * 64 + u * 8;
+      const uint32_t cw = *reinterpret_cast<const uint32_t *>(sm + kOffRawC + j * 256 + c0 / 2);
+      const float sc = e4m3_to_float(sm[kOffRawS + j * 32 + c0 / 16]);
+      const uint32_t s2 = pack_bf16x2(sc, sc);
+      uint4 w;
+      w.x = bf16x2_mul(lut[cw & 0xFF], s2);
+      w.y = bf16x2_mul(lut[(cw >> 8) & 0xFF], s2);
+      w.z = bf16x2_mul(lut[(cw >> 16) & 0xFF], s2);
+      w.w = bf16x2_mul(lut[cw >> 24], s2);
+      *reinterpret_cast<uint4 *>(sm + kOffK + kc * kChunkBytes + j * 128 + ((u ^ (j & 7)) << 4)) =
+          w;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+      if (half == 0) ok = ok && mbar_wait(&ms.bar_q, 0);
+      const uint32_t qa = smem_u32(sm + kOffQ), ka = smem_u32(sm + kOffK);
+      for (int kc = half * 4; kc < half * 4 + 4; ++kc)
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_f16(tmem + kColS, desc_k128_sw128(qa + kc * kQChunkBytes + 32 * ks),
-                desc_k128_sw128(ka + kc * kChunkBytes + 32 * ks), idesc, (kc | ks) != 0);
-    mma_commit(&ms.bar_s);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_f16(tmem + kColS, desc_k128_sw128(qa + kc * kQChunkBytes + 32 * ks),
+                  desc_k128_sw128(ka + kc * kChunkBytes + 32 * ks), idesc, (kc | ks) != 0);
+      if (half == 1) mma_commit(&ms.bar_s);
+    }
   }
 
   // ---- 4. softmax: warps 0 and 4 read TMEM lanes 0..31 (= heads); warp 0 takes the columns
@@ -281,10 +282,10 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
 
 // Merge the tiles of each (query, head): out = sum_t O_t 2^(m_t - M) / sum_t l_t 2^(m_t - M);
 // lse = (M + log2 L) * ln 2.  m is in the log2 domain (logits * scale * log2 e).
-// Grid (kD / 128, H, nq), 128 threads: thread = one channel.  The channel's partials are read 32
-// tiles at a time with unconditional loads (indices clamped, so all 32 are in flight at once;
+// Grid (kD / 128, H, nq), 128 threads: thread = one channel.  The channel's partials are read 64
+// tiles at a time with unconditional loads (indices clamped, so all 64 are in flight at once;
 // the first batch before the weights are known), then summed in tile order.
-constexpr int kCombBatch = 32;
+constexpr int kCombBatch = 64;
 __global__ void __launch_bounds__(128) attn_mma_combine_kernel(
     int H, int n_tiles, const float *__restrict__ o_part, const float *__restrict__ m_part,
     const float *__restrict__ l_part, uint16_t *__restrict__ out, float *__restrict__ lse) {
