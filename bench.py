@@ -168,6 +168,10 @@ def run_ours(args, rank, world):
     parts = profile_calls(st, args.steps, flush)
     dom_name, dom_ms, dom_bytes = ("csa2_index_score_topk_pool (Full + pool, 1,048,576 keys)",
                                    parts["full_index"], by["index_keys_full"])
+    # DRAM bytes (read + write) of that call's kernels in one ncu capture of the current code:
+    # scan 134.26 + 4.15 MB, pool filter 0.54 MB, pool select 0.11 MB, position Top-K 0.33 MB.
+    # Reset to None whenever those kernels change.
+    dom_traffic = 139_393_792
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
 
     # end to end through the C ABI with host buffers (direct calls, no graph), and with the graph
@@ -191,7 +195,7 @@ def run_ours(args, rank, world):
         "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "peak_source": peaks["source"] + " (burst copy)", "traffic": None,
+                     "peak_source": peaks["source"] + " (burst copy)", "traffic": dom_traffic,
                      "ms_per_launch": round(dom_ms, 5), "algorithmic_bytes": dom_bytes},
         "breakdown_ms": {k: round(v, 5) for k, v in parts.items()},
         "timing": "step = one CUDA-graph replay of all calls; CUDA events on the launching stream",
@@ -417,6 +421,25 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def profile_step(name, steps, prefill_tokens=0):
+    """A short run for profiler captures: build one workload's step (optionally a prefill with
+    fewer new tokens), run it `steps` times, print one JSON line.  The bf16 source rows are dropped
+    once the cache is quantised, so the device holds only what the step reads."""
+    import torch
+    from fp4_kv_top_csa2_b300 import synth
+    from fp4_kv_top_csa2_b300.step import Step
+    w = synth.WORKLOADS[name]
+    if prefill_tokens and w.kind == "prefill":
+        w = synth.scaled(w, T=prefill_tokens)
+    st = Step(synth.make_inputs(w), device="cuda")
+    st.drop_source_rows()
+    for _ in range(steps):
+        st.run()
+    torch.cuda.synchronize()
+    return {"profile_step": name, "steps": steps, "T": w.T,
+            "device_bytes": torch.cuda.memory_allocated()}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -427,7 +450,16 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-steps", type=int, default=2)
+    ap.add_argument("--profile-step", default=None,
+                    help="run only this workload's step (--steps times) for a profiler capture")
+    ap.add_argument("--prefill-tokens", type=int, default=0,
+                    help="with --profile-step on the prefill workload: new tokens per step")
     args = ap.parse_args()
+    if args.profile_step:
+        sys.path.insert(0, ROOT)
+        print(json.dumps(profile_step(args.profile_step, args.steps, args.prefill_tokens)),
+              flush=True)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     sys.path.insert(0, ROOT)

@@ -75,6 +75,11 @@ class Step:
             self.ws_attn = csa2.workspace(
                 csa2.csa2_sparse_attn_decode_workspace_size(self.nq, w.H, w.topk), dev)
 
+    def drop_source_rows(self):
+        """Free the bf16 rows the cache was quantised from (the step only reads the new rows)."""
+        self.kv_bf16 = None
+        torch.cuda.empty_cache()
+
     # ------------------------------------------------------------------------------------------
     def quantize_new_rows(self, stream=None):
         csa2.csa2_kv_quant_fp4(self.new_x, self.codes, self.sf, out_rows=self.new_rows,
