@@ -230,6 +230,15 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_mma_kernel(
 #pragma unroll
       for (int h = 0; h < kAccCols; ++h) wv[h] = h < p.Hi ? p.w[(int64_t)c.n * p.Hi + h] : 0.0f;
       bool ok = true;
+      // CAND: this row's block id for every tile of the chunk, loaded up front (ct <= 16)
+      int blks[16];
+      if (MODE == kCand) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int cb = (int)((((int64_t)(c.t0 + i)) * kTileKeys + row) >> 3);
+          blks[i] = (c.t0 + i < c.t1 && cb < p.n_cand) ? p.cand[(int64_t)c.n * p.n_cand + cb] : -1;
+        }
+      }
       for (int t = c.t0; t < c.t1; ++t, ++acc) {
         const uint32_t a = acc % kAccBufs, aph = (acc / kAccBufs) & 1;
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.tfull[a], aph));
@@ -249,8 +258,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_mma_kernel(
           valid = pos < V;
         } else {
           slot = (int64_t)t * kTileKeys + row;
-          const int cb = (int)(slot >> 3);
-          const int blk = cb < p.n_cand ? p.cand[(int64_t)c.n * p.n_cand + cb] : -1;
+          int blk = -1;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (t - c.t0 == i) blk = blks[i];
           pos = (int64_t)blk * kBlock + (slot & 7);
           valid = blk >= 0 && pos < V;
         }
