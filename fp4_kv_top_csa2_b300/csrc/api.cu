@@ -53,7 +53,11 @@ struct WsCursor {
 //            the Top-K block list, and either the score of every visible position (tensor-core
 //            path while that array stays small: the final selection reads it by position) or
 //            the scores of the positions of the selected blocks (rescored).
-constexpr int64_t kKeepScoresMax = (int64_t)1 << 27;  // elements
+constexpr int64_t kKeepScoresMax = (int64_t)1 << 27;  // elements (one-query-per-MMA scan)
+// Chunked prefill (more than 1,024 queries, the 32-queries-per-MMA scan): keeping every score
+// (4 B per visible pair, 4.4 GB at 4,096 x 266,240) costs one write pass instead of rescoring
+// 16,384 candidates per query.
+constexpr int64_t kKeepScoresMaxMulti = (int64_t)1 << 31;
 
 struct ScoreWs {
   float *bm = nullptr;
@@ -82,10 +86,12 @@ ScoreWs score_ws(void *base, int nq, int64_t max_vis, int n_cand_blocks, int top
     w.nl = w.pool_list ? n_pool : w.kb;
     w.bm = c.take<float>((size_t)nq * w.nb_max);
     if (!w.pool_list) w.blocks = c.take<int32_t>((size_t)nq * w.kb);
-    if (index_mma_supported(nq) && (int64_t)nq * max_vis <= kKeepScoresMax)
-      w.pos_scores = c.take<float>((size_t)nq * max_vis);
-    else
-      w.scores = c.take<float>((size_t)nq * w.nl * kBlock);
+    const bool keep_mma = index_mma_supported(nq) && (int64_t)nq * max_vis <= kKeepScoresMax;
+    const bool keep_multi = nq > kMaxScanQueries && (int64_t)nq * max_vis <= kKeepScoresMaxMulti;
+    if (keep_mma || keep_multi) w.pos_scores = c.take<float>((size_t)nq * max_vis);
+    // rescoring scratch: always when no score array is kept; with the prefill array too, for
+    // calls that take the CUDA-core scan (several sequences, or not 8 indexer heads)
+    if (!keep_mma) w.scores = c.take<float>((size_t)nq * w.nl * kBlock);
     w.topk = c.take<char>(std::max(topk_workspace_bytes(nq, w.nb_max),
                                    topk_workspace_bytes(nq, (int64_t)w.nl * kBlock)));
   }
@@ -146,12 +152,13 @@ int index_score_topk_impl(const void *q_idx, int q_dtype, const float *w, int nq
   // candidate pool of at least that many blocks (the top blocks by block maximum, the same
   // selection) serves as the block list itself.
   float *bm = out_block_max ? out_block_max : ws.bm;
+  float *pos_scores = (mma || multi) ? ws.pos_scores : nullptr;  // written by the scan
   if (mma) {
     e = launch_score_scan_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx, q_seq,
-                              q_vis, max_vis, bm, ws.nb_max, ws.pos_scores, max_vis, st);
+                              q_vis, max_vis, bm, ws.nb_max, pos_scores, max_vis, st);
   } else if (multi) {  // chunked prefill over one sequence: 32 queries per key tile
     e = launch_score_scan_multi(q_idx, q_dtype, w, nq, k_idx, k_rows, k_scale, q_vis, max_vis,
-                                bm, ws.nb_max, st);
+                                bm, ws.nb_max, pos_scores, max_vis, st);
   } else {
     e = launch_score_scan(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
                           max_vis, bm, ws.nb_max, st);
@@ -163,10 +170,10 @@ int index_score_topk_impl(const void *q_idx, int q_dtype, const float *w, int nq
   if (e == cudaSuccess && n_pool > 0 && !ws.pool_list)  // a pool smaller than the block list
     e = launch_topk(bm, ws.nb_max, ws.nb_max, nullptr, 0, kBlock, q_vis, nq, n_pool, out_pool, st,
                     nullptr, 0, ws.topk);
-  if (ws.pos_scores) {  // the scan kept every score: select among the blocks' positions
+  if (pos_scores) {  // the scan kept every score: select among the blocks' positions
     if (e == cudaSuccess)
       e = launch_topk(nullptr, 0, (int64_t)ws.nl * kBlock, list, ws.nl, 1, q_vis, nq, topk,
-                      out_idx, st, ws.pos_scores, max_vis, ws.topk);
+                      out_idx, st, pos_scores, max_vis, ws.topk);
     return cuda_status(e);
   }
   if (e == cudaSuccess)

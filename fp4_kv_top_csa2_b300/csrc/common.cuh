@@ -193,7 +193,8 @@ bool index_multi_supported(int nq, int Hi, int B);  // 32-query scan over one se
 cudaError_t launch_score_scan_multi(const void *q_idx, int dtype, const float *w, int nq,
                                     const void *k_idx, int64_t k_rows, const float *k_scale,
                                     const int32_t *q_vis, int64_t max_vis, float *bm,
-                                    int64_t bm_stride, cudaStream_t st);
+                                    int64_t bm_stride, float *scores, int64_t sc_stride,
+                                    cudaStream_t st);
 cudaError_t launch_score_scan_mma(const void *q_idx, int dtype, const float *w, int nq, int Hi,
                                   const void *k_idx, int64_t k_rows, const float *k_scale,
                                   const int64_t *cu_ctx, const int32_t *q_seq,

@@ -40,6 +40,8 @@ struct MqParams {
   const int32_t *q_vis;  // [nq]
   float *bm;             // [nq, bm_stride]
   int64_t bm_stride;
+  float *scores;         // [nq, sc_stride] per position (optional)
+  int64_t sc_stride;
   int64_t base;          // first key row of the (single) sequence
   int64_t max_vis;       // largest q_vis (positions beyond it are never read)
   int nq, n_tiles, ct;   // key tiles of 128, tiles per chunk
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_multi_kernel(
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
             const int q = g * kMqQ + half * 16 + qq;
+            if (p.scores && valid && q < p.nq) p.scores[(int64_t)q * p.sc_stride + pos] = sc;
             if ((lane & 7) == 0 && valid && q < p.nq)
               p.bm[(int64_t)q * p.bm_stride + (pos >> 3)] = m;
           }
@@ -204,11 +207,13 @@ bool index_multi_supported(int nq, int Hi, int B) {
   return B == 1 && Hi == 8 && nq > 1024 && encode_fn() != nullptr;
 }
 
-// Block maxima of every query over one sequence (all queries in sequence 0, rows from 0).
+// Block maxima of every query over one sequence (all queries in sequence 0, rows from 0), and
+// the score of every visible position when `scores` is not null.
 cudaError_t launch_score_scan_multi(const void *q_idx, int dtype, const float *w, int nq,
                                     const void *k_idx, int64_t k_rows, const float *k_scale,
                                     const int32_t *q_vis, int64_t max_vis, float *bm,
-                                    int64_t bm_stride, cudaStream_t st) {
+                                    int64_t bm_stride, float *scores, int64_t sc_stride,
+                                    cudaStream_t st) {
   if (nq == 0 || max_vis == 0) return cudaSuccess;
   CUtensorMap km, qm;
   if (!make_rows128_map(&km, k_idx, k_rows, 128) ||
@@ -216,6 +221,7 @@ cudaError_t launch_score_scan_multi(const void *q_idx, int dtype, const float *w
     return cudaErrorInvalidValue;
   MqParams p{};
   p.w = w; p.k_scale = k_scale; p.q_vis = q_vis; p.bm = bm; p.bm_stride = bm_stride;
+  p.scores = scores; p.sc_stride = sc_stride;
   p.base = 0; p.max_vis = max_vis; p.nq = nq;
   p.n_tiles = (int)((max_vis + 127) / 128);
   const int grid = sm_count();
