@@ -30,8 +30,7 @@ constexpr int kPfOffPhi = 128 * 1024;          // 64 rows (heads) x 128 B (64 ro
 constexpr int kPfOffPlo = 136 * 1024;
 constexpr int kPfOffRaw = 144 * 1024;          // 2 x (64 x 256 B codes + 64 x 32 B scales)
 constexpr int kPfRawBytes = kPfTS * 288;       // 18 KB
-constexpr int kPfOffLut = kPfOffRaw + 2 * kPfRawBytes;
-constexpr int kPfOffMisc = kPfOffLut + 1024;
+constexpr int kPfOffMisc = kPfOffRaw + 2 * kPfRawBytes;
 constexpr int kPfSmem = kPfOffMisc + 2048 + 1024;
 
 struct PfMisc {
@@ -40,7 +39,9 @@ struct PfMisc {
   int any_rescale;
   int slot_ok[2][kPfTS];
   float factor[64];
+  float mhalf[2][64];  // per-half tile maxima (then the second half's running sums)
 };
+static_assert(sizeof(PfMisc) <= 2048, "misc block");
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return (uint32_t)__half_as_ushort(__float2half_rn(lo)) |
@@ -51,6 +52,21 @@ __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
   __half2 y = *reinterpret_cast<__half2 *>(&b);
   __half2 z = __hmul2(x, y);
   return *reinterpret_cast<uint32_t *>(&z);
+}
+
+// Two E2M1 codes (one byte, channel 2j in the low nibble) -> f16x2 of their values (exact;
+// the low nibble goes to the low half).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(r) : "r"(byte));
+  return r;
+}
+// One E4M3 scale byte -> f16x2 holding it twice (exact: E4M3 values are fp16 normals).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t byte) {
+  uint32_t r;
+  const uint16_t two = (uint16_t)(byte | (byte << 8));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
+  return r;
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -98,7 +114,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t *sm = smem_raw + ((1024 - (raw_u32 & 1023)) & 1023);
   PfMisc &ms = *reinterpret_cast<PfMisc *>(sm + kPfOffMisc);
-  uint32_t *lut = reinterpret_cast<uint32_t *>(sm + kPfOffLut);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = blockIdx.x;
   const int32_t *idx_n = idx + (int64_t)n * topk;
@@ -115,8 +130,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     tmem_alloc(&ms.tmem_base, 512);
     tmem_relinquish();
   }
-  // byte of two E2M1 codes -> f16x2 of their values (exact)
-  lut[tid] = pack_f16x2(e2m1_to_float(tid & 15), e2m1_to_float(tid >> 4));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -135,19 +148,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       const int64_t qrow = (int64_t)n * H + h;
       const int c0 = kc * 64 + u * 8;
       const uint32_t cw = *reinterpret_cast<const uint32_t *>(q_codes + qrow * kCodeBytes + c0 / 2);
-      const float sc = e4m3_to_float(q_sf[qrow * kSfBytes + c0 / 16]);
-      const uint32_t s2 = pack_f16x2(sc, sc);
-      w.x = f16x2_mul(lut[cw & 0xFF], s2);
-      w.y = f16x2_mul(lut[(cw >> 8) & 0xFF], s2);
-      w.z = f16x2_mul(lut[(cw >> 16) & 0xFF], s2);
-      w.w = f16x2_mul(lut[cw >> 24], s2);
+      const uint32_t s2 = e4m3_to_f16x2_dup(q_sf[qrow * kSfBytes + c0 / 16]);
+      w.x = f16x2_mul(e2m1x2_to_f16x2(cw & 0xFF), s2);
+      w.y = f16x2_mul(e2m1x2_to_f16x2((cw >> 8) & 0xFF), s2);
+      w.z = f16x2_mul(e2m1x2_to_f16x2((cw >> 16) & 0xFF), s2);
+      w.w = f16x2_mul(e2m1x2_to_f16x2(cw >> 24), s2);
     }
     *reinterpret_cast<uint4 *>(sm + kPfOffQ + kc * 8192 + h * 128 + ((u ^ (h & 7)) << 4)) = w;
   }
 
-  // per-head softmax state, owned by warps 0/1 (thread = head = TMEM lane of S)
+  // per-head softmax state: warps 0,1 (columns 0..31 of S) and 4,5 (columns 32..63) share each
+  // head (thread = head = TMEM lane of S); both halves keep the same reference maximum and
+  // their own running sums
   float m_ref = -INFINITY, l_run = 0.0f;
   bool ok = true;
+  constexpr uint32_t idesc_qk = idesc_f32acc(0, 0, 128, kPfTS);  // f16 x f16
   for (int t = 0; t < n_tiles; ++t) {
     const int buf = t & 1;
     uint8_t *raw = sm + kPfOffRaw + buf * kPfRawBytes;
@@ -157,79 +172,84 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     if (t + 1 < n_tiles && tid < kPfTS)
       pf_gather(sm + kPfOffRaw + (buf ^ 1) * kPfRawBytes, ms, buf ^ 1, tid, idx_n,
                 (t + 1) * kPfTS, topk, base, codes, sf);
-    for (int v = tid; v < kPfTS * 64; v += kPfThreads) {
-      const int j = v >> 6, rest = v & 63, kc = rest >> 3, u = rest & 7;
-      const int c0 = kc * 64 + u * 8;
-      const uint32_t cw = *reinterpret_cast<const uint32_t *>(raw + j * 256 + c0 / 2);
-      const float sc = e4m3_to_float(raw[kPfTS * 256 + j * 32 + c0 / 16]);
-      const uint32_t s2 = pack_f16x2(sc, sc);
-      uint4 w;
-      w.x = f16x2_mul(lut[cw & 0xFF], s2);
-      w.y = f16x2_mul(lut[(cw >> 8) & 0xFF], s2);
-      w.z = f16x2_mul(lut[(cw >> 16) & 0xFF], s2);
-      w.w = f16x2_mul(lut[cw >> 24], s2);
-      *reinterpret_cast<uint4 *>(sm + kPfOffK + kc * 8192 + j * 128 + ((u ^ (j & 7)) << 4)) = w;
-    }
     if (tid == 0) ms.any_rescale = 0;
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {  // S = Qhat Khat^T
-      constexpr uint32_t idesc = idesc_f32acc(0, 0, 128, kPfTS);  // f16 x f16
-      const uint32_t qa = smem_u32(sm + kPfOffQ), ka = smem_u32(sm + kPfOffK);
-      for (int kc = 0; kc < 8; ++kc)
+    // dequantise chunks 0..3, start S on them, dequantise chunks 4..7, finish S
+    for (int half = 0; half < 2; ++half) {
+      for (int v = tid; v < kPfTS * 32; v += kPfThreads) {
+        const int j = v >> 5, rest = v & 31, kc = half * 4 + (rest >> 3), u = rest & 7;
+        const int c0 = kc * 64 + u * 8;
+        const uint32_t cw = *reinterpret_cast<const uint32_t *>(raw + j * 256 + c0 / 2);
+        const uint32_t s2 = e4m3_to_f16x2_dup(raw[kPfTS * 256 + j * 32 + c0 / 16]);
+        uint4 w;
+        w.x = f16x2_mul(e2m1x2_to_f16x2(cw & 0xFF), s2);
+        w.y = f16x2_mul(e2m1x2_to_f16x2((cw >> 8) & 0xFF), s2);
+        w.z = f16x2_mul(e2m1x2_to_f16x2((cw >> 16) & 0xFF), s2);
+        w.w = f16x2_mul(e2m1x2_to_f16x2(cw >> 24), s2);
+        *reinterpret_cast<uint4 *>(sm + kPfOffK + kc * 8192 + j * 128 + ((u ^ (j & 7)) << 4)) = w;
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (tid == 0) {  // S = Qhat Khat^T over this half's chunks
+        const uint32_t qa = smem_u32(sm + kPfOffQ), ka = smem_u32(sm + kPfOffK);
+        for (int kc = half * 4; kc < half * 4 + 4; ++kc)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_f16(tS, desc_k128_sw128(qa + kc * 8192 + 32 * ks),
-                  desc_k128_sw128(ka + kc * 8192 + 32 * ks), idesc, (kc | ks) != 0);
-      mma_commit(&ms.bar_s);
+          for (int ks = 0; ks < 4; ++ks)
+            mma_f16(tS, desc_k128_sw128(qa + kc * 8192 + 32 * ks),
+                    desc_k128_sw128(ka + kc * 8192 + 32 * ks), idesc_qk, (kc | ks) != 0);
+        if (half == 1) mma_commit(&ms.bar_s);
+      }
     }
-    if (warp < 2) {  // softmax rows
+    if ((warp & 3) < 2) {  // softmax rows: warps 0,1 columns 0..31, warps 4,5 columns 32..63
       ok = __all_sync(0xffffffffu, mbar_wait(&ms.bar_s, t & 1)) && ok;
       tc_fence_after();
-      const int h = warp * 32 + lane;
-      float s[kPfTS];
-      const uint32_t la = tS + ((uint32_t)(warp * 32) << 16);
+      const int h = (warp & 3) * 32 + lane;
+      const int sh = warp >> 2, j0 = sh * 32;
+      float s[32];
+      const uint32_t la = tS + j0 + ((uint32_t)((warp & 3) * 32) << 16);
       {
-        uint32_t r[kPfTS / 16][16];
-#pragma unroll
-        for (int c = 0; c < kPfTS / 16; ++c) tmem_ld16(la + 16 * c, r[c]);
+        uint32_t r[2][16];
+        tmem_ld16(la, r[0]);
+        tmem_ld16(la + 16, r[1]);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < kPfTS / 16; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int i = 0; i < 16; ++i) s[16 * c + i] = __uint_as_float(r[c][i]) * scale_log2e;
       }
       float mt = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < kPfTS; ++j)
-        if (ms.slot_ok[buf][j]) mt = fmaxf(mt, s[j]);
+      for (int j = 0; j < 32; ++j)
+        if (ms.slot_ok[buf][j0 + j]) mt = fmaxf(mt, s[j]);
+      ms.mhalf[sh][h] = mt;
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps
+      mt = fmaxf(ms.mhalf[0][h], ms.mhalf[1][h]);
       float factor = 1.0f;
       if (mt > m_ref + kPfRescale) {  // (also true the first time: m_ref = -inf)
         if (m_ref != -INFINITY) {
           factor = exp2f(m_ref - mt);
-          atomicOr(&ms.any_rescale, 1);
+          if (sh == 0) atomicOr(&ms.any_rescale, 1);
         }
         l_run *= factor;
         m_ref = mt;
       }
-      ms.factor[h] = factor;
+      if (sh == 0) ms.factor[h] = factor;
       // numerators as fp16 hi + lo parts (p = hi + lo to ~2^-22): one fp16 operand alone
       // (2^-12) is too coarse when large rows of opposite sign nearly cancel
-      uint32_t hi[kPfTS / 2], lo[kPfTS / 2];
+      uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int j = 0; j < kPfTS; j += 2) {
-        const float p0 = ms.slot_ok[buf][j] ? exp2f(s[j] - m_ref) : 0.0f;
-        const float p1 = ms.slot_ok[buf][j + 1] ? exp2f(s[j + 1] - m_ref) : 0.0f;
+      for (int j = 0; j < 32; j += 2) {
+        const float p0 = ms.slot_ok[buf][j0 + j] ? exp2f(s[j] - m_ref) : 0.0f;
+        const float p1 = ms.slot_ok[buf][j0 + j + 1] ? exp2f(s[j + 1] - m_ref) : 0.0f;
         l_run += p0 + p1;
         const __half h0 = __float2half_rn(p0), h1 = __float2half_rn(p1);
         hi[j / 2] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
         lo[j / 2] = pack_f16x2(p0 - __half2float(h0), p1 - __half2float(h1));
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int off = h * 128 + ((u ^ (h & 7)) << 4);
+      for (int u = 0; u < 4; ++u) {
+        const int off = h * 128 + (((4 * sh + u) ^ (h & 7)) << 4);
         *reinterpret_cast<uint4 *>(sm + kPfOffPhi + off) =
             make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
         *reinterpret_cast<uint4 *>(sm + kPfOffPlo + off) =
@@ -274,12 +294,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   }
   // ---- epilogue: thread = channel lane; column 64*qb + h of O^T is channel 128*qb + lane'
   ok = mbar_wait(&ms.bar_o, (n_tiles - 1) & 1) && ok;
-  if (warp < 2) {  // publish the final per-head state through shared memory
-    const int h = warp * 32 + lane;
-    ms.factor[h] = (l_run > 0.0f && ok) ? 1.0f / l_run : 0.0f;
-    if (h < H && lse)
-      lse[(int64_t)n * H + h] = (l_run > 0.0f && ok) ? (m_ref + log2f(l_run)) * 0.69314718055994531f
-                                                     : -INFINITY;
+  if ((warp & 3) < 2) {  // publish the final per-head state through shared memory
+    const int h = (warp & 3) * 32 + lane;
+    if (warp >= 4) ms.mhalf[1][h] = l_run;  // the second half's running sum
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (warp < 4) {
+      const float l = l_run + ms.mhalf[1][h];
+      ms.factor[h] = (l > 0.0f && ok) ? 1.0f / l : 0.0f;
+      if (h < H && lse)
+        lse[(int64_t)n * H + h] = (l > 0.0f && ok) ? (m_ref + log2f(l)) * 0.69314718055994531f
+                                                   : -INFINITY;
+    }
   }
   tc_fence_before();
   __syncthreads();
