@@ -21,7 +21,9 @@
 namespace csa2 {
 
 constexpr int kPfTS = 64;
-constexpr int kPfThreads = 256;
+constexpr int kPfWorkers = 256;                // warps 0..7: gather, dequantise, softmax, epilogue
+constexpr int kPfMmaWarp = 8;                  // warp 8: TMEM allocation and every MMA issue
+constexpr int kPfThreads = kPfWorkers + 32;
 constexpr float kPfRescale = 10.0f;  // log2 headroom before the reference maximum moves
 
 constexpr int kPfOffQ = 0;                     // 8 chunks x (64 rows x 128 B) = 64 KB (+8 KB overrun)
@@ -34,9 +36,9 @@ constexpr int kPfOffMisc = kPfOffRaw + 2 * kPfRawBytes;
 constexpr int kPfSmem = kPfOffMisc + 2048 + 1024;
 
 struct PfMisc {
-  uint64_t bar_g[2], bar_s, bar_o;
+  uint64_t bar_g[2], bar_dq[4], bar_pv[4], bar_s, bar_p;
   uint32_t tmem_base;
-  int any_rescale;
+  int any_rescale[2];
   int slot_ok[2][kPfTS];
   float factor[64];
   float mhalf[2][64];  // per-half tile maxima (then the second half's running sums)
@@ -122,11 +124,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   if (tid == 0) {
     mbar_init(&ms.bar_g[0], kPfTS);
     mbar_init(&ms.bar_g[1], kPfTS);
+    for (int c = 0; c < 4; ++c) {
+      mbar_init(&ms.bar_dq[c], kPfWorkers);
+      mbar_init(&ms.bar_pv[c], 1);
+    }
     mbar_init(&ms.bar_s, 1);
-    mbar_init(&ms.bar_o, 1);
+    mbar_init(&ms.bar_p, kPfWorkers);
+    ms.any_rescale[0] = 0;
+    ms.any_rescale[1] = 0;
     fence_barrier_init();
   }
-  if (warp == 0) {
+  if (warp == kPfMmaWarp) {
     tmem_alloc(&ms.tmem_base, 512);
     tmem_relinquish();
   }
@@ -137,192 +145,204 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   const uint32_t tS = tmem + 256;
   pdl_wait();
   pdl_trigger();
-  const int64_t base = cu_ctx[q_seq[n]];
-
-  if (tid < kPfTS) pf_gather(sm + kPfOffRaw, ms, 0, tid, idx_n, 0, topk, base, codes, sf);
-  // the FP4 query, exactly dequantised into the swizzled Q chunks
-  for (int v = tid; v < 64 * 64; v += kPfThreads) {
-    const int h = v >> 6, rest = v & 63, kc = rest >> 3, u = rest & 7;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (h < H) {
-      const int64_t qrow = (int64_t)n * H + h;
-      const int c0 = kc * 64 + u * 8;
-      const uint32_t cw = *reinterpret_cast<const uint32_t *>(q_codes + qrow * kCodeBytes + c0 / 2);
-      const uint32_t s2 = e4m3_to_f16x2_dup(q_sf[qrow * kSfBytes + c0 / 16]);
-      w.x = f16x2_mul(e2m1x2_to_f16x2(cw & 0xFF), s2);
-      w.y = f16x2_mul(e2m1x2_to_f16x2((cw >> 8) & 0xFF), s2);
-      w.z = f16x2_mul(e2m1x2_to_f16x2((cw >> 16) & 0xFF), s2);
-      w.w = f16x2_mul(e2m1x2_to_f16x2(cw >> 24), s2);
-    }
-    *reinterpret_cast<uint4 *>(sm + kPfOffQ + kc * 8192 + h * 128 + ((u ^ (h & 7)) << 4)) = w;
-  }
-
-  // per-head softmax state: warps 0,1 (columns 0..31 of S) and 4,5 (columns 32..63) share each
-  // head (thread = head = TMEM lane of S); both halves keep the same reference maximum and
-  // their own running sums
-  float m_ref = -INFINITY, l_run = 0.0f;
   bool ok = true;
-  constexpr uint32_t idesc_qk = idesc_f32acc(0, 0, 128, kPfTS);  // f16 x f16
-  for (int t = 0; t < n_tiles; ++t) {
-    const int buf = t & 1;
-    uint8_t *raw = sm + kPfOffRaw + buf * kPfRawBytes;
-    ok = mbar_wait(&ms.bar_g[buf], (t >> 1) & 1) && ok;
-    if (t > 0) ok = mbar_wait(&ms.bar_o, (t - 1) & 1) && ok;  // PV(t-1) done: K, P free
-    // prefetch the next tile's rows into the other raw buffer (consumed two steps ago)
-    if (t + 1 < n_tiles && tid < kPfTS)
-      pf_gather(sm + kPfOffRaw + (buf ^ 1) * kPfRawBytes, ms, buf ^ 1, tid, idx_n,
-                (t + 1) * kPfTS, topk, base, codes, sf);
-    if (tid == 0) ms.any_rescale = 0;
-    // dequantise chunks 0..3, start S on them, dequantise chunks 4..7, finish S
-    for (int half = 0; half < 2; ++half) {
-      for (int v = tid; v < kPfTS * 32; v += kPfThreads) {
-        const int j = v >> 5, rest = v & 31, kc = half * 4 + (rest >> 3), u = rest & 7;
+
+  if (warp == kPfMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_f32acc(0, 0, 128, kPfTS);              // f16 x f16
+      constexpr uint32_t idesc_pv = idesc_f32acc(0, 0, 128, 64) | (1u << 15);    // A MN-major
+      const uint32_t qa = smem_u32(sm + kPfOffQ), ka = smem_u32(sm + kPfOffK);
+      const uint32_t ph = smem_u32(sm + kPfOffPhi), pl = smem_u32(sm + kPfOffPlo);
+      for (int t = 0; t < n_tiles; ++t) {
+        // S = Qhat Khat^T, two chunks at a time as the workers finish them
+        for (int cp = 0; cp < 4; ++cp) {
+          ok = mbar_wait(&ms.bar_dq[cp], t & 1) && ok;
+          tc_fence_after();
+          for (int kc = 2 * cp; kc < 2 * cp + 2; ++kc)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_f16(tS, desc_k128_sw128(qa + kc * 8192 + 32 * ks),
+                      desc_k128_sw128(ka + kc * 8192 + 32 * ks), idesc_qk, (kc | ks) != 0);
+        }
+        mma_commit(&ms.bar_s);
+        // O^T += Vhat^T (P_hi + P_lo)^T, one commit per 128-channel block so the next tile's
+        // dequantisation can reuse chunks 2qb, 2qb+1 as soon as block qb is done
+        ok = mbar_wait(&ms.bar_p, t & 1) && ok;
+        tc_fence_after();
+        for (int qb = 0; qb < 4; ++qb) {
+#pragma unroll
+          for (int ks = 0; ks < kPfTS / 16; ++ks) {
+            const uint64_t ad = desc_mn_sw128_atoms(ka + (2 * qb) * 8192 + ks * 16 * 128, 8192);
+            mma_f16(tmem + qb * 64, ad, desc_k128_sw128(ph + 32 * ks), idesc_pv,
+                    (t > 0 || ks > 0) ? 1u : 0u);
+            mma_f16(tmem + qb * 64, ad, desc_k128_sw128(pl + 32 * ks), idesc_pv, 1u);
+          }
+          mma_commit(&ms.bar_pv[qb]);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ workers (warps 0..7)
+    const int64_t base = cu_ctx[q_seq[n]];
+    if (tid < kPfTS) pf_gather(sm + kPfOffRaw, ms, 0, tid, idx_n, 0, topk, base, codes, sf);
+    // the FP4 query, exactly dequantised into the swizzled Q chunks
+    for (int v = tid; v < 64 * 64; v += kPfWorkers) {
+      const int h = v >> 6, rest = v & 63, kc = rest >> 3, u = rest & 7;
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (h < H) {
+        const int64_t qrow = (int64_t)n * H + h;
         const int c0 = kc * 64 + u * 8;
-        const uint32_t cw = *reinterpret_cast<const uint32_t *>(raw + j * 256 + c0 / 2);
-        const uint32_t s2 = e4m3_to_f16x2_dup(raw[kPfTS * 256 + j * 32 + c0 / 16]);
-        uint4 w;
+        const uint32_t cw =
+            *reinterpret_cast<const uint32_t *>(q_codes + qrow * kCodeBytes + c0 / 2);
+        const uint32_t s2 = e4m3_to_f16x2_dup(q_sf[qrow * kSfBytes + c0 / 16]);
         w.x = f16x2_mul(e2m1x2_to_f16x2(cw & 0xFF), s2);
         w.y = f16x2_mul(e2m1x2_to_f16x2((cw >> 8) & 0xFF), s2);
         w.z = f16x2_mul(e2m1x2_to_f16x2((cw >> 16) & 0xFF), s2);
         w.w = f16x2_mul(e2m1x2_to_f16x2(cw >> 24), s2);
-        *reinterpret_cast<uint4 *>(sm + kPfOffK + kc * 8192 + j * 128 + ((u ^ (j & 7)) << 4)) = w;
+      }
+      *reinterpret_cast<uint4 *>(sm + kPfOffQ + kc * 8192 + h * 128 + ((u ^ (h & 7)) << 4)) = w;
+    }
+    // per-head softmax state: warps 0,1 (columns 0..31 of S) and 4,5 (columns 32..63) share
+    // each head (thread = head = TMEM lane of S); both halves keep the same reference maximum
+    // and their own running sums
+    float m_ref = -INFINITY, l_run = 0.0f;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int buf = t & 1;
+      uint8_t *raw = sm + kPfOffRaw + buf * kPfRawBytes;
+      ok = mbar_wait(&ms.bar_g[buf], (t >> 1) & 1) && ok;
+      // prefetch the next tile's rows into the other raw buffer (dequantised last tile)
+      if (t + 1 < n_tiles && tid < kPfTS)
+        pf_gather(sm + kPfOffRaw + (buf ^ 1) * kPfRawBytes, ms, buf ^ 1, tid, idx_n,
+                  (t + 1) * kPfTS, topk, base, codes, sf);
+      // dequantise two chunks at a time, each pair once PV(t-1) no longer reads it
+      for (int cp = 0; cp < 4; ++cp) {
+        if (t > 0) ok = mbar_wait(&ms.bar_pv[cp], (t - 1) & 1) && ok;
+#pragma unroll 4
+        for (int v = tid; v < kPfTS * 16; v += kPfWorkers) {
+          const int j = v >> 4, rest = v & 15, kc = 2 * cp + (rest >> 3), u = rest & 7;
+          const int c0 = kc * 64 + u * 8;
+          const uint32_t cw = *reinterpret_cast<const uint32_t *>(raw + j * 256 + c0 / 2);
+          const uint32_t s2 = e4m3_to_f16x2_dup(raw[kPfTS * 256 + j * 32 + c0 / 16]);
+          uint4 w;
+          w.x = f16x2_mul(e2m1x2_to_f16x2(cw & 0xFF), s2);
+          w.y = f16x2_mul(e2m1x2_to_f16x2((cw >> 8) & 0xFF), s2);
+          w.z = f16x2_mul(e2m1x2_to_f16x2((cw >> 16) & 0xFF), s2);
+          w.w = f16x2_mul(e2m1x2_to_f16x2(cw >> 24), s2);
+          *reinterpret_cast<uint4 *>(sm + kPfOffK + kc * 8192 + j * 128 + ((u ^ (j & 7)) << 4)) =
+              w;
+        }
+        fence_async_smem();
+        mbar_arrive(&ms.bar_dq[cp]);
+      }
+      if ((warp & 3) < 2) {  // softmax rows: warps 0,1 columns 0..31, warps 4,5 columns 32..63
+        ok = __all_sync(0xffffffffu, mbar_wait(&ms.bar_s, t & 1)) && ok;
+        tc_fence_after();
+        const int h = (warp & 3) * 32 + lane;
+        const int sh = warp >> 2, j0 = sh * 32;
+        float s[32];
+        const uint32_t la = tS + j0 + ((uint32_t)((warp & 3) * 32) << 16);
+        {
+          uint32_t r[2][16];
+          tmem_ld16(la, r[0]);
+          tmem_ld16(la + 16, r[1]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) s[16 * c + i] = __uint_as_float(r[c][i]) * scale_log2e;
+        }
+        float mt = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (ms.slot_ok[buf][j0 + j]) mt = fmaxf(mt, s[j]);
+        ms.mhalf[sh][h] = mt;
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps
+        mt = fmaxf(ms.mhalf[0][h], ms.mhalf[1][h]);
+        float factor = 1.0f;
+        if (mt > m_ref + kPfRescale) {  // (also true the first time: m_ref = -inf)
+          if (m_ref != -INFINITY) {
+            factor = exp2f(m_ref - mt);
+            if (sh == 0) atomicOr(&ms.any_rescale[buf], 1);
+          }
+          l_run *= factor;
+          m_ref = mt;
+        }
+        if (sh == 0) ms.factor[h] = factor;
+        // numerators as fp16 hi + lo parts (p = hi + lo to ~2^-22): one fp16 operand alone
+        // (2^-12) is too coarse when large rows of opposite sign nearly cancel.  P(t-1) is no
+        // longer read: PV(t-1) is complete (every bar_pv of t-1 was waited above).
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = ms.slot_ok[buf][j0 + j] ? exp2f(s[j] - m_ref) : 0.0f;
+          const float p1 = ms.slot_ok[buf][j0 + j + 1] ? exp2f(s[j + 1] - m_ref) : 0.0f;
+          l_run += p0 + p1;
+          const __half b0 = __float2half_rn(p0), b1 = __float2half_rn(p1);
+          hi[j / 2] = (uint32_t)__half_as_ushort(b0) | ((uint32_t)__half_as_ushort(b1) << 16);
+          lo[j / 2] = pack_f16x2(p0 - __half2float(b0), p1 - __half2float(b1));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int off = h * 128 + (((4 * sh + u) ^ (h & 7)) << 4);
+          *reinterpret_cast<uint4 *>(sm + kPfOffPhi + off) =
+              make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
+          *reinterpret_cast<uint4 *>(sm + kPfOffPlo + off) =
+              make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+        }
       }
       fence_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (tid == 0) {  // S = Qhat Khat^T over this half's chunks
-        const uint32_t qa = smem_u32(sm + kPfOffQ), ka = smem_u32(sm + kPfOffK);
-        for (int kc = half * 4; kc < half * 4 + 4; ++kc)
+      asm volatile("bar.sync 2, 256;" ::: "memory");  // the workers: P, factors, flag visible
+      if (tid == 0) ms.any_rescale[buf ^ 1] = 0;      // its readers (tile t-1) are all past
+      if (ms.any_rescale[buf] && warp < 4) {  // O^T[:, h] *= factor[h]: thread = channel lane
+        tc_fence_after();
+        const uint32_t la = tmem + ((uint32_t)(warp * 32) << 16);
+        for (int c = 0; c < 256; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(la + c, r);
+          tmem_ld_wait();
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_f16(tS, desc_k128_sw128(qa + kc * 8192 + 32 * ks),
-                    desc_k128_sw128(ka + kc * 8192 + 32 * ks), idesc_qk, (kc | ks) != 0);
-        if (half == 1) mma_commit(&ms.bar_s);
+          for (int i = 0; i < 16; ++i)
+            r[i] = __float_as_uint(__uint_as_float(r[i]) * ms.factor[(c + i) & 63]);
+          tmem_st16(la + c, r);
+        }
+        tmem_st_wait();
       }
+      tc_fence_before();
+      asm volatile("bar.sync 2, 256;" ::: "memory");  // factors read before they change
+      mbar_arrive(&ms.bar_p);
     }
-    if ((warp & 3) < 2) {  // softmax rows: warps 0,1 columns 0..31, warps 4,5 columns 32..63
-      ok = __all_sync(0xffffffffu, mbar_wait(&ms.bar_s, t & 1)) && ok;
-      tc_fence_after();
+    // ---- epilogue: thread = channel lane; column 64*qb + h of O^T is channel 128*qb + lane'
+    ok = mbar_wait(&ms.bar_pv[3], (n_tiles - 1) & 1) && ok;
+    tc_fence_after();
+    if ((warp & 3) < 2) {  // publish the final per-head state through shared memory
       const int h = (warp & 3) * 32 + lane;
-      const int sh = warp >> 2, j0 = sh * 32;
-      float s[32];
-      const uint32_t la = tS + j0 + ((uint32_t)((warp & 3) * 32) << 16);
-      {
-        uint32_t r[2][16];
-        tmem_ld16(la, r[0]);
-        tmem_ld16(la + 16, r[1]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int i = 0; i < 16; ++i) s[16 * c + i] = __uint_as_float(r[c][i]) * scale_log2e;
-      }
-      float mt = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (ms.slot_ok[buf][j0 + j]) mt = fmaxf(mt, s[j]);
-      ms.mhalf[sh][h] = mt;
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps
-      mt = fmaxf(ms.mhalf[0][h], ms.mhalf[1][h]);
-      float factor = 1.0f;
-      if (mt > m_ref + kPfRescale) {  // (also true the first time: m_ref = -inf)
-        if (m_ref != -INFINITY) {
-          factor = exp2f(m_ref - mt);
-          if (sh == 0) atomicOr(&ms.any_rescale, 1);
-        }
-        l_run *= factor;
-        m_ref = mt;
-      }
-      if (sh == 0) ms.factor[h] = factor;
-      // numerators as fp16 hi + lo parts (p = hi + lo to ~2^-22): one fp16 operand alone
-      // (2^-12) is too coarse when large rows of opposite sign nearly cancel
-      uint32_t hi[16], lo[16];
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const float p0 = ms.slot_ok[buf][j0 + j] ? exp2f(s[j] - m_ref) : 0.0f;
-        const float p1 = ms.slot_ok[buf][j0 + j + 1] ? exp2f(s[j + 1] - m_ref) : 0.0f;
-        l_run += p0 + p1;
-        const __half h0 = __float2half_rn(p0), h1 = __float2half_rn(p1);
-        hi[j / 2] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-        lo[j / 2] = pack_f16x2(p0 - __half2float(h0), p1 - __half2float(h1));
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int off = h * 128 + (((4 * sh + u) ^ (h & 7)) << 4);
-        *reinterpret_cast<uint4 *>(sm + kPfOffPhi + off) =
-            make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
-        *reinterpret_cast<uint4 *>(sm + kPfOffPlo + off) =
-            make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+      if (warp >= 4) ms.mhalf[1][h] = l_run;  // the second half's running sum
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (warp < 4) {
+        const float l = l_run + ms.mhalf[1][h];
+        ms.factor[h] = (l > 0.0f && ok) ? 1.0f / l : 0.0f;
+        if (h < H && lse)
+          lse[(int64_t)n * H + h] = (l > 0.0f && ok) ? (m_ref + log2f(l)) * 0.69314718055994531f
+                                                     : -INFINITY;
       }
     }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (ms.any_rescale && warp < 4) {  // O^T[:, h] *= factor[h]: thread = channel lane
-      const uint32_t la = tmem + ((uint32_t)(warp * 32) << 16);
-      for (int c = 0; c < 256; c += 16) {
-        uint32_t r[16];
-        tmem_ld16(la + c, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          r[i] = __float_as_uint(__uint_as_float(r[i]) * ms.factor[(c + i) & 63]);
-        tmem_st16(la + c, r);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-    }
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {  // O^T += Vhat^T (P_hi + P_lo)^T
-      constexpr uint32_t idesc_pv = idesc_f32acc(0, 0, 128, 64) | (1u << 15);  // f16, A MN-major
-      const uint32_t ka = smem_u32(sm + kPfOffK);
-      const uint32_t ph = smem_u32(sm + kPfOffPhi), pl = smem_u32(sm + kPfOffPlo);
-      for (int qb = 0; qb < 4; ++qb) {
-#pragma unroll
-        for (int ks = 0; ks < kPfTS / 16; ++ks) {
-          const uint64_t ad = desc_mn_sw128_atoms(ka + (2 * qb) * 8192 + ks * 16 * 128, 8192);
-          mma_f16(tmem + qb * 64, ad, desc_k128_sw128(ph + 32 * ks), idesc_pv,
-                  (t > 0 || ks > 0) ? 1u : 0u);
-          mma_f16(tmem + qb * 64, ad, desc_k128_sw128(pl + 32 * ks), idesc_pv, 1u);
-        }
-      }
-      mma_commit(&ms.bar_o);
-    }
-  }
-  // ---- epilogue: thread = channel lane; column 64*qb + h of O^T is channel 128*qb + lane'
-  ok = mbar_wait(&ms.bar_o, (n_tiles - 1) & 1) && ok;
-  if ((warp & 3) < 2) {  // publish the final per-head state through shared memory
-    const int h = (warp & 3) * 32 + lane;
-    if (warp >= 4) ms.mhalf[1][h] = l_run;  // the second half's running sum
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 2, 256;" ::: "memory");
     if (warp < 4) {
-      const float l = l_run + ms.mhalf[1][h];
-      ms.factor[h] = (l > 0.0f && ok) ? 1.0f / l : 0.0f;
-      if (h < H && lse)
-        lse[(int64_t)n * H + h] = (l > 0.0f && ok) ? (m_ref + log2f(l)) * 0.69314718055994531f
-                                                   : -INFINITY;
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp < 4) {
-    const uint32_t la = tmem + ((uint32_t)(warp * 32) << 16);
-    const int cl = warp * 32 + lane;  // channel within a 128-channel block
-    for (int qb = 0; qb < 4; ++qb) {
-      for (int h0 = 0; h0 < 64; h0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(la + qb * 64 + h0, r);
-        tmem_ld_wait();
+      const uint32_t la = tmem + ((uint32_t)(warp * 32) << 16);
+      const int cl = warp * 32 + lane;  // channel within a 128-channel block
+      for (int qb = 0; qb < 4; ++qb) {
+        for (int h0 = 0; h0 < 64; h0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(la + qb * 64 + h0, r);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int h = h0 + i;
-          if (h < H)
-            out[((int64_t)n * H + h) * kD + qb * 128 + cl] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * ms.factor[h]));
+          for (int i = 0; i < 16; ++i) {
+            const int h = h0 + i;
+            if (h < H)
+              out[((int64_t)n * H + h) * kD + qb * 128 + cl] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * ms.factor[h]));
+          }
         }
       }
     }
@@ -330,7 +350,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 512);
+  if (warp == kPfMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 bool attn_prefill_supported(int H) { return H <= 64 && encode_fn() != nullptr; }
