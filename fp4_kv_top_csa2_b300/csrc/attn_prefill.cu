@@ -83,11 +83,9 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void pf_gather(uint8_t *raw, PfMisc &ms, int buf, int tid,
-                                          const int32_t *idx_n, int slot0, int topk,
+// Row r (sequence-local, -1 = empty slot) of one tile slot into the raw buffer.
+__device__ __forceinline__ void pf_gather(uint8_t *raw, PfMisc &ms, int buf, int tid, int r,
                                           int64_t base, const uint8_t *codes, const uint8_t *sf) {
-  const int slot = slot0 + tid;
-  const int r = slot < topk ? idx_n[slot] : -1;
   ms.slot_ok[buf][tid] = r >= 0;
   uint8_t *c = raw + tid * 256;
   uint8_t *s = raw + kPfTS * 256 + tid * 32;
@@ -185,7 +183,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   } else {
     // ------------------------------------------------------------------ workers (warps 0..7)
     const int64_t base = cu_ctx[q_seq[n]];
-    if (tid < kPfTS) pf_gather(sm + kPfOffRaw, ms, 0, tid, idx_n, 0, topk, base, codes, sf);
+    // slot tid of each tile is gathered by thread tid (< 64); its index is loaded one tile ahead
+    int r_next = -1;
+    if (tid < kPfTS) {
+      pf_gather(sm + kPfOffRaw, ms, 0, tid, tid < topk ? idx_n[tid] : -1, base, codes, sf);
+      r_next = kPfTS + tid < topk ? idx_n[kPfTS + tid] : -1;
+    }
     // the FP4 query, exactly dequantised into the swizzled Q chunks
     for (int v = tid; v < 64 * 64; v += kPfWorkers) {
       const int h = v >> 6, rest = v & 63, kc = rest >> 3, u = rest & 7;
@@ -211,10 +214,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       const int buf = t & 1;
       uint8_t *raw = sm + kPfOffRaw + buf * kPfRawBytes;
       ok = mbar_wait(&ms.bar_g[buf], (t >> 1) & 1) && ok;
-      // prefetch the next tile's rows into the other raw buffer (dequantised last tile)
-      if (t + 1 < n_tiles && tid < kPfTS)
-        pf_gather(sm + kPfOffRaw + (buf ^ 1) * kPfRawBytes, ms, buf ^ 1, tid, idx_n,
-                  (t + 1) * kPfTS, topk, base, codes, sf);
+      // prefetch the next tile's rows into the other raw buffer (dequantised last tile), and
+      // load the index of the tile after it
+      if (t + 1 < n_tiles && tid < kPfTS) {
+        pf_gather(sm + kPfOffRaw + (buf ^ 1) * kPfRawBytes, ms, buf ^ 1, tid, r_next, base, codes,
+                  sf);
+        const int slot = (t + 2) * kPfTS + tid;
+        r_next = slot < topk ? idx_n[slot] : -1;
+      }
       // dequantise two chunks at a time, each pair once PV(t-1) no longer reads it
       for (int cp = 0; cp < 4; ++cp) {
         if (t > 0) ok = mbar_wait(&ms.bar_pv[cp], (t - 1) & 1) && ok;
