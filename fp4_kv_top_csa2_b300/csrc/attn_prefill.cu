@@ -36,10 +36,10 @@ constexpr int kPfOffMisc = kPfOffRaw + 2 * kPfRawBytes;
 constexpr int kPfSmem = kPfOffMisc + 2048 + 1024;
 
 struct PfMisc {
-  uint64_t bar_g[2], bar_dq[4], bar_pv[4], bar_s, bar_p;
+  uint64_t bar_dq[4], bar_pv[4], bar_s, bar_p;
   uint32_t tmem_base;
   int any_rescale[2];
-  int slot_ok[2][kPfTS];
+  int rows[2][kPfTS];  // the row of each slot of the tiles held in the two raw buffers
   float factor[64];
   float mhalf[2][64];  // per-half tile maxima (then the second half's running sums)
 };
@@ -83,24 +83,28 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Row r (sequence-local, -1 = empty slot) of one tile slot into the raw buffer.
-__device__ __forceinline__ void pf_gather(uint8_t *raw, PfMisc &ms, int buf, int tid, int r,
-                                          int64_t base, const uint8_t *codes, const uint8_t *sf) {
-  ms.slot_ok[buf][tid] = r >= 0;
-  uint8_t *c = raw + tid * 256;
-  uint8_t *s = raw + kPfTS * 256 + tid * 32;
-  if (r >= 0) {
-    const int64_t row = base + r;
-    sm100::mbar_arrive_expect_tx(&ms.bar_g[buf], 288);
-    bulk_g2s(c, codes + row * kCodeBytes, 256, &ms.bar_g[buf]);
-    bulk_g2s(s, sf + row * kSfBytes, 32, &ms.bar_g[buf]);
-  } else {
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int i = 0; i < 16; ++i) reinterpret_cast<uint4 *>(c)[i] = z;
-    reinterpret_cast<uint4 *>(s)[0] = z;
-    reinterpret_cast<uint4 *>(s)[1] = z;
-    sm100::mbar_arrive(&ms.bar_g[buf]);
+// The 64 rows of one tile (sequence-local row numbers in rows[], -1 = empty slot) into a raw
+// buffer: 64 x (256 B codes + 32 B scales) as 1,152 16-byte cp.async copies spread over the
+// 256 worker threads (empty slots are zero-filled).  Completion: cp.async.wait_all by every
+// worker, then a workers' barrier.
+__device__ __forceinline__ void pf_gather_tile(uint8_t *raw, const int *rows, int tid, int64_t base,
+                                               const uint8_t *codes, const uint8_t *sf) {
+  for (int i = tid; i < kPfTS * 18; i += kPfWorkers) {
+    const int j = i / 18, part = i - j * 18;
+    const int r = rows[j];
+    uint8_t *dst = part < 16 ? raw + j * 256 + part * 16 : raw + kPfTS * 256 + j * 32 + (part - 16) * 16;
+    if (r >= 0) {
+      const int64_t row = base + r;
+      const uint8_t *src = part < 16 ? codes + row * kCodeBytes + part * 16
+                                     : sf + row * kSfBytes + (part - 16) * 16;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm100::smem_u32(dst)),
+                   "l"(reinterpret_cast<uint64_t>(src))
+                   : "memory");
+    } else {
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
@@ -120,8 +124,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   const int n_tiles = (topk + kPfTS - 1) / kPfTS;
 
   if (tid == 0) {
-    mbar_init(&ms.bar_g[0], kPfTS);
-    mbar_init(&ms.bar_g[1], kPfTS);
     for (int c = 0; c < 4; ++c) {
       mbar_init(&ms.bar_dq[c], kPfWorkers);
       mbar_init(&ms.bar_pv[c], 1);
@@ -183,12 +185,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   } else {
     // ------------------------------------------------------------------ workers (warps 0..7)
     const int64_t base = cu_ctx[q_seq[n]];
-    // slot tid of each tile is gathered by thread tid (< 64); its index is loaded one tile ahead
+    // the row indices of tile t sit in ms.rows[t & 1]; thread tid < 64 loads slot tid of the
+    // tile two ahead into r_next
     int r_next = -1;
     if (tid < kPfTS) {
-      pf_gather(sm + kPfOffRaw, ms, 0, tid, tid < topk ? idx_n[tid] : -1, base, codes, sf);
-      r_next = kPfTS + tid < topk ? idx_n[kPfTS + tid] : -1;
+      ms.rows[0][tid] = tid < topk ? idx_n[tid] : -1;
+      ms.rows[1][tid] = kPfTS + tid < topk ? idx_n[kPfTS + tid] : -1;
+      r_next = 2 * kPfTS + tid < topk ? idx_n[2 * kPfTS + tid] : -1;
     }
+    asm volatile("bar.sync 2, 256;" ::: "memory");
+    pf_gather_tile(sm + kPfOffRaw, ms.rows[0], tid, base, codes, sf);
     // the FP4 query, exactly dequantised into the swizzled Q chunks
     for (int v = tid; v < 64 * 64; v += kPfWorkers) {
       const int h = v >> 6, rest = v & 63, kc = rest >> 3, u = rest & 7;
@@ -213,15 +219,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
       uint8_t *raw = sm + kPfOffRaw + buf * kPfRawBytes;
-      ok = mbar_wait(&ms.bar_g[buf], (t >> 1) & 1) && ok;
-      // prefetch the next tile's rows into the other raw buffer (dequantised last tile), and
-      // load the index of the tile after it
-      if (t + 1 < n_tiles && tid < kPfTS) {
-        pf_gather(sm + kPfOffRaw + (buf ^ 1) * kPfRawBytes, ms, buf ^ 1, tid, r_next, base, codes,
-                  sf);
-        const int slot = (t + 2) * kPfTS + tid;
-        r_next = slot < topk ? idx_n[slot] : -1;
-      }
+      asm volatile("cp.async.wait_all;" ::: "memory");  // this tile's rows (own copies)
+      asm volatile("bar.sync 2, 256;" ::: "memory");      // ... and everyone's
+      // prefetch the next tile's rows into the other raw buffer (dequantised last tile)
+      if (t + 1 < n_tiles)
+        pf_gather_tile(sm + kPfOffRaw + (buf ^ 1) * kPfRawBytes, ms.rows[buf ^ 1], tid, base,
+                       codes, sf);
       // dequantise two chunks at a time, each pair once PV(t-1) no longer reads it
       for (int cp = 0; cp < 4; ++cp) {
         if (t > 0) ok = mbar_wait(&ms.bar_pv[cp], (t - 1) & 1) && ok;
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         float mt = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (ms.slot_ok[buf][j0 + j]) mt = fmaxf(mt, s[j]);
+          if (ms.rows[buf][j0 + j] >= 0) mt = fmaxf(mt, s[j]);
         ms.mhalf[sh][h] = mt;
         asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps
         mt = fmaxf(ms.mhalf[0][h], ms.mhalf[1][h]);
@@ -282,8 +285,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          const float p0 = ms.slot_ok[buf][j0 + j] ? exp2f(s[j] - m_ref) : 0.0f;
-          const float p1 = ms.slot_ok[buf][j0 + j + 1] ? exp2f(s[j + 1] - m_ref) : 0.0f;
+          const float p0 = ms.rows[buf][j0 + j] >= 0 ? exp2f(s[j] - m_ref) : 0.0f;
+          const float p1 = ms.rows[buf][j0 + j + 1] >= 0 ? exp2f(s[j + 1] - m_ref) : 0.0f;
           l_run += p0 + p1;
           const __half b0 = __float2half_rn(p0), b1 = __float2half_rn(p1);
           hi[j / 2] = (uint32_t)__half_as_ushort(b0) | ((uint32_t)__half_as_ushort(b1) << 16);
@@ -314,6 +317,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
           tmem_st16(la + c, r);
         }
         tmem_st_wait();
+      }
+      // the slots of tile t+2 go where tile t's were (tile t's readers are past the barrier
+      // above); the barrier below publishes them for the gather issued at tile t+1
+      if (tid < kPfTS) {
+        ms.rows[buf][tid] = r_next;
+        const int slot = (t + 3) * kPfTS + tid;
+        r_next = slot < topk ? idx_n[slot] : -1;
       }
       tc_fence_before();
       asm volatile("bar.sync 2, 256;" ::: "memory");  // factors read before they change
