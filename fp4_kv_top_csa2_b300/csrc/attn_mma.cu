@@ -8,7 +8,9 @@
 // MMA shape, heads padded).  Small tiles keep the chain of dependent steps short and spread one
 // query over many SMs (64 x 2 CTAs for 2,048 rows and 64 heads).  Steps:
 //   1. Q [32 heads x 512] bf16 arrives by TMA as eight 128B-swizzled K-chunks of 64 channels;
-//      each selected row arrives as two bulk copies (256 B of codes, 32 B of scales).
+//      the selected rows (256 B of codes, 32 B of scales each) arrive as 16-byte cp.async copies
+//      spread over all threads (many small copies issue faster this way than one bulk copy
+//      per row).
 //   2. Every row is dequantised exactly (E2M1 x E4M3 has <= 6 significant bits) to bf16 and
 //      stored once, as eight 128B-swizzled chunks [32 rows x 64 channels].
 //   3. S = Q Khat^T: kind::f16, M=128 (heads) x N=32 (rows) x K=512, fp32 in TMEM.
@@ -50,7 +52,7 @@ constexpr int kAttSmem = kOffMisc + 1024 + 1024;      // + alignment slack
 static_assert(kOffQ + 7 * kQChunkBytes + 128 * 128 <= kOffMisc, "Q over-read stays in smem");
 
 struct AttMisc {
-  uint64_t bar_q, bar_g, bar_s, bar_o;
+  uint64_t bar_q, bar_s, bar_o;
   uint32_t tmem_base;
   int slot_ok[kAttTS];
   float m2[kAttHG];
@@ -67,15 +69,6 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162 *>(&b);
   __nv_bfloat162 z = __hmul2(x, y);
   return *reinterpret_cast<uint32_t *>(&z);
-}
-
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
-                                         uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(sm100::smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(sm100::smem_u32(bar))
-      : "memory");
 }
 
 __device__ __forceinline__ void fence_async_smem() {
@@ -99,7 +92,6 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
 
   if (tid == 0) {
     mbar_init(&ms.bar_q, 1);
-    mbar_init(&ms.bar_g, kAttTS);
     mbar_init(&ms.bar_s, 1);
     mbar_init(&ms.bar_o, 1);
     fence_barrier_init();
@@ -125,26 +117,30 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
     for (int kc = 0; kc < 8; ++kc)
       tma_load_2d(sm + kOffQ + kc * kQChunkBytes, &qmap, &ms.bar_q, kc * 64, n * H + h0);
   }
-  if (tid < kAttTS) {
-    const int slot = tile * kAttTS + tid;
+  // the 32 rows as 32 x 18 16-byte cp.async copies (256 B codes + 32 B scales per row) spread
+  // over all threads; an empty slot is a zero row (value 0, never NaN), masked in the softmax
+  for (int i = tid; i < kAttTS * 18; i += kAttThreads) {
+    const int j = i / 18, part = i - j * 18;
+    const int slot = tile * kAttTS + j;
     const int r = slot < topk ? idx[(int64_t)n * topk + slot] : -1;
-    ms.slot_ok[tid] = r >= 0;
+    if (part == 0) ms.slot_ok[j] = r >= 0;
+    uint8_t *dst = part < 16 ? sm + kOffRawC + j * 256 + part * 16
+                             : sm + kOffRawS + j * 32 + (part - 16) * 16;
     if (r >= 0) {
       const int64_t row = base + r;
-      mbar_arrive_expect_tx(&ms.bar_g, 288);
-      bulk_g2s(sm + kOffRawC + tid * 256, codes + row * kCodeBytes, 256, &ms.bar_g);
-      bulk_g2s(sm + kOffRawS + tid * 32, sf + row * kSfBytes, 32, &ms.bar_g);
-    } else {  // empty slot: zero row (value 0, never NaN) and masked in the softmax
-      uint4 z = make_uint4(0, 0, 0, 0);
-      uint4 *c = reinterpret_cast<uint4 *>(sm + kOffRawC + tid * 256);
-      for (int i = 0; i < 16; ++i) c[i] = z;
-      uint4 *s = reinterpret_cast<uint4 *>(sm + kOffRawS + tid * 32);
-      s[0] = z;
-      s[1] = z;
-      mbar_arrive(&ms.bar_g);
+      const uint8_t *src = part < 16 ? codes + row * kCodeBytes + part * 16
+                                     : sf + row * kSfBytes + (part - 16) * 16;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                   "l"(reinterpret_cast<uint64_t>(src))
+                   : "memory");
+    } else {
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
     }
   }
-  bool ok = mbar_wait(&ms.bar_g, 0);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  bool ok = true;
+  __syncthreads();
 
   // ---- 2./3. dequantise the rows once (chunk kc holds channels 64kc..64kc+63 of all 32 rows)
   //           and S = Q Khat^T: the MMAs over chunks 0..3 run while chunks 4..7 are dequantised
