@@ -264,32 +264,23 @@ def profile_calls(st, steps, flush):
 
 def run_e2e(st, steps, dev, graph=False):
     """Same step through the C ABI, inputs copied from pinned host memory each step and the
-    attention outputs read back, all inside the timed region.  graph=True replays the captured
-    step between the copies instead of issuing the calls one by one."""
+    attention outputs read back, all inside the timed region.  The step's per-token inputs
+    (new rows, every layer's queries and weights) sit in one device arena and its outputs in
+    another, so each direction is one copy.  graph=True replays the captured step between the
+    copies instead of issuing the calls one by one."""
     import torch
-    host_in = {"new_x": st.new_x.cpu().pin_memory()}
-    for i, L in enumerate(st.layers):
-        host_in[f"q_attn{i}"] = L["q_attn"].cpu().pin_memory()
-        if "q_idx" in L:
-            host_in[f"q_idx{i}"] = L["q_idx"].cpu().pin_memory()
-            host_in[f"w{i}"] = L["w"].cpu().pin_memory()
-    host_out = [torch.empty_like(L["out"], device="cpu").pin_memory() for L in st.layers]
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    host_in = st.in_arena.buf.cpu().pin_memory()
+    host_out = torch.empty_like(st.out_arena.buf, device="cpu").pin_memory()
+    h2d = host_in.numel()
+    d2h = host_out.numel()
 
     def one():
-        st.new_x.copy_(host_in["new_x"], non_blocking=True)
-        for i, L in enumerate(st.layers):
-            L["q_attn"].copy_(host_in[f"q_attn{i}"], non_blocking=True)
-            if "q_idx" in L:
-                L["q_idx"].copy_(host_in[f"q_idx{i}"], non_blocking=True)
-                L["w"].copy_(host_in[f"w{i}"], non_blocking=True)
+        st.in_arena.buf.copy_(host_in, non_blocking=True)
         if graph:
             st.replay()
         else:
             st.run()
-        for i, L in enumerate(st.layers):
-            host_out[i].copy_(L["out"], non_blocking=True)
+        host_out.copy_(st.out_arena.buf, non_blocking=True)
 
     one()
     torch.cuda.synchronize()

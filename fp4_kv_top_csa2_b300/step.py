@@ -23,6 +23,21 @@ from . import csa2
 from .synth import BLOCK, D, new_token_rows
 
 
+class _Arena:
+    """One contiguous device buffer holding several tensors as 256-byte aligned views, so a
+    step's per-token inputs (or outputs) cross between host and device in one copy."""
+
+    def __init__(self, specs, device):
+        placed, off = [], 0
+        for name, shape, dtype in specs:
+            nbytes = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+            placed.append((name, off, shape, dtype, nbytes))
+            off += (nbytes + 255) // 256 * 256
+        self.buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+        self.views = {name: self.buf[o:o + nb].view(dtype).view(shape)
+                      for name, o, shape, dtype, nb in placed}
+
+
 class Step:
     def __init__(self, inputs: dict, device="cuda", build_cache=True):
         self.inp = inputs
@@ -41,19 +56,35 @@ class Step:
         self.max_vis = inputs["max_vis"]
         self.nq = inputs["q_seq"].numel()
         self.new_rows = new_token_rows(inputs).to(dev)
-        self.new_x = self.kv_bf16[self.new_rows].contiguous()
+        # per-step inputs (new rows, each layer's queries and weights) and outputs live in two
+        # arenas, one host<->device copy each
+        in_specs = [("new_x", (self.new_rows.numel(), D), torch.bfloat16)]
+        out_specs = []
+        for i, L in enumerate(inputs["layers"]):
+            in_specs.append((f"q_attn{i}", tuple(L["q_attn"].shape), L["q_attn"].dtype))
+            if "q_idx" in L:
+                in_specs.append((f"q_idx{i}", tuple(L["q_idx"].shape), L["q_idx"].dtype))
+                in_specs.append((f"w{i}", tuple(L["w"].shape), L["w"].dtype))
+            out_specs.append((f"out{i}", (self.nq, w.H, D), torch.bfloat16))
+        self.in_arena = _Arena(in_specs, dev)
+        self.out_arena = _Arena(out_specs, dev)
+        self.new_x = self.in_arena.views["new_x"]
+        self.new_x.copy_(self.kv_bf16[self.new_rows])
         if build_cache:  # the cache as it stands before the step (all rows), quantised on the GPU
             csa2.csa2_kv_quant_fp4(self.kv_bf16, self.codes, self.sf)
         self.layers = []
         nb = (self.max_vis + BLOCK - 1) // BLOCK
         hier = w.kind == "hier"
-        for L in inputs["layers"]:
-            d = {"mode": L["mode"], "q_attn": L["q_attn"].to(dev)}
+        for i, L in enumerate(inputs["layers"]):
+            d = {"mode": L["mode"], "q_attn": self.in_arena.views[f"q_attn{i}"]}
+            d["q_attn"].copy_(L["q_attn"])
             if "q_idx" in L:
-                d["q_idx"] = L["q_idx"].to(dev)
-                d["w"] = L["w"].to(dev)
+                d["q_idx"] = self.in_arena.views[f"q_idx{i}"]
+                d["q_idx"].copy_(L["q_idx"])
+                d["w"] = self.in_arena.views[f"w{i}"]
+                d["w"].copy_(L["w"])
                 d["idx"] = torch.empty((self.nq, w.topk), dtype=torch.int32, device=dev)
-            d["out"] = torch.empty((self.nq, w.H, D), dtype=torch.bfloat16, device=dev)
+            d["out"] = self.out_arena.views[f"out{i}"]
             d["lse"] = torch.empty((self.nq, w.H), dtype=torch.float32, device=dev)
             self.layers.append(d)
         self.bm = torch.empty((self.nq, nb), dtype=torch.float32, device=dev) if hier else None
