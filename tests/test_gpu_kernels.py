@@ -253,9 +253,12 @@ def _attn_case(B, H, n_rows, topk, seed, holes=True):
     return x, q, idx, cu
 
 
-@pytest.mark.parametrize("B,H,n_rows,topk", [(3, 64, 3000, 2048), (2, 16, 600, 512),
-                                              (1, 64, 100, 33), (4, 64, 50, 1)])
+@pytest.mark.parametrize("B,H,n_rows,topk", [(3, 64, 3000, 2048), (2, 64, 4000, 2048),
+                                              (2, 16, 600, 512), (1, 64, 100, 33),
+                                              (4, 64, 50, 1)])
 def test_decode_attention(csa2, B, H, n_rows, topk):
+    """Batches of 1 to 4 sequences, 16 or 64 heads, Top-K 1 to 2,048 with empty slots (and one
+    sequence with none).  Two calls on one workspace must give the same result."""
     x, q, idx, cu = _attn_case(B, H, n_rows, topk, B * 1000 + topk)
     if topk == 1:
         idx[1] = -1  # a sequence with no valid slot
@@ -267,6 +270,10 @@ def test_decode_attention(csa2, B, H, n_rows, topk):
     ws = csa2.workspace(csa2.csa2_sparse_attn_decode_workspace_size(B, H, topk))
     scale = 1 / math.sqrt(512)
     csa2.csa2_sparse_attn_decode(q.cuda(), codes, sf, cu.cuda(), idx.cuda(), scale, out, lse, ws=ws)
+    out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
+    csa2.csa2_sparse_attn_decode(q.cuda(), codes, sf, cu.cuda(), idx.cuda(), scale, out2, lse2,
+                                 ws=ws)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
     ref = oracle.sparse_attn_decode(_bits(q), codes.cpu().numpy(), sf.cpu().numpy(), cu.numpy(),
                                     idx.numpy(), scale)
     ob, lh = _bits(out), lse.cpu().numpy()
