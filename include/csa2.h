@@ -235,9 +235,10 @@ int csa2_sparse_attn_decode(const void *q_bf16, int B, int H, const uint8_t *cod
 /* ------------------------------------------------------------------------------------------ */
 /*
  * As csa2_sparse_attn_decode, for T query tokens each with its own idx row (causality is carried
- * by the indexer's q_vis).  The query-key contraction runs as a block-scaled FP4 product, so the
- * query is first quantised per (token, head) row with exactly the csa2_kv_quant_fp4 rule (16-
- * channel E4M3 scales, E2M1 values); the definition above then uses that dequantised query.  The
+ * by the indexer's q_vis).  The query-key contraction is a block-scaled FP4 product: the query is
+ * first quantised per (token, head) row with exactly the csa2_kv_quant_fp4 rule (16-channel E4M3
+ * scales, E2M1 values), and the definition above then uses that dequantised query.  (The kernel
+ * computes that product on the exactly dequantised fp16 values with fp32 accumulation.)  The
  * probability-value product uses fp16 probabilities and the exactly dequantised rows.
  *
  * q_bf16  [T, H, 512] bf16.    q_seq [T] int32 in [0, B).   idx [T, topk] int32.
