@@ -47,7 +47,8 @@ struct MqParams {
   int nq, n_tiles, ct;   // key tiles of 128, tiles per chunk
 };
 
-template <int DT>
+// KS: per-key scales present (without them the epilogue skips the multiply by 1).
+template <int DT, bool KS>
 __global__ void __launch_bounds__(kMqThreads, 1) index_multi_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
     const MqParams p) {
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_multi_kernel(
         if (!ok) break;
         tc_fence_after();
         const int64_t pos = (int64_t)t * 128 + row;
-        const float ks = (p.k_scale && pos < p.max_vis) ? p.k_scale[p.base + pos] : 1.0f;
+        const float ks = (KS && pos < p.max_vis) ? p.k_scale[p.base + pos] : 1.0f;
 #pragma unroll 1
         for (int half_q = 0; half_q < 2; ++half_q) {  // 8 queries = 64 columns per round
           uint32_t r[4][16];
@@ -178,8 +179,10 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_multi_kernel(
             float sc = 0.0f;
 #pragma unroll
             for (int h = 0; h < 8; ++h)
-              sc = fmaf(wq[qq * 8 + h],
-                        fmaxf(__uint_as_float(r[qq8 >> 1][8 * (qq8 & 1) + h]) * ks, 0.0f), sc);
+            {
+              const float x = __uint_as_float(r[qq8 >> 1][8 * (qq8 & 1) + h]);
+              sc = fmaf(wq[qq * 8 + h], fmaxf(KS ? x * ks : x, 0.0f), sc);
+            }
             const bool valid = pos < vq[qq];
             float m = valid ? sc : -INFINITY;
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
@@ -228,18 +231,16 @@ cudaError_t launch_score_scan_multi(const void *q_idx, int dtype, const float *w
   const int64_t groups = (nq + kMqQ - 1) / kMqQ;
   p.ct = (int)std::max<int64_t>(1, std::min<int64_t>(16, groups * p.n_tiles / (grid * 8)));
   const size_t smem = sizeof(MqSmem) + 1024;
+  auto go = [&](auto kern) {
+    cudaError_t err = set_smem_once(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(kern, dim3(grid), dim3(kMqThreads), smem, st, km, qm, p);
+  };
   cudaError_t e;
-  if (dtype == CSA2_E4M3) {
-    e = set_smem_once(index_multi_kernel<CSA2_E4M3>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(index_multi_kernel<CSA2_E4M3>, dim3(grid), dim3(kMqThreads), smem, st, km, qm, p);
-  } else {
-    e = set_smem_once(index_multi_kernel<CSA2_BF16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(index_multi_kernel<CSA2_BF16>, dim3(grid), dim3(kMqThreads), smem, st, km, qm, p);
-  }
+  if (dtype == CSA2_E4M3)
+    e = k_scale ? go(index_multi_kernel<CSA2_E4M3, true>) : go(index_multi_kernel<CSA2_E4M3, false>);
+  else
+    e = k_scale ? go(index_multi_kernel<CSA2_BF16, true>) : go(index_multi_kernel<CSA2_BF16, false>);
   note_launches(1);
   return e;
 }
