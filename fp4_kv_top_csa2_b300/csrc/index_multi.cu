@@ -8,9 +8,9 @@
 // the indexer scores the causally visible positions) is applied in the epilogue, which writes
 // the block maxima over 8 positions for every query.
 //
-// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
-// warps 2..9 = epilogue; warp w reads TMEM lanes 32*(w%4)..+31 and the 128 accumulator columns
-// of queries 16*((w-2)/4) .. +15.  TMEM: two 256-column accumulators.  Work = chunks of up to
+// Warp roles (576 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
+// warps 2..17 = epilogue; warp w reads TMEM lanes 32*(w%4)..+31 and the 64 accumulator columns
+// of queries 8*((w-2)/4) .. +7.  TMEM: two 256-column accumulators.  Work = chunks of up to
 // CT key tiles of one 32-query group, dealt round-robin to a persistent grid (one CTA per SM).
 #include "sm100.cuh"
 
@@ -19,14 +19,16 @@ namespace csa2 {
 constexpr int kMqQ = 32;                        // queries per group
 constexpr int kMqN = 256;                       // MMA N = 32 queries x 8 heads
 constexpr int kMqStages = 4;
-constexpr int kMqThreads = 320;
+constexpr int kMqEpiWarps = 16;                 // epilogue warps: 4 per TMEM lane quarter
+constexpr int kMqQPW = kMqQ / (kMqEpiWarps / 4);  // queries per epilogue warp (8)
+constexpr int kMqThreads = 64 + kMqEpiWarps * 32;
 constexpr int kMqQBytes = kMqN * 128;           // 32 KB
 
 struct MqSmem {
   uint8_t keys[kMqStages][128 * 128];           // 16 KB tiles, 1024-byte aligned
   uint8_t q[2][kMqQBytes];
-  float wsm[8][16 * 8];  // per epilogue warp: its 16 queries' head weights for the chunk
-  int vsm[8][16];        // and their visible lengths
+  float wsm[kMqEpiWarps][kMqQPW * 8];  // per epilogue warp: its queries' head weights
+  int vsm[kMqEpiWarps][kMqQPW];        // and their visible lengths
   uint64_t full[kMqStages], empty[kMqStages];
   uint64_t qfull[2], qempty[2];
   uint64_t tfull[2], tempty[2];
@@ -67,7 +69,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_multi_kernel(
       mbar_init(&sm.qfull[s], 1);
       mbar_init(&sm.qempty[s], 1);
       mbar_init(&sm.tfull[s], 1);
-      mbar_init(&sm.tempty[s], 256);
+      mbar_init(&sm.tempty[s], kMqEpiWarps * 32);
     }
     sm.abort = 0;
     fence_barrier_init();
@@ -137,24 +139,24 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_multi_kernel(
       }
     }
   } else {  // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;                 // 0..7
-    const int quarter = warp & 3, half = ew >> 2;
+    const int ew = warp - 2;                 // 0 .. kMqEpiWarps-1
+    const int quarter = warp & 3, qslot = ew >> 2;  // queries qslot*kMqQPW .. +kMqQPW-1
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     uint32_t acc = 0;
     for (int j = blockIdx.x; j < total; j += gridDim.x) {
       const int g = j / chunks_per_group, t0 = (j % chunks_per_group) * p.ct;
       const int t1 = min(p.n_tiles, t0 + p.ct);
-      // this chunk's weights and visibility (the 16 queries of this warp's half), warp-local
+      // this chunk's weights and visibility (this warp's queries), warp-local
       float *wq = sm.wsm[ew];
       int *vq = sm.vsm[ew];
       __syncwarp();
-      for (int i = lane; i < 16 * 8; i += 32) {
-        const int q = g * kMqQ + half * 16 + i / 8;
+      for (int i = lane; i < kMqQPW * 8; i += 32) {
+        const int q = g * kMqQ + qslot * kMqQPW + i / 8;
         wq[i] = q < p.nq ? __ldg(p.w + (int64_t)q * 8 + (i & 7)) : 0.0f;
       }
-      if (lane < 16) {
-        const int q = g * kMqQ + half * 16 + lane;
+      if (lane < kMqQPW) {
+        const int q = g * kMqQ + qslot * kMqQPW + lane;
         vq[lane] = q < p.nq ? p.q_vis[q] : 0;
       }
       __syncwarp();
@@ -167,9 +169,9 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_multi_kernel(
         const int64_t pos = (int64_t)t * 128 + row;
         const float ks = (KS && pos < p.max_vis) ? p.k_scale[p.base + pos] : 1.0f;
 #pragma unroll 1
-        for (int half_q = 0; half_q < 2; ++half_q) {  // 8 queries = 64 columns per round
+        for (int half_q = 0; half_q < kMqQPW / 8; ++half_q) {  // 8 queries = 64 columns a round
           uint32_t r[4][16];
-          const uint32_t col = lane_addr + a * kMqN + half * 128 + half_q * 64;
+          const uint32_t col = lane_addr + a * kMqN + qslot * kMqQPW * 8 + half_q * 64;
 #pragma unroll
           for (int l = 0; l < 4; ++l) tmem_ld16(col + 16 * l, r[l]);  // four loads, one wait
           tmem_ld_wait();
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_multi_kernel(
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            const int q = g * kMqQ + half * 16 + qq;
+            const int q = g * kMqQ + qslot * kMqQPW + qq;
             if (p.scores && valid && q < p.nq) p.scores[(int64_t)q * p.sc_stride + pos] = sc;
             if ((lane & 7) == 0 && valid && q < p.nq)
               p.bm[(int64_t)q * p.bm_stride + (pos >> 3)] = m;
