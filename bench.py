@@ -44,19 +44,71 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples (every 50 ms) with host timestamps, so the samples
-    that fall inside the timed window can be picked out afterwards."""
+    """SM clock and throttle-reason samples with host timestamps, so the samples that fall
+    inside the timed window can be picked out afterwards.  NVML is polled every ~0.5 ms (the
+    timed window of a decode run lasts a few milliseconds); without NVML, nvidia-smi every 50 ms.
+    Both only read the GPU's state."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    NVML_BITS = [("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40),
+                 ("sw_thermal_slowdown", 0x20), ("sw_power_cap", 0x4)]
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.nvml = None
+        self.period = "50 ms"
         self.samples = []  # (host time, sm_mhz, sm_max_mhz, active reasons)
+        self.running = False
+
+    def _nvml_index(self):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if ids and all(x.isdigit() for x in ids) and self.index < len(ids):
+            return int(ids[self.index])
+        return self.index
+
+    @staticmethod
+    def _nvml_open(index):
+        """Read-only NVML queries through the driver's library: (sm clock, max sm clock,
+        active clock-event reason bits) as functions of nothing."""
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+            raise OSError("nvmlDeviceGetHandleByIndex")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+        def clock(fn):
+            v = ctypes.c_uint()
+            if fn(h, ctypes.c_int(1), ctypes.byref(v)) != 0:  # NVML_CLOCK_SM
+                raise OSError("clock query")
+            return float(v.value)
+
+        def bits():
+            v = ctypes.c_ulonglong()
+            if reasons(h, ctypes.byref(v)) != 0:
+                raise OSError("reason query")
+            return int(v.value)
+        return (lambda: clock(lib.nvmlDeviceGetClockInfo)), clock(lib.nvmlDeviceGetMaxClockInfo), bits
 
     def start(self):
+        try:
+            self.nvml = self._nvml_open(self._nvml_index())
+            self.nvml[0]()
+            self.nvml[2]()
+            self.period = "0.5 ms"
+            self.running = True
+            self.t = threading.Thread(target=self._poll_nvml, daemon=True)
+            self.t.start()
+            return self
+        except Exception:  # no NVML: nvidia-smi instead
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
@@ -71,6 +123,18 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def _poll_nvml(self):
+        sm_fn, smax, bits_fn = self.nvml
+        while self.running:
+            try:
+                sm = sm_fn()
+                bits = bits_fn()
+            except Exception:
+                break
+            act = [nm for nm, b in self.NVML_BITS if bits & b]
+            self.samples.append((time.time(), sm, smax, act))
+            time.sleep(0.0005)
+
     def _read(self):
         for line in self.proc.stdout:
             parts = [x.strip() for x in line.split(",")]
@@ -84,6 +148,10 @@ class ClockSampler:
             self.samples.append((time.time(), sm, smax, act))
 
     def stop(self):
+        if self.nvml:
+            self.running = False
+            self.t.join(timeout=2)
+            return
         if self.proc:
             time.sleep(0.1)
             self.proc.terminate()
@@ -98,12 +166,13 @@ class ClockSampler:
         where = "timed window"
         if not inside:  # window shorter than the sampling period: nearest samples around it
             inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
-            where = "nearest to the timed window (window shorter than the 50 ms sample period)"
+            where = f"nearest to the timed window (window shorter than the {self.period} period)"
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         reasons = sorted({r for s in inside for r in s[3]})
         return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": inside[0][2],
-                "reasons": reasons, "samples": len(inside), "sampled": where}
+                "reasons": reasons, "samples": len(inside), "sampled": where,
+                "source": "nvml" if self.nvml else "nvidia-smi"}
 
 
 # ------------------------------------------------------------------------------------------------
