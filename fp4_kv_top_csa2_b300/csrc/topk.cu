@@ -1245,7 +1245,8 @@ static cudaError_t launch_topk_reg(const float *vals, int64_t stride, int64_t n_
 }
 
 static bool topk_use_reg(int nq, int64_t n_elems) {
-  return nq <= 64 && n_elems >= 1 && n_elems <= kRgSpan;
+  (void)nq;  // one CTA per query, any number of queries
+  return n_elems >= 1 && n_elems <= kRgSpan;
 }
 
 // The chunked two-kernel path serves few queries over many elements.
