@@ -27,7 +27,7 @@ constexpr int kMqQBytes = kMqN * 128;           // 32 KB
 struct MqSmem {
   uint8_t keys[kMqStages][128 * 128];           // 16 KB tiles, 1024-byte aligned
   uint8_t q[2][kMqQBytes];
-  float wsm[kMqEpiWarps][kMqQPW * 8];  // per epilogue warp: its queries' head weights
+  __align__(16) float wsm[kMqEpiWarps][kMqQPW * 8];  // per epilogue warp: its queries' head weights
   int vsm[kMqEpiWarps][kMqQPW];        // and their visible lengths
   uint64_t full[kMqStages], empty[kMqStages];
   uint64_t qfull[2], qempty[2];
@@ -143,23 +143,32 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_multi_kernel(
     const int quarter = warp & 3, qslot = ew >> 2;  // queries qslot*kMqQPW .. +kMqQPW-1
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    // After the transposed block-maximum reduction below, lane l holds the maximum of block
+    // l/8 (of this warp's 32 rows) for query rq of the warp's eight.
+    const int rq = ((lane & 1) << 2) | (lane & 2) | ((lane >> 2) & 1);
     uint32_t acc = 0;
     for (int j = blockIdx.x; j < total; j += gridDim.x) {
       const int g = j / chunks_per_group, t0 = (j % chunks_per_group) * p.ct;
       const int t1 = min(p.n_tiles, t0 + p.ct);
-      // this chunk's weights and visibility (this warp's queries), warp-local
+      const int q0 = g * kMqQ + qslot * kMqQPW;
+      // this chunk's weights and visible lengths (this warp's queries; a query beyond nq sees
+      // nothing, so every store below is masked by visibility alone)
       float *wq = sm.wsm[ew];
       int *vq = sm.vsm[ew];
       __syncwarp();
       for (int i = lane; i < kMqQPW * 8; i += 32) {
-        const int q = g * kMqQ + qslot * kMqQPW + i / 8;
+        const int q = q0 + i / 8;
         wq[i] = q < p.nq ? __ldg(p.w + (int64_t)q * 8 + (i & 7)) : 0.0f;
       }
       if (lane < kMqQPW) {
-        const int q = g * kMqQ + qslot * kMqQPW + lane;
+        const int q = q0 + lane;
         vq[lane] = q < p.nq ? p.q_vis[q] : 0;
       }
       __syncwarp();
+      const int vmin = __reduce_min_sync(0xffffffffu, lane < kMqQPW ? vq[lane] : INT_MAX);
+      const int my_vis = vq[rq];
+      float *const bm_row = p.bm + (int64_t)(q0 + rq) * p.bm_stride;
+      float *const sc_rows = p.scores ? p.scores + (int64_t)q0 * p.sc_stride : nullptr;
       bool ok = true;
       for (int t = t0; t < t1; ++t, ++acc) {
         const uint32_t a = acc & 1, aph = (acc >> 1) & 1;
@@ -168,36 +177,68 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_multi_kernel(
         tc_fence_after();
         const int64_t pos = (int64_t)t * 128 + row;
         const float ks = (KS && pos < p.max_vis) ? p.k_scale[p.base + pos] : 1.0f;
-#pragma unroll 1
-        for (int half_q = 0; half_q < kMqQPW / 8; ++half_q) {  // 8 queries = 64 columns a round
+        // every position of this tile is visible to all eight queries
+        const bool all_vis = (int64_t)t * 128 + 128 <= vmin;
+        float v[kMqQPW];
+        {
           uint32_t r[4][16];
-          const uint32_t col = lane_addr + a * kMqN + qslot * kMqQPW * 8 + half_q * 64;
+          const uint32_t col = lane_addr + a * kMqN + qslot * kMqQPW * 8;
 #pragma unroll
           for (int l = 0; l < 4; ++l) tmem_ld16(col + 16 * l, r[l]);  // four loads, one wait
           tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&sm.tempty[a]);  // the accumulator is in registers: release it
+          const float4 *w4 = reinterpret_cast<const float4 *>(wq);
 #pragma unroll
-          for (int qq8 = 0; qq8 < 8; ++qq8) {
-            const int qq = half_q * 8 + qq8;
+          for (int qq = 0; qq < kMqQPW; ++qq) {
+            const float4 wa = w4[2 * qq], wb = w4[2 * qq + 1];
+            const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
             float sc = 0.0f;
 #pragma unroll
-            for (int h = 0; h < 8; ++h)
-            {
-              const float x = __uint_as_float(r[qq8 >> 1][8 * (qq8 & 1) + h]);
-              sc = fmaf(wq[qq * 8 + h], fmaxf(KS ? x * ks : x, 0.0f), sc);
+            for (int h = 0; h < 8; ++h) {
+              const float x = __uint_as_float(r[qq >> 1][8 * (qq & 1) + h]);
+              sc = fmaf(wv[h], fmaxf(KS ? x * ks : x, 0.0f), sc);
             }
-            const bool valid = pos < vq[qq];
-            float m = valid ? sc : -INFINITY;
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            const int q = g * kMqQ + qslot * kMqQPW + qq;
-            if (p.scores && valid && q < p.nq) p.scores[(int64_t)q * p.sc_stride + pos] = sc;
-            if ((lane & 7) == 0 && valid && q < p.nq)
-              p.bm[(int64_t)q * p.bm_stride + (pos >> 3)] = m;
+            v[qq] = sc;
           }
         }
-        tc_fence_before();
-        mbar_arrive(&sm.tempty[a]);
+        if (sc_rows) {
+          float *sp = sc_rows + pos;
+          if (all_vis) {
+#pragma unroll
+            for (int qq = 0; qq < kMqQPW; ++qq, sp += p.sc_stride) *sp = v[qq];
+          } else {
+#pragma unroll
+            for (int qq = 0; qq < kMqQPW; ++qq, sp += p.sc_stride)
+              if (pos < vq[qq]) *sp = v[qq];
+          }
+        }
+        if (!all_vis) {
+#pragma unroll
+          for (int qq = 0; qq < kMqQPW; ++qq) v[qq] = pos < vq[qq] ? v[qq] : -INFINITY;
+        }
+        // Block maxima of eight queries over eight lanes in three exchange steps: at each
+        // step a lane keeps half of its queries, sends the other half to its partner and takes
+        // the maximum with what it receives.
+        const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
+        float u[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float keep = b0 ? v[i + 4] : v[i], send = b0 ? v[i] : v[i + 4];
+          u[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+        }
+        float y[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float keep = b1 ? u[i + 2] : u[i], send = b1 ? u[i] : u[i + 2];
+          y[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+        }
+        {
+          const float keep = b2 ? y[1] : y[0], send = b2 ? y[0] : y[1];
+          const float m = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+          const int64_t first = (int64_t)t * 128 + quarter * 32 + (lane & ~7);
+          if (first < my_vis) bm_row[first >> 3] = m;
+        }
       }
       if (!ok) { sm.abort = 1; break; }
     }
