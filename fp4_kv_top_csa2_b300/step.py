@@ -11,7 +11,14 @@ Prefill: the T new rows are quantised into the cache, the indexer selects Top-K 
 (query i sees positions [0, P0 + i]), then sparse prefill attention.
 
 All device buffers (cache, queries, outputs, workspaces) are allocated once here with torch
-(caller-side allocation); `run()` only enqueues C-ABI calls on the current stream.
+(caller-side allocation); `run()` only enqueues C-ABI calls.
+
+Layers of one step depend on one another only through indices: a Reindex layer needs the
+candidate pool of the first Full layer, a Reuse layer the indices of the layer it reuses, and
+every attention the new rows in the cache.  With several layers `run()` therefore gives each
+layer its own stream (layer 0 on the caller's) and orders them by events along exactly those
+dependencies, so the other layers' selections and attentions overlap.  Each layer then has its
+own workspaces.  `concurrent=False` issues the same calls one after another on one stream.
 """
 from __future__ import annotations
 
@@ -39,7 +46,7 @@ class _Arena:
 
 
 class Step:
-    def __init__(self, inputs: dict, device="cuda", build_cache=True):
+    def __init__(self, inputs: dict, device="cuda", build_cache=True, concurrent=True):
         self.inp = inputs
         self.w = w = inputs["workload"]
         self.dev = device
@@ -97,14 +104,33 @@ class Step:
                      csa2.csa2_index_score_topk_pool_workspace_size(self.nq, self.max_vis,
                                                                     w.topk, w.n_pool_blocks))
         self.ws_index = csa2.workspace(ws, dev)
+        # the layer each layer takes its indices from
+        self.src, last = [], None
+        for i, L in enumerate(self.layers):
+            if L["mode"] in ("full", "reindex"):
+                last = i
+            self.src.append(last)
+        self.concurrent = concurrent and len(self.layers) > 1
+        self.side = []
+        if self.concurrent:
+            self.side = [torch.cuda.Stream(device=dev) for _ in self.layers[1:]]
+            self.ev_ready = torch.cuda.Event()
+            self.ev_pool = torch.cuda.Event()
+            self.ev_idx = [torch.cuda.Event() for _ in self.layers]
+            self.ev_done = [torch.cuda.Event() for _ in self.layers]
+        for i, L in enumerate(self.layers):
+            if "idx" in L:
+                L["ws_index"] = (csa2.workspace(ws, dev) if self.concurrent and i > 0
+                                 else self.ws_index)
         self.ws_pool = (csa2.workspace(csa2.csa2_hier_candidate_pool_workspace_size(
             self.nq, nb, w.n_pool_blocks), dev) if hier else None)
         if w.kind == "prefill":
-            self.ws_attn = csa2.workspace(
-                csa2.csa2_sparse_attn_prefill_workspace_size(self.nq, w.H, w.topk), dev)
+            ws_a = csa2.csa2_sparse_attn_prefill_workspace_size(self.nq, w.H, w.topk)
         else:
-            self.ws_attn = csa2.workspace(
-                csa2.csa2_sparse_attn_decode_workspace_size(self.nq, w.H, w.topk), dev)
+            ws_a = csa2.csa2_sparse_attn_decode_workspace_size(self.nq, w.H, w.topk)
+        self.ws_attn = csa2.workspace(ws_a, dev)
+        for i, L in enumerate(self.layers):
+            L["ws_attn"] = csa2.workspace(ws_a, dev) if self.concurrent and i > 0 else self.ws_attn
 
     def drop_source_rows(self):
         """Free the bf16 rows the cache was quantised from (the step only reads the new rows)."""
@@ -120,17 +146,17 @@ class Step:
         csa2.csa2_index_score_topk(
             layer["q_idx"], self.w.idx_dtype, layer["w"], self.k_idx, self.cu_ctx, self.q_seq,
             self.q_vis, self.max_vis, self.w.topk, layer["idx"], cand_blocks=cand,
-            out_block_max=block_max, ws=self.ws_index, stream=stream)
+            out_block_max=block_max, ws=layer["ws_index"], stream=stream)
 
     def attend(self, layer, idx, stream=None):
         if self.w.kind == "prefill":
             csa2.csa2_sparse_attn_prefill(layer["q_attn"], self.q_seq, self.codes, self.sf,
                                           self.cu_ctx, idx, self.scale, layer["out"],
-                                          layer["lse"], ws=self.ws_attn, stream=stream)
+                                          layer["lse"], ws=layer["ws_attn"], stream=stream)
         else:
             csa2.csa2_sparse_attn_decode(layer["q_attn"], self.codes, self.sf, self.cu_ctx, idx,
                                          self.scale, layer["out"], layer["lse"],
-                                         ws=self.ws_attn, stream=stream)
+                                         ws=layer["ws_attn"], stream=stream)
 
     def index_with_pool(self, layer, stream=None):
         """The first Full layer of the hierarchical decoder: its selection and the candidate
@@ -138,25 +164,48 @@ class Step:
         csa2.csa2_index_score_topk_pool(
             layer["q_idx"], self.w.idx_dtype, layer["w"], self.k_idx, self.cu_ctx, self.q_seq,
             self.q_vis, self.max_vis, self.w.topk, layer["idx"], self.w.n_pool_blocks, self.pool,
-            out_block_max=self.bm, ws=self.ws_index, stream=stream)
+            out_block_max=self.bm, ws=layer["ws_index"], stream=stream)
+
+    def _select(self, i, L, stream):
+        """Layer i's own selection (Full or Reindex); True if it builds the candidate pool."""
+        if L["mode"] == "full":
+            if self.pool is not None and all(M["mode"] != "full" for M in self.layers[:i]):
+                self.index_with_pool(L, stream=stream)
+                return True
+            self.index(L, stream=stream)
+        elif L["mode"] == "reindex":
+            self.index(L, cand=self.pool, stream=stream)
+        return False
 
     def run(self, stream=None):
-        """One step: quantise the new rows, then every layer in order."""
-        self.quantize_new_rows(stream)
-        last_idx = None
+        """One step: quantise the new rows, then every layer (see the module docstring for the
+        order of the calls)."""
+        main = stream if stream is not None else torch.cuda.current_stream()
+        self.quantize_new_rows(main)
+        if not self.concurrent:
+            for i, L in enumerate(self.layers):
+                self._select(i, L, main)
+                self.attend(L, self.layers[self.src[i]]["idx"], stream=main)
+            return
+        self.ev_ready.record(main)
+        streams = [main] + self.side
         for i, L in enumerate(self.layers):
-            if L["mode"] == "full":
-                first_full = self.pool is not None and all(
-                    M["mode"] != "full" for M in self.layers[:i])
-                if first_full:
-                    self.index_with_pool(L, stream=stream)
-                else:
-                    self.index(L, stream=stream)
-                last_idx = L["idx"]
-            elif L["mode"] == "reindex":
-                self.index(L, cand=self.pool, stream=stream)
-                last_idx = L["idx"]
-            self.attend(L, last_idx, stream=stream)
+            s = streams[i]
+            if i > 0:
+                s.wait_event(self.ev_ready)
+            if L["mode"] == "reindex" and self.pool is not None:
+                s.wait_event(self.ev_pool)
+            elif L["mode"] not in ("full", "reindex"):
+                s.wait_event(self.ev_idx[self.src[i]])
+            if self._select(i, L, s):
+                self.ev_pool.record(s)
+            if L["mode"] in ("full", "reindex"):
+                self.ev_idx[i].record(s)
+            self.attend(L, self.layers[self.src[i]]["idx"], stream=s)
+            if i > 0:
+                self.ev_done[i].record(s)
+        for i in range(1, len(self.layers)):
+            main.wait_event(self.ev_done[i])
 
     # ------------------------------------------------------------------------------------------
     def capture(self):

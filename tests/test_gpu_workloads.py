@@ -112,3 +112,41 @@ def test_workload_full_size(mods, name):
             o, l = ref_a[n]
             check_attn(out_b[n], lse[n], o, l, oracle.double_to_bf16(o),
                        f"{name} layer {li} ({mode}) attention {n}")
+
+
+@pytest.mark.parametrize("B,L", [(1, 65536), (3, 40000)])
+def test_concurrent_layers_match_serial(mods, B, L):
+    """The hierarchical decoder's layers on their own streams (ordered by events along the
+    pool and index dependencies), run directly and as a replayed CUDA graph, give bit for bit
+    what the same calls give one after another on one stream."""
+    step, synth = mods
+    w = synth.scaled(synth.WORKLOADS["hier_decode_l1m"], B=B, L=(L,) * B)
+    inp = synth.make_inputs(w)
+    ser = step.Step(inp, concurrent=False)
+    con = step.Step(inp, concurrent=True)
+    assert not ser.side and len(con.side) == len(w.modes) - 1
+    ser.run()
+    torch.cuda.synchronize()
+    want = [(M["out"].clone(), M["lse"].clone(), M.get("idx")) for M in ser.layers]
+    want_idx = [None if i is None else i.clone() for _, _, i in want]
+
+    def same():
+        torch.cuda.synchronize()
+        for li, (M, (o, l, _), ix) in enumerate(zip(con.layers, want, want_idx)):
+            assert torch.equal(M["out"].view(torch.int16), o.view(torch.int16)), li
+            assert torch.equal(M["lse"], l), li
+            if ix is not None:
+                assert torch.equal(M["idx"], ix), li
+        assert torch.equal(con.pool, ser.pool)
+
+    for _ in range(3):
+        for M in con.layers:
+            M["out"].zero_()
+        con.run()
+        same()
+    con.capture()
+    for _ in range(3):
+        for M in con.layers:
+            M["out"].zero_()
+        con.replay()
+        same()
