@@ -2,7 +2,7 @@
 //
 // For sequence n, head h: softmax_j(scale * q_h . khat_j) over the selected rows j, applied to
 // the same rows (K = V = the dequantised latent row; the model card's Introduction, CSA2
-// paragraph: attention reuses "Top-K sparse-attention indices" into the FP4 main KV).
+// paragraph: the sparse attention reads the FP4 main-KV rows that a shared Top-K index set names).
 //
 // One CTA = one query (sequence) x one tile of 32 selected rows x one group of 32 heads (M=128
 // MMA shape, heads padded).  Small tiles keep the chain of dependent steps short and spread one

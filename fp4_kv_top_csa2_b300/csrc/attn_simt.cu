@@ -2,7 +2,7 @@
 //
 // For each query n and head h: softmax(scale * q_h . khat_j) over the selected rows j, applied
 // to the same rows (K = V = the dequantised latent row; the model card's Introduction, CSA2
-// paragraph: layers reuse "Top-K sparse-attention indices" into the FP4 main KV).
+// paragraph: the sparse attention reads the FP4 main-KV rows that a shared Top-K index set names).
 //
 // Grid: (split, head group of 16, query).  A CTA walks its share of the Top-K slots in chunks of
 // 32 rows: gather codes + scales, dequantise exactly into fp32 shared memory, scores for 16 heads

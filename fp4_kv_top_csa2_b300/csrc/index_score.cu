@@ -7,7 +7,7 @@
 // Two kernels share one per-key routine, so a position scored by the Full-mode scan and again by
 // candidate scoring gets the identical fp32 value:
 //   * score_scan:  every visible position of every query -> block maxima over 8 positions
-//                  (the Full layer's "selects blocks by their maximum index score");
+//                  (the Full layer ranks blocks by the largest score inside them);
 //   * score_cand:  the positions of a list of blocks (Reindex over the candidate pool, and the
 //                  second stage of Full-mode Top-K).
 #include "common.cuh"

@@ -2,8 +2,8 @@
 //
 // Order: larger score first, equal scores (+0 == -0) -> lower position first.  Output: the
 // selected positions in ascending order, then -1.  Used for Full-mode selection, the candidate
-// pool ("selects blocks by their maximum index score", "DeepSeek V4.1-Flash", aiwiki.ai, section
-// "Compressed Sparse Attention 2") and Reindex selection.
+// pool (blocks ranked by the largest index score inside them, "DeepSeek V4.1-Flash", aiwiki.ai,
+// section "Compressed Sparse Attention 2") and Reindex selection.
 //
 // Keys are order-preserving 32-bit images of the scores (key 0 = not a candidate).  The k-th
 // largest key T is built three bits per round: each round counts, in one pass, how many keys

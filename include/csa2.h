@@ -59,9 +59,9 @@ const char *csa2_error_string(int status);
 /* 1. FP4 main-KV quantisation                                                                  */
 /* ------------------------------------------------------------------------------------------ */
 /*
- * [MC] Introduction, CSA2 paragraph: the main KV is cached as FP4, "E2M1 format, one E4M3 scale
- * per 16 channels"; [WIKI] "KV-cache formats and bounded replay": the main global KV is stored
- * in FP4.  The scale-selection and rounding rules are not given there; this library defines,
+ * [MC] Introduction, CSA2 paragraph: the main KV cache holds E2M1 (FP4) values, and every group
+ * of 16 channels shares one E4M3 scale; [WIKI] "KV-cache formats and bounded replay" likewise
+ * keeps the main global KV in FP4.  The scale-selection and rounding rules are not given there; this library defines,
  * for each row and each group g of 16 consecutive channels:
  *     amax   = max |x_i| over the group              (x is bf16; bf16 -> fp32 is exact)
  *     scode  = E4M3(amax / 6)                         (fp32 division, round-to-nearest-even,
@@ -162,10 +162,10 @@ int csa2_index_score_topk_reindex_noalloc(const void *q_idx, int q_dtype, const 
 /* 3. Hierarchical candidate pool                                                               */
 /* ------------------------------------------------------------------------------------------ */
 /*
- * [MC] Introduction: "a Hierarchical Sparse Indexer further restricts later indexing layers to a
- * candidate pool constructed by the first Full Mode layer"; [WIKI] "Compressed Sparse Attention
- * 2": the first Full layer "selects blocks by their maximum index score"; the released pool is
- * 2,048 blocks of eight positions (16,384 positions), independent of context length.
+ * [MC] Introduction: in the hierarchical indexer, the first Full-mode layer builds a candidate
+ * pool and the later indexing layers search only inside it; [WIKI] "Compressed Sparse Attention
+ * 2": that layer ranks blocks by the largest index score they contain, and the released pool is
+ * 2,048 blocks of eight positions (16,384 positions), whatever the context length.
  * For query n the pool is the min(n_pool_blocks, ceil(q_vis[n]/block_size)) blocks with the
  * largest block_max[n, b] (ties to the lower block id), block ids in ascending order, -1 padded.
  *
@@ -185,8 +185,8 @@ int csa2_hier_candidate_pool(const float *block_max, int nq, const int32_t *q_vi
 /*
  * csa2_index_score_topk_pool -- the first Full layer of the hierarchical decoder in one call:
  * the Full-mode selection of csa2_index_score_topk (cand_blocks NULL) and the candidate pool of
- * csa2_hier_candidate_pool over the same block maxima ([MC] Introduction: the pool is
- * "constructed by the first Full Mode layer").  out_idx, out_block_max (optional here too) and
+ * csa2_hier_candidate_pool over the same block maxima ([MC] Introduction: the first Full-mode
+ * layer is the one that builds the pool).  out_idx, out_block_max (optional here too) and
  * out_pool_blocks are exactly what csa2_index_score_topk followed by csa2_hier_candidate_pool
  * would write.  Both selections take the top blocks by block maximum, so when n_pool_blocks >=
  * min(topk, ceil(max_vis/8)) the pool is also the block list the Full selection draws its
@@ -210,14 +210,14 @@ int csa2_index_score_topk_pool(const void *q_idx, int q_dtype, const float *w, i
 /* 4. Sparse attention, decode                                                                  */
 /* ------------------------------------------------------------------------------------------ */
 /*
- * [MC] Introduction: layers "reuse Top-K sparse-attention indices"; attention reads only the
- * selected rows of the FP4 main KV.  Definition used here, per sequence b and head h:
+ * [MC] Introduction: layers may share one Top-K index set for their sparse attention, which
+ * reads only the selected rows of the FP4 main KV.  Definition used here, per sequence b and head h:
  *     khat_j = dequant(codes[cu_ctx[b]+idx[b,j]], sf[...])   (value(code) * value(scale), exact)
  *     s_j    = softmax_scale * <q[b,h,:], khat_j>             over slots with idx[b,j] >= 0
  *     out    = sum_j softmax(s)_j * khat_j                     (K = V = the latent row)
  *     lse    = log(sum_j exp(s_j))     (natural log; -inf and out = 0 when no slot is valid)
- * Reuse mode ([WIKI] CSA2: reuses "the most recent compatible top-k selection") is this call
- * with the idx buffer of an earlier layer.
+ * Reuse mode ([WIKI] CSA2: a Reuse layer takes the latest compatible Top-K result instead of
+ * selecting again) is this call with the idx buffer of an earlier layer.
  *
  * q_bf16  [B, H, 512] bf16.   1 <= H <= 128.   codes [rows, 256] / sf [rows, 32] (the cache).
  * cu_ctx  [B+1] int64.        idx [B, topk] int32, each >= 0 entry < cu_ctx[b+1]-cu_ctx[b].

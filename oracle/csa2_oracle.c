@@ -44,7 +44,7 @@ double orc_e2m1_value(int code)
     return s ? -mag : mag;
 }
 
-/* E4M3 ("fn" variant, [MC] Introduction "one E4M3 scale"): 1 sign, 4 exponent bits (bias 7),
+/* E4M3 ("fn" variant; the scale format of [MC] Introduction): 1 sign, 4 exponent bits (bias 7),
  * 3 mantissa bits, no inf, S.1111.111 is NaN; exp == 0 is subnormal man * 2^-9. */
 double orc_e4m3_value(int code)
 {
@@ -176,7 +176,7 @@ void orc_kv_dequant_fp4(const uint8_t *codes, const uint8_t *sf, int64_t n_rows,
 }
 
 /* ------------------------------------------------------------------------------------------ */
-/* a2 / a5: indexer score ([WIKI] CSA2: "index keys and queries"; formula is [SPEC])          */
+/* a2 / a5: indexer score ([WIKI] CSA2: the indexer has its own keys and queries; [SPEC] form) */
 /* ------------------------------------------------------------------------------------------ */
 
 /* dtype 0 = bf16 (2 bytes/element), 1 = E4M3 (1 byte/element). */
@@ -248,7 +248,7 @@ int orc_topk(const float *scores, const int64_t *pos, int64_t n, int K, int32_t 
     return kept;
 }
 
-/* [WIKI] CSA2 "selects blocks by their maximum index score": block b covers positions
+/* [WIKI] CSA2: blocks are ranked by the largest index score inside them.  Block b covers positions
  * [bs*b, bs*b+bs) intersected with [0, n); bm_b is the largest score in it. */
 void orc_block_max(const float *scores, int64_t n, int bs, float *bm)
 {
