@@ -40,7 +40,7 @@ def _load() -> ctypes.CDLL:
                                                       I64, P, I, I, P, P]),
         "csa2_index_score_topk_pool_workspace_size": (SZ, [I, I64, I, I]),
         "csa2_index_score_topk_pool": (I, [P, I, P, I, I, I, P, I, I64, P, P, I, P, P, I64, I, P,
-                                           P, I, I, P, P, SZ, P]),
+                                           P, I, I, P, P, SZ, P, P]),
         "csa2_hier_candidate_pool_workspace_size": (SZ, [I, I64, I]),
         "csa2_hier_candidate_pool": (I, [P, I, P, I64, I, I, P, P, SZ, P]),
         "csa2_sparse_attn_decode_workspace_size": (SZ, [I, I, I]),
@@ -62,6 +62,14 @@ lib = _load()
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _event(ev):
+    if ev is None:
+        return None
+    if not ev.cuda_event:
+        raise ValueError("pool_event has no CUDA event yet: record it once before passing it")
+    return ctypes.c_void_p(ev.cuda_event)
 
 
 def _stream(stream):
@@ -127,8 +135,11 @@ def csa2_index_score_topk_pool_workspace_size(nq, max_vis, topk, n_pool_blocks):
 
 def csa2_index_score_topk_pool(q_idx, q_dtype, w, k_idx, cu_ctx, q_seq, q_vis, max_vis, topk,
                                out_idx, n_pool_blocks, out_pool_blocks, k_scale=None,
-                               out_block_max=None, block_size=8, ws=None, stream=None):
-    """Full-mode selection and the candidate pool of the same block maxima, in one call."""
+                               out_block_max=None, block_size=8, ws=None, stream=None,
+                               pool_event=None):
+    """Full-mode selection and the candidate pool of the same block maxima, in one call.
+    `pool_event` (a torch.cuda.Event that has been recorded at least once, so that it exists) is
+    recorded on the stream once the pool is complete."""
     nq, Hi, Di = q_idx.shape
     B = cu_ctx.numel() - 1
     wp, wn = _ws(ws)
@@ -136,7 +147,7 @@ def csa2_index_score_topk_pool(q_idx, q_dtype, w, k_idx, cu_ctx, q_seq, q_vis, m
         _ptr(q_idx), q_dtype, _ptr(w), nq, Hi, Di, _ptr(k_idx), q_dtype, k_idx.shape[0],
         _ptr(k_scale), _ptr(cu_ctx), B, _ptr(q_seq), _ptr(q_vis), max_vis, topk, _ptr(out_idx),
         _ptr(out_block_max), block_size, n_pool_blocks, _ptr(out_pool_blocks), wp, wn,
-        _stream(stream)))
+        _stream(stream), _event(pool_event)))
 
 
 def csa2_hier_candidate_pool_workspace_size(nq, max_blocks, n_pool_blocks):

@@ -106,7 +106,7 @@ int index_score_topk_impl(const void *q_idx, int q_dtype, const float *w, int nq
                           const int32_t *q_vis, int64_t max_vis, const int32_t *cand_blocks,
                           int n_cand_blocks, int topk, int32_t *out_idx, float *out_block_max,
                           int n_pool, int32_t *out_pool, void *workspace, size_t ws_bytes,
-                          void *stream) {
+                          void *stream, void *pool_event = nullptr) {
   if (nq < 0 || nq > 65535 || B < 1 || Hi < 1 || Hi > 16 || topk < 1 || topk > 4096 ||
       max_vis < 0 || max_vis > (int64_t)1 << 30 || k_rows < 0 || k_rows > INT32_MAX)
     return CSA2_ERR_INVALID_ARG;
@@ -117,7 +117,10 @@ int index_score_topk_impl(const void *q_idx, int q_dtype, const float *w, int nq
                   : (n_cand_blocks != 0))
     return CSA2_ERR_INVALID_ARG;
   if (n_pool < 0 || n_pool > 4096 || (n_pool > 0 && cand_blocks)) return CSA2_ERR_INVALID_ARG;
-  if (nq == 0) return CSA2_OK;
+  if (nq == 0)  // nothing to select; the (empty) pool is complete
+    return pool_event ? cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(pool_event),
+                                                    static_cast<cudaStream_t>(stream)))
+                      : CSA2_OK;
   if (!q_idx || !w || !k_idx || !cu_ctx || !q_seq || !q_vis || !out_idx ||
       (n_pool > 0 && !out_pool))
     return CSA2_ERR_INVALID_ARG;
@@ -170,6 +173,8 @@ int index_score_topk_impl(const void *q_idx, int q_dtype, const float *w, int nq
   if (e == cudaSuccess && n_pool > 0 && !ws.pool_list)  // a pool smaller than the block list
     e = launch_topk(bm, ws.nb_max, ws.nb_max, nullptr, 0, kBlock, q_vis, nq, n_pool, out_pool, st,
                     nullptr, 0, ws.topk);
+  if (e == cudaSuccess && pool_event)  // the pool is complete: let its consumers start
+    e = cudaEventRecord(static_cast<cudaEvent_t>(pool_event), st);
   if (pos_scores) {  // the scan kept every score: select among the blocks' positions
     if (e == cudaSuccess)
       e = launch_topk(nullptr, 0, (int64_t)ws.nl * kBlock, list, ws.nl, 1, q_vis, nq, topk,
@@ -244,12 +249,12 @@ int csa2_index_score_topk_pool(const void *q_idx, int q_dtype, const float *w, i
                                const int32_t *q_seq, const int32_t *q_vis, int64_t max_vis,
                                int topk, int32_t *out_idx, float *out_block_max,
                                int block_size, int n_pool_blocks, int32_t *out_pool_blocks,
-                               void *workspace, size_t ws_bytes, void *stream) {
+                               void *workspace, size_t ws_bytes, void *stream, void *pool_event) {
   if (block_size != kBlock || n_pool_blocks < 1) return CSA2_ERR_INVALID_ARG;
   return index_score_topk_impl(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_dtype, k_rows, k_scale,
                                cu_ctx, B, q_seq, q_vis, max_vis, nullptr, 0, topk, out_idx,
                                out_block_max, n_pool_blocks, out_pool_blocks, workspace, ws_bytes,
-                               stream);
+                               stream, pool_event);
 }
 
 size_t csa2_hier_candidate_pool_workspace_size(int nq, int64_t max_blocks, int n_pool_blocks) {

@@ -14,11 +14,13 @@ All device buffers (cache, queries, outputs, workspaces) are allocated once here
 (caller-side allocation); `run()` only enqueues C-ABI calls.
 
 Layers of one step depend on one another only through indices: a Reindex layer needs the
-candidate pool of the first Full layer, a Reuse layer the indices of the layer it reuses, and
-every attention the new rows in the cache.  With several layers `run()` therefore gives each
-layer its own stream (layer 0 on the caller's) and orders them by events along exactly those
-dependencies, so the other layers' selections and attentions overlap.  Each layer then has its
-own workspaces.  `concurrent=False` issues the same calls one after another on one stream.
+candidate pool of the first Full layer (complete before that layer's own position selection,
+which csa2_index_score_topk_pool marks with an event), a Reuse layer the indices of the layer it
+reuses, and every attention the new rows in the cache.  With several layers `run()` therefore
+gives each layer its own stream (layer 0 on the caller's, the new rows' quantisation on one more)
+and orders them by events along exactly those dependencies, so the other layers' selections and
+attentions overlap.  Each layer then has its own workspaces.  `concurrent=False` issues the same
+calls one after another on one stream.
 """
 from __future__ import annotations
 
@@ -114,8 +116,11 @@ class Step:
         self.side = []
         if self.concurrent:
             self.side = [torch.cuda.Stream(device=dev) for _ in self.layers[1:]]
+            self.qstream = torch.cuda.Stream(device=dev)
+            self.ev_start = torch.cuda.Event()
             self.ev_ready = torch.cuda.Event()
             self.ev_pool = torch.cuda.Event()
+            self.ev_pool.record()  # creates the event, which the C ABI records into
             self.ev_idx = [torch.cuda.Event() for _ in self.layers]
             self.ev_done = [torch.cuda.Event() for _ in self.layers]
         for i, L in enumerate(self.layers):
@@ -158,49 +163,52 @@ class Step:
                                          self.scale, layer["out"], layer["lse"],
                                          ws=layer["ws_attn"], stream=stream)
 
-    def index_with_pool(self, layer, stream=None):
+    def index_with_pool(self, layer, stream=None, pool_event=None):
         """The first Full layer of the hierarchical decoder: its selection and the candidate
         pool in one call (csa2_index_score_topk_pool)."""
         csa2.csa2_index_score_topk_pool(
             layer["q_idx"], self.w.idx_dtype, layer["w"], self.k_idx, self.cu_ctx, self.q_seq,
             self.q_vis, self.max_vis, self.w.topk, layer["idx"], self.w.n_pool_blocks, self.pool,
-            out_block_max=self.bm, ws=layer["ws_index"], stream=stream)
+            out_block_max=self.bm, ws=layer["ws_index"], stream=stream, pool_event=pool_event)
 
-    def _select(self, i, L, stream):
-        """Layer i's own selection (Full or Reindex); True if it builds the candidate pool."""
+    def _select(self, i, L, stream, pool_event=None):
+        """Layer i's own selection (Full or Reindex)."""
         if L["mode"] == "full":
             if self.pool is not None and all(M["mode"] != "full" for M in self.layers[:i]):
-                self.index_with_pool(L, stream=stream)
-                return True
-            self.index(L, stream=stream)
+                self.index_with_pool(L, stream=stream, pool_event=pool_event)
+            else:
+                self.index(L, stream=stream)
         elif L["mode"] == "reindex":
             self.index(L, cand=self.pool, stream=stream)
-        return False
 
     def run(self, stream=None):
         """One step: quantise the new rows, then every layer (see the module docstring for the
         order of the calls)."""
         main = stream if stream is not None else torch.cuda.current_stream()
-        self.quantize_new_rows(main)
         if not self.concurrent:
+            self.quantize_new_rows(main)
             for i, L in enumerate(self.layers):
                 self._select(i, L, main)
                 self.attend(L, self.layers[self.src[i]]["idx"], stream=main)
             return
-        self.ev_ready.record(main)
+        # the new rows go into the cache beside layer 0's selection (which does not read it)
+        self.ev_start.record(main)
+        self.qstream.wait_event(self.ev_start)
+        self.quantize_new_rows(self.qstream)
+        self.ev_ready.record(self.qstream)
         streams = [main] + self.side
         for i, L in enumerate(self.layers):
             s = streams[i]
             if i > 0:
-                s.wait_event(self.ev_ready)
+                s.wait_event(self.ev_start)
             if L["mode"] == "reindex" and self.pool is not None:
                 s.wait_event(self.ev_pool)
             elif L["mode"] not in ("full", "reindex"):
                 s.wait_event(self.ev_idx[self.src[i]])
-            if self._select(i, L, s):
-                self.ev_pool.record(s)
+            self._select(i, L, s, pool_event=self.ev_pool)
             if L["mode"] in ("full", "reindex"):
                 self.ev_idx[i].record(s)
+            s.wait_event(self.ev_ready)
             self.attend(L, self.layers[self.src[i]]["idx"], stream=s)
             if i > 0:
                 self.ev_done[i].record(s)

@@ -195,6 +195,10 @@ int csa2_hier_candidate_pool(const float *block_max, int nq, const int32_t *q_vi
  * Arguments as csa2_index_score_topk (Full mode) plus block_size (must be 8), n_pool_blocks
  * (1..4096) and out_pool_blocks ([nq, n_pool_blocks] int32); workspace / ws_bytes at least
  * csa2_index_score_topk_pool_workspace_size(nq, max_vis, topk, n_pool_blocks) bytes.
+ * pool_event  NULL, or a cudaEvent_t created by the caller: it is recorded on `stream` as soon
+ *             as out_pool_blocks is complete (before the position selection that fills out_idx),
+ *             so work that needs only the pool (the Reindex layers) can wait on it and start
+ *             early.  The call neither creates nor destroys it.
  */
 size_t csa2_index_score_topk_pool_workspace_size(int nq, int64_t max_vis, int topk,
                                                  int n_pool_blocks);
@@ -204,7 +208,7 @@ int csa2_index_score_topk_pool(const void *q_idx, int q_dtype, const float *w, i
                                const int32_t *q_seq, const int32_t *q_vis, int64_t max_vis,
                                int topk, int32_t *out_idx, float *out_block_max,
                                int block_size, int n_pool_blocks, int32_t *out_pool_blocks,
-                               void *workspace, size_t ws_bytes, void *stream);
+                               void *workspace, size_t ws_bytes, void *stream, void *pool_event);
 
 /* ------------------------------------------------------------------------------------------ */
 /* 4. Sparse attention, decode                                                                  */

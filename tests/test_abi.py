@@ -69,7 +69,7 @@ def test_host_validation_rejects_bad_arguments(csa2):
     # index + pool: block size 8, pool size 1..4096, pool output required, workspace
     pargs = lambda bs, npool, outp, wsb: L.csa2_index_score_topk_pool(
         p, 1, p, 1, 8, 128, p, 1, 5000, None, p, 1, p, p, 1000, 16, p, None, bs, npool, outp, p,
-        wsb, None)
+        wsb, None, None)
     assert pargs(4, 2048, p, 1 << 30) == -1
     assert pargs(8, 0, p, 1 << 30) == -1
     assert pargs(8, 5000, p, 1 << 30) == -1
