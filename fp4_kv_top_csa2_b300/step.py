@@ -13,14 +13,18 @@ Prefill: the T new rows are quantised into the cache, the indexer selects Top-K 
 All device buffers (cache, queries, outputs, workspaces) are allocated once here with torch
 (caller-side allocation); `run()` only enqueues C-ABI calls.
 
-Layers of one step depend on one another only through indices: a Reindex layer needs the
-candidate pool of the first Full layer (complete before that layer's own position selection,
-which csa2_index_score_topk_pool marks with an event), a Reuse layer the indices of the layer it
-reuses, and every attention the new rows in the cache.  With several layers `run()` therefore
-gives each layer its own stream (layer 0 on the caller's, the new rows' quantisation on one more)
-and orders them by events along exactly those dependencies, so the other layers' selections and
-attentions overlap.  Each layer then has its own workspaces.  `concurrent=False` issues the same
-calls one after another on one stream.
+Order of the calls.  In a decoder, layer i+1's index and attention queries are computed from
+layer i's output, so `run()` issues the layers one after another, in the model's order, on the
+caller's stream.  The one overlap it uses is the quantisation of the new rows, which runs on a
+second stream beside layer 0's selection (the indexer does not read the main-KV cache) and is
+waited for before the first attention.
+
+`overlap_layers=True` is for callers whose layer inputs are all known before the step (as in
+this synthetic step, or layers of independent requests): the layers' calls then depend on one
+another only through indices -- a Reindex layer needs the candidate pool of the first Full layer
+(complete before that layer's own position selection, which csa2_index_score_topk_pool marks
+with an event), a Reuse layer the indices of the layer it reuses -- and each layer runs on its
+own stream, ordered by events along exactly those dependencies, with its own workspaces.
 """
 from __future__ import annotations
 
@@ -48,7 +52,7 @@ class _Arena:
 
 
 class Step:
-    def __init__(self, inputs: dict, device="cuda", build_cache=True, concurrent=True):
+    def __init__(self, inputs: dict, device="cuda", build_cache=True, overlap_layers=False):
         self.inp = inputs
         self.w = w = inputs["workload"]
         self.dev = device
@@ -112,20 +116,20 @@ class Step:
             if L["mode"] in ("full", "reindex"):
                 last = i
             self.src.append(last)
-        self.concurrent = concurrent and len(self.layers) > 1
+        self.overlap_layers = overlap_layers and len(self.layers) > 1
+        self.qstream = torch.cuda.Stream(device=dev)
+        self.ev_start = torch.cuda.Event()
+        self.ev_ready = torch.cuda.Event()
         self.side = []
-        if self.concurrent:
+        if self.overlap_layers:
             self.side = [torch.cuda.Stream(device=dev) for _ in self.layers[1:]]
-            self.qstream = torch.cuda.Stream(device=dev)
-            self.ev_start = torch.cuda.Event()
-            self.ev_ready = torch.cuda.Event()
             self.ev_pool = torch.cuda.Event()
             self.ev_pool.record()  # creates the event, which the C ABI records into
             self.ev_idx = [torch.cuda.Event() for _ in self.layers]
             self.ev_done = [torch.cuda.Event() for _ in self.layers]
         for i, L in enumerate(self.layers):
             if "idx" in L:
-                L["ws_index"] = (csa2.workspace(ws, dev) if self.concurrent and i > 0
+                L["ws_index"] = (csa2.workspace(ws, dev) if self.overlap_layers and i > 0
                                  else self.ws_index)
         self.ws_pool = (csa2.workspace(csa2.csa2_hier_candidate_pool_workspace_size(
             self.nq, nb, w.n_pool_blocks), dev) if hier else None)
@@ -135,7 +139,8 @@ class Step:
             ws_a = csa2.csa2_sparse_attn_decode_workspace_size(self.nq, w.H, w.topk)
         self.ws_attn = csa2.workspace(ws_a, dev)
         for i, L in enumerate(self.layers):
-            L["ws_attn"] = csa2.workspace(ws_a, dev) if self.concurrent and i > 0 else self.ws_attn
+            L["ws_attn"] = (csa2.workspace(ws_a, dev) if self.overlap_layers and i > 0
+                            else self.ws_attn)
 
     def drop_source_rows(self):
         """Free the bf16 rows the cache was quantised from (the step only reads the new rows)."""
@@ -185,17 +190,18 @@ class Step:
         """One step: quantise the new rows, then every layer (see the module docstring for the
         order of the calls)."""
         main = stream if stream is not None else torch.cuda.current_stream()
-        if not self.concurrent:
-            self.quantize_new_rows(main)
-            for i, L in enumerate(self.layers):
-                self._select(i, L, main)
-                self.attend(L, self.layers[self.src[i]]["idx"], stream=main)
-            return
         # the new rows go into the cache beside layer 0's selection (which does not read it)
         self.ev_start.record(main)
         self.qstream.wait_event(self.ev_start)
         self.quantize_new_rows(self.qstream)
         self.ev_ready.record(self.qstream)
+        if not self.overlap_layers:
+            for i, L in enumerate(self.layers):
+                self._select(i, L, main)
+                if i == 0:
+                    main.wait_event(self.ev_ready)
+                self.attend(L, self.layers[self.src[i]]["idx"], stream=main)
+            return
         streams = [main] + self.side
         for i, L in enumerate(self.layers):
             s = streams[i]

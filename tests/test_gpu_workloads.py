@@ -115,15 +115,15 @@ def test_workload_full_size(mods, name):
 
 
 @pytest.mark.parametrize("B,L", [(1, 65536), (3, 40000)])
-def test_concurrent_layers_match_serial(mods, B, L):
+def test_overlapped_layers_match_model_order(mods, B, L):
     """The hierarchical decoder's layers on their own streams (ordered by events along the
     pool and index dependencies), run directly and as a replayed CUDA graph, give bit for bit
-    what the same calls give one after another on one stream."""
+    what the model-order step gives."""
     step, synth = mods
     w = synth.scaled(synth.WORKLOADS["hier_decode_l1m"], B=B, L=(L,) * B)
     inp = synth.make_inputs(w)
-    ser = step.Step(inp, concurrent=False)
-    con = step.Step(inp, concurrent=True)
+    ser = step.Step(inp)
+    con = step.Step(inp, overlap_layers=True)
     assert not ser.side and len(con.side) == len(w.modes) - 1
     ser.run()
     torch.cuda.synchronize()
