@@ -4,6 +4,15 @@
 // One warp per row, one lane per 16-channel group (a 512-channel row is exactly 32 groups, so a
 // warp moves 1 KB in with two 16-byte loads per lane and 256 + 32 bytes out with one 8-byte and
 // one 1-byte store per lane, all coalesced).  HBM-bound: 1024 B read + 288 B written per row.
+//
+// The code of x is E2M1(fp32(x / s)) rounded to nearest even.  It is computed without the
+// division: x is bf16 (8 significant bits) and s an E4M3 value (4), so x / s either equals a
+// decision point T (a midpoint between E2M1 neighbours: 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) or
+// differs from it by more than 2^-11 relative -- far more than one fp32 rounding -- and T * s
+// (at most 7 significant bits) is exact in fp32.  So comparing |x| with T * s takes exactly the
+// decision the rounded quotient takes, ties included.  Three comparisons find the code: against
+// 1.75 s, then 0.75 s or 3.5 s (all "at least": the even code wins a tie there), then 0.25 s,
+// 1.25 s, 2.5 s or 5 s ("greater than": the even code is below).
 #include "common.cuh"
 
 namespace csa2 {
@@ -24,12 +33,21 @@ __device__ __forceinline__ uint32_t quant_group16(const uint32_t (&v)[8], uint64
   const float sd = e4m3_to_float(scode);
   uint64_t packed = 0;
   if (sd != 0.0f) {
+    const float t1 = 0.25f * sd, t2 = 0.75f * sd, t3 = 1.25f * sd, t4 = 1.75f * sd;
+    const float t5 = 2.5f * sd, t6 = 3.5f * sd, t7 = 5.0f * sd;
+    uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float q = __fdiv_rn(x[i], sd);
-      const uint32_t code = e2m1_mag_code(fabsf(q)) | ((__float_as_uint(q) >> 28) & 8u);
-      packed |= (uint64_t)code << (4 * i);
+      const float a = fabsf(x[i]);
+      const bool ge4 = a >= t4;
+      const bool ge2 = a >= (ge4 ? t6 : t2);
+      const bool gt1 = a > (ge2 ? (ge4 ? t7 : t3) : (ge4 ? t5 : t1));
+      const uint32_t code = (ge4 ? 4u : 0u) | (ge2 ? 2u : 0u) | (gt1 ? 1u : 0u) |
+                            ((__float_as_uint(x[i]) >> 28) & 8u);
+      if (i < 8) lo |= code << (4 * i);
+      else hi |= code << (4 * (i - 8));
     }
+    packed = ((uint64_t)hi << 32) | lo;
   }
   *codes64 = packed;
   return scode;

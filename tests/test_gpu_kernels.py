@@ -281,8 +281,10 @@ def test_decode_attention(csa2, B, H, n_rows, topk):
         check_attn(ob[b], lh[b], ref[b][0], ref[b][1], oracle.double_to_bf16(ref[b][0]), f"seq {b}")
 
 
-@pytest.mark.parametrize("T,H,topk", [(5, 64, 2048), (3, 16, 100)])
+@pytest.mark.parametrize("T,H,topk", [(5, 64, 2048), (3, 16, 100), (2, 64, 40), (2, 64, 90),
+                                      (3, 32, 200), (2, 64, 4000)])
 def test_prefill_attention(csa2, T, H, topk):
+    """Tile counts from one to 63 (64 rows per tile, ragged last tiles), every 11th slot empty."""
     n_rows = 4000
     x, _, _, _ = _attn_case(1, H, n_rows, topk, T)
     g = torch.Generator().manual_seed(T + 7)
