@@ -118,11 +118,21 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
       tma_load_2d(sm + kOffQ + kc * kQChunkBytes, &qmap, &ms.bar_q, kc * 64, n * H + h0);
   }
   // the 32 rows as 32 x 18 16-byte cp.async copies (256 B codes + 32 B scales per row) spread
-  // over all threads; an empty slot is a zero row (value 0, never NaN), masked in the softmax
-  for (int i = tid; i < kAttTS * 18; i += kAttThreads) {
+  // over all threads; an empty slot is a zero row (value 0, never NaN), masked in the softmax.
+  // A thread's row numbers are all loaded first, so their latencies overlap.
+  constexpr int kCopies = kAttTS * 18, kIters = (kCopies + kAttThreads - 1) / kAttThreads;
+  int rr[kIters];
+#pragma unroll
+  for (int k = 0; k < kIters; ++k) {
+    const int i = tid + k * kAttThreads, slot = tile * kAttTS + i / 18;
+    rr[k] = (i < kCopies && slot < topk) ? idx[(int64_t)n * topk + slot] : -1;
+  }
+#pragma unroll
+  for (int k = 0; k < kIters; ++k) {
+    const int i = tid + k * kAttThreads;
+    if (i >= kCopies) break;
     const int j = i / 18, part = i - j * 18;
-    const int slot = tile * kAttTS + j;
-    const int r = slot < topk ? idx[(int64_t)n * topk + slot] : -1;
+    const int r = rr[k];
     if (part == 0) ms.slot_ok[j] = r >= 0;
     uint8_t *dst = part < 16 ? sm + kOffRawC + j * 256 + part * 16
                              : sm + kOffRawS + j * 32 + (part - 16) * 16;
