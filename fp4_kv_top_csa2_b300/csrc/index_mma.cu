@@ -171,12 +171,18 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_mma_kernel(
           if (MODE == kScan) {
             tma_load_2d(sm.keys[s], &kmap, &sm.full[s], 0, (int32_t)(base + (int64_t)t * kTileKeys));
           } else {
+            // the tile's block ids first (independent loads, one latency), then its boxes
             const int32_t *cand = p.cand + (int64_t)c.n * p.n_cand;
-#pragma unroll 1
+            int blk[kTileKeys / kBlock];
+#pragma unroll
             for (int b = 0; b < kTileKeys / kBlock; ++b) {
               const int cb = t * (kTileKeys / kBlock) + b;
-              const int blk = cb < p.n_cand ? cand[cb] : -1;
-              const int32_t row = blk >= 0 ? (int32_t)(base + (int64_t)blk * kBlock) : -kBlock;
+              blk[b] = cb < p.n_cand ? __ldg(cand + cb) : -1;
+            }
+#pragma unroll
+            for (int b = 0; b < kTileKeys / kBlock; ++b) {
+              const int32_t row =
+                  blk[b] >= 0 ? (int32_t)(base + (int64_t)blk[b] * kBlock) : -kBlock;
               tma_load_2d(sm.keys[s] + b * kBlock * kKeyRowBytes, &kmap, &sm.full[s], 0, row);
             }
           }
