@@ -53,15 +53,6 @@ __device__ __forceinline__ uint32_t float_to_e4m3_sat(float s) {
   return (((exp - 120u) << 3) | r) + up;
 }
 
-// |q| -> E2M1 magnitude code, round to nearest even, saturating at 6.  Decision points are the
-// midpoints between neighbours; at a midpoint the even code (mantissa bit 0) wins, which is why
-// some comparisons are strict and some are not.
-__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
-  return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-         (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
-         (uint32_t)(a > 5.0f);
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

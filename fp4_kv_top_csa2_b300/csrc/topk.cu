@@ -5,26 +5,31 @@
 // pool (blocks ranked by the largest index score inside them, "DeepSeek V4.1-Flash", aiwiki.ai,
 // section "Compressed Sparse Attention 2") and Reindex selection.
 //
-// Keys are order-preserving 32-bit images of the scores (key 0 = not a candidate).  The k-th
-// largest key T is built three bits per round: each round counts, in one pass, how many keys
-// are >= each of the 7 possible extensions of the current prefix, and keeps the largest one
-// with at least k keys (11 rounds, block-wide counts, no atomics).  need_eq = k - #(keys > T)
-// equal keys are taken, the lowest positions first.  The output is an ordered emission: every
-// warp owns a contiguous segment, counts its selections with ballots, one scan gives each warp
-// its offset, and a second sweep writes positions in index order (no sort).
+// Keys are order-preserving 32-bit images of the scores (key 0 = not a candidate).  Every kernel
+// finds the k-th largest key T, takes every key > T and the need_eq = k - #(keys > T) keys equal
+// to T with the lowest positions, and emits in index order: each warp owns a contiguous
+// segment, counts its selections with ballots, one scan gives each warp its offset, and a
+// second sweep writes positions (no sort).  T comes from radix11_kth: 11-bit digits, a shared
+// histogram per digit and a block scan, finished by a single warp ranking the keys once no more
+// than 32 remain in play.
 //
-// Where the data lives:
-//   * n <= 16,384 elements: copied once into shared memory (key, position), then everything
-//     runs there.
-//   * larger n: a strided sample of 8,192 keys gives a threshold T_est expected to keep about
-//     1.6 K elements.  One sweep appends every candidate with key >= T_est to its warp's 512
-//     shared-memory slots (index order), the slots are compacted, and the selection finishes
-//     there.  The true Top-K (ties included) is inside that set whenever it holds at least K
-//     elements; if the estimate misses (fewer than K kept, or a warp's slots overflow) the
-//     selection runs over global memory instead.
-// The three ways an element can be addressed (block maxima by index; candidate slots through
-// a block list with slot-indexed or position-indexed scores) are separate kernel instances, so
-// every global load is straight-line code with clamped indices and validity as a mask.
+// Kernels, by size (launch_topk picks one):
+//   * topk_reg_kernel -- n <= 16,384 elements, any number of queries, one 1024-thread CTA per
+//     query.  The elements stay in registers (16 per thread).  A threshold from the exact rank
+//     of 128 sampled keys keeps a little over k candidates, which are compacted in index order
+//     into shared memory; the selection runs on them.
+//   * topk_filter_kernel + topk_select_kernel -- larger n, at most 64 queries (the decoder's
+//     131,072 block maxima): one filter CTA per 4,096-element chunk keeps the (key, position)
+//     pairs at or above a threshold from the exact rank of 256 strided samples (the same in
+//     every CTA); one select CTA per query gathers the kept lists and selects.
+//   * topk_kernel -- larger n with many queries (chunked prefill): one CTA per query; up to
+//     16,384 elements staged in shared memory, else a strided sample of 8,192 keys gives an
+//     estimate T_est (kth_radix, 8-bit digits) and the keys >= T_est are staged instead.
+// A sampled threshold that keeps fewer than k elements (or more than the staging room) falls
+// back to selecting over all elements, so every path is exact.  The three ways an element can
+// be addressed (block maxima by index; candidate slots through a block list with slot-indexed
+// or position-indexed scores) are separate kernel instances, so every global load is
+// straight-line code with clamped indices and validity as a mask.
 #include "common.cuh"
 
 namespace csa2 {
