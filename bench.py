@@ -175,6 +175,18 @@ class ClockSampler:
                 "source": "nvml" if self.nvml else "nvidia-smi"}
 
 
+def slowest(seconds, world, device):
+    """The job's time for a step every rank ran: the largest over ranks (all-reduce MAX; a no-op
+    on one rank).  `device` is where the collective's tensor lives (CUDA for NCCL, CPU for gloo)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(seconds)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        seconds = float(t.item())
+    return seconds
+
+
 # ------------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------------
@@ -224,11 +236,7 @@ def run_ours(args, rank, world):
     assert csa2.kernel_launches() == launches0  # replays enqueue no new host-side launches
     launches = launches_per_step * args.steps
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest(sum(step_ms) / len(step_ms), world, dev)
     by = st.algorithmic_bytes()
     tokens_per_s = world * w.B / (ms / 1e3)
     step_gbs = by["total"] / (ms / 1e3) / 1e9
@@ -244,8 +252,8 @@ def run_ours(args, rank, world):
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
 
     # end to end through the C ABI with host buffers (direct calls, no graph), and with the graph
-    e2e = run_e2e(st, args.steps, dev, graph=False)
-    e2e_graph = run_e2e(st, args.steps, dev, graph=True)
+    e2e = run_e2e(st, args.steps, dev, world, graph=False)
+    e2e_graph = run_e2e(st, args.steps, dev, world, graph=True)
     clk.stop()
 
     line = {
@@ -331,12 +339,13 @@ def profile_calls(st, steps, flush):
     return out
 
 
-def run_e2e(st, steps, dev, graph=False):
+def run_e2e(st, steps, dev, world=1, graph=False):
     """Same step through the C ABI, inputs copied from pinned host memory each step and the
     attention outputs read back, all inside the timed region.  The step's per-token inputs
     (new rows, every layer's queries and weights) sit in one device arena and its outputs in
     another, so each direction is one copy.  graph=True replays the captured step between the
-    copies instead of issuing the calls one by one."""
+    copies instead of issuing the calls one by one.  With several ranks the job's rate is the
+    tokens of all ranks over the slowest rank's time."""
     import torch
     host_in = st.in_arena.buf.cpu().pin_memory()
     host_out = torch.empty_like(st.out_arena.buf, device="cpu").pin_memory()
@@ -357,8 +366,8 @@ def run_e2e(st, steps, dev, graph=False):
     for _ in range(steps):
         one()
     torch.cuda.synchronize()
-    dt = (time.perf_counter() - t0) / steps
-    return {"value": round(st.w.B / dt, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    dt = slowest((time.perf_counter() - t0) / steps, world, dev)
+    return {"value": round(world * st.w.B / dt, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 4),
             "path": "graph replay" if graph else "direct C-ABI calls"}
 
