@@ -135,6 +135,7 @@ def _run_index(csa2, k, q, w, cu, vis, dtype, topk, cand=None, bm=None):
     (1, 8, [5, 3001, 20000], 2048, 0.0),
     (1, 8, [9000, 40000], 100, 0.1),
     (1, 8, [17000], 1, 0.1),
+    (1, 8, [20000, 4100], 4096, 0.0),  # largest topk
     (0, 4, [4096, 700], 512, 0.0),
     (1, 16, [3000], 3000, 0.0),
 ])
@@ -255,7 +256,10 @@ def _attn_case(B, H, n_rows, topk, seed, holes=True):
 
 @pytest.mark.parametrize("B,H,n_rows,topk", [(3, 64, 3000, 2048), (2, 64, 4000, 2048),
                                               (2, 16, 600, 512), (1, 64, 100, 33),
-                                              (4, 64, 50, 1)])
+                                              (4, 64, 50, 1),
+                                              (2, 128, 3000, 1024),   # H > 64: CUDA-core kernel
+                                              (1, 80, 500, 300),
+                                              (1, 64, 20000, 16384)])  # largest topk
 def test_decode_attention(csa2, B, H, n_rows, topk):
     """Batches of 1 to 4 sequences, 16 or 64 heads, Top-K 1 to 2,048 with empty slots (and one
     sequence with none).  Two calls on one workspace must give the same result."""
@@ -282,7 +286,7 @@ def test_decode_attention(csa2, B, H, n_rows, topk):
 
 
 @pytest.mark.parametrize("T,H,topk", [(5, 64, 2048), (3, 16, 100), (2, 64, 40), (2, 64, 90),
-                                      (3, 32, 200), (2, 64, 4000)])
+                                      (3, 32, 200), (2, 64, 4000), (2, 128, 300)])
 def test_prefill_attention(csa2, T, H, topk):
     """Tile counts from one to 63 (64 rows per tile, ragged last tiles), every 11th slot empty."""
     n_rows = 4000
