@@ -124,7 +124,8 @@ class Step:
         if self.overlap_layers:
             self.side = [torch.cuda.Stream(device=dev) for _ in self.layers[1:]]
             self.ev_pool = torch.cuda.Event()
-            self.ev_pool.record()  # creates the event, which the C ABI records into
+            # creates the event on the step's device, where the C ABI records into it
+            self.ev_pool.record(torch.cuda.current_stream(dev))
             self.ev_idx = [torch.cuda.Event() for _ in self.layers]
             self.ev_done = [torch.cuda.Event() for _ in self.layers]
         for i, L in enumerate(self.layers):
