@@ -10,6 +10,7 @@
 import math
 
 import numpy as np
+import pytest
 import torch
 
 import oracle
@@ -79,3 +80,67 @@ def test_prefill_fp4_representable_query_equals_decode():
     pre = oracle.sparse_attn_prefill(qb[None], np.zeros(1, np.int32), codes, sf, cu, idx, 0.05)
     dec = oracle.sparse_attn_decode(qb[None], codes, sf, cu, idx, 0.05)
     assert np.array_equal(pre[0][0], dec[0][0]) and np.array_equal(pre[0][1], dec[0][1])
+
+
+# ------------------------------------------------------------------------------------------------
+# The prefill query is quantised to FP4 (16-channel E4M3 scales, E2M1 values) before the product.
+# A query row built from the hand-worked groups of tests/golden/kv_quant_rows.txt (cases A-E: a
+# tie to the even code, a scale that rounds up, a group that flushes to zero) is not
+# FP4-representable; its quantised value comes from the worked codes, decoded with the OCP
+# definitions (E2M1 magnitudes written out, E4M3 through torch's float8_e4m3fn).
+# ------------------------------------------------------------------------------------------------
+import os
+
+_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _golden_query_row():
+    path = os.path.join(os.path.dirname(__file__), "golden", "kv_quant_rows.txt")
+    x = np.zeros(512)
+    qhat = np.zeros(512)
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        _, g, xs, sf, by = line.split()
+        g = int(g.split("=")[1])
+        x[16 * g:16 * g + 16] = [float(v) for v in xs.split("=")[1].split(",")]
+        s = float(torch.tensor([int(sf.split("=")[1], 16)], dtype=torch.uint8)
+                  .view(torch.float8_e4m3fn).to(torch.float64))
+        for j, b in enumerate(int(v, 16) for v in by.split("=")[1].split(",")):
+            for c, code in ((2 * j, b & 15), (2 * j + 1, b >> 4)):
+                qhat[16 * g + c] = (-1 if code & 8 else 1) * _E2M1[code & 7] * s
+    return x, qhat
+
+
+def _check_query_quant(fn):
+    x, qhat = _golden_query_row()
+    rows = np.stack([x, -x, 2.0 * x])  # three (token, head) rows: sign and scale change
+    qb = torch.from_numpy(rows).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = fn(qb)
+    assert np.array_equal(got[0], qhat) and np.array_equal(got[1], -qhat)
+    assert np.array_equal(got[2], 2.0 * qhat)
+
+
+def test_prefill_query_is_quantised_to_fp4():
+    x, qhat = _golden_query_row()
+    assert not np.array_equal(x, qhat)  # the row is not FP4-representable
+    _check_query_quant(oracle.quantize_query_fp4)
+    # prefill attention uses the quantised query: it equals decode attention on q-hat, and
+    # differs from decode attention on the raw query
+    n = 64
+    codes, sf, _ = _cache(n, 8)
+    idx = np.arange(n, dtype=np.int32)[None, :]
+    cu = np.array([0, n])
+    qb = torch.from_numpy(np.stack([x, 2 * x])).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    qh = torch.from_numpy(np.stack([qhat, 2 * qhat])).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    pre = oracle.sparse_attn_prefill(qb[None], np.zeros(1, np.int32), codes, sf, cu, idx, 0.5)
+    dec_hat = oracle.sparse_attn_decode(qh[None], codes, sf, cu, idx, 0.5)
+    dec_raw = oracle.sparse_attn_decode(qb[None], codes, sf, cu, idx, 0.5)
+    assert np.array_equal(pre[0][0], dec_hat[0][0]) and np.array_equal(pre[0][1], dec_hat[0][1])
+    assert not np.array_equal(pre[0][1], dec_raw[0][1])
+
+
+def test_query_quant_pin_catches_a_skipped_quantisation():
+    with pytest.raises(AssertionError):
+        _check_query_quant(lambda qb: oracle.bf16_to_double(qb))

@@ -89,3 +89,70 @@ def test_bf16_rounding_matches_torch():
     ref = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     got = oracle.double_to_bf16(x.numpy().astype(np.float64))
     assert np.array_equal(ref, got)
+
+
+# ------------------------------------------------------------------------------------------------
+# One-step rounding of doubles to bf16.  The oracle's attention result is a double; it is rounded
+# to bf16 once.  Going double -> float -> bf16 instead rounds twice, and a double just above or
+# below a bf16 midpoint is then pulled onto the midpoint by the first rounding and sent to the
+# even neighbour by the second.  The expected bits come from exact rational arithmetic.
+# ------------------------------------------------------------------------------------------------
+def _bf16_exact(x: float) -> int:
+    """Round the double x to bf16 (8 significant bits, ties to even, subnormal quantum 2^-133,
+    overflow to inf) with Python fractions; returns the 16-bit pattern."""
+    from fractions import Fraction
+    import struct
+    if x == 0.0:
+        return 0x8000 if math.copysign(1.0, x) < 0 else 0
+    f = Fraction(abs(x))
+    e = math.floor(math.log2(abs(x)))
+    while Fraction(2) ** e > f:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= f:
+        e += 1
+    q = Fraction(2) ** (max(e, -126) - 7)
+    n = f / q
+    lo = n.numerator // n.denominator
+    rem = n - lo
+    r = lo + (1 if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and lo % 2 == 1) else 0)
+    val = r * q
+    if val >= Fraction(2) ** 128:
+        bits = 0x7F80
+    else:
+        bits = struct.unpack("<I", struct.pack("<f", float(val)))[0] >> 16
+    return bits | (0x8000 if x < 0 else 0)
+
+
+def _near_midpoints():
+    """Doubles within 2^-40 (relative) of bf16 midpoints, on both sides, over the normal and the
+    subnormal range; none of them is an fp32 value."""
+    rng = np.random.default_rng(11)
+    xs = []
+    for e in list(range(-140, 128, 7)) + [-133, -127, -126, 0, 127]:
+        for _ in range(6):
+            m = int(rng.integers(0, 128)) if e < -126 else int(rng.integers(128, 256))
+            mid = (m + 0.5) * 2.0 ** (max(e, -126) - 7 if e >= -126 else -133)
+            for s in (1.0, -1.0):
+                for d in (2.0 ** -40, -(2.0 ** -40)):
+                    xs.append(s * mid * (1.0 + d))
+    return np.array(xs, dtype=np.float64)
+
+
+def _check_double_to_bf16(fn):
+    x = _near_midpoints()
+    assert not np.any(x.astype(np.float32).astype(np.float64) == x)  # none is an fp32 value
+    want = np.array([_bf16_exact(v) for v in x], dtype=np.uint16)
+    got = np.asarray(fn(x), dtype=np.uint16)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{bad.size} of {x.size} wrong, e.g. {x[bad[:3]]}"
+
+
+def test_bf16_rounding_of_doubles_is_one_step():
+    _check_double_to_bf16(oracle.double_to_bf16)
+
+
+def test_bf16_rounding_pin_catches_double_rounding():
+    def twice(x):  # the plausible mistake: double -> float -> bf16
+        return torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    with pytest.raises(AssertionError):
+        _check_double_to_bf16(twice)
