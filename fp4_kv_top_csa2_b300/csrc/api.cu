@@ -99,14 +99,15 @@ ScoreWs score_ws(void *base, int nq, int64_t max_vis, int n_cand_blocks, int top
   return w;
 }
 
-// csa2_index_score_topk and csa2_index_score_topk_pool (n_pool > 0: Full mode with the pool).
-int index_score_topk_impl(const void *q_idx, int q_dtype, const float *w, int nq, int Hi, int Di,
-                          const void *k_idx, int k_dtype, int64_t k_rows, const float *k_scale,
-                          const int64_t *cu_ctx, int B, const int32_t *q_seq,
-                          const int32_t *q_vis, int64_t max_vis, const int32_t *cand_blocks,
-                          int n_cand_blocks, int topk, int32_t *out_idx, float *out_block_max,
-                          int n_pool, int32_t *out_pool, void *workspace, size_t ws_bytes,
-                          void *stream, void *pool_event = nullptr) {
+// Argument checks shared by every indexer entry point (with or without a workspace): ranges,
+// dtype / Di pairs, the Reindex / Full / pool combinations, null and 16-byte alignment checks.
+// CSA2_OK with nq == 0 means "nothing to enqueue".
+int index_args_ok(const void *q_idx, int q_dtype, const float *w, int nq, int Hi, int Di,
+                  const void *k_idx, int k_dtype, int64_t k_rows, const float *k_scale,
+                  const int64_t *cu_ctx, int B, const int32_t *q_seq, const int32_t *q_vis,
+                  int64_t max_vis, const int32_t *cand_blocks, int n_cand_blocks, int topk,
+                  const int32_t *out_idx, const float *out_block_max, int n_pool,
+                  const int32_t *out_pool) {
   if (nq < 0 || nq > 65535 || B < 1 || Hi < 1 || Hi > 16 || topk < 1 || topk > 4096 ||
       max_vis < 0 || max_vis > (int64_t)1 << 30 || k_rows < 0 || k_rows > INT32_MAX)
     return CSA2_ERR_INVALID_ARG;
@@ -117,10 +118,7 @@ int index_score_topk_impl(const void *q_idx, int q_dtype, const float *w, int nq
                   : (n_cand_blocks != 0))
     return CSA2_ERR_INVALID_ARG;
   if (n_pool < 0 || n_pool > 4096 || (n_pool > 0 && cand_blocks)) return CSA2_ERR_INVALID_ARG;
-  if (nq == 0)  // nothing to select; the (empty) pool is complete
-    return pool_event ? cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(pool_event),
-                                                    static_cast<cudaStream_t>(stream)))
-                      : CSA2_OK;
+  if (nq == 0) return CSA2_OK;
   if (!q_idx || !w || !k_idx || !cu_ctx || !q_seq || !q_vis || !out_idx ||
       (n_pool > 0 && !out_pool))
     return CSA2_ERR_INVALID_ARG;
@@ -128,6 +126,47 @@ int index_score_topk_impl(const void *q_idx, int q_dtype, const float *w, int nq
                         cand_blocks, out_idx, out_block_max, out_pool};
   for (const void *p : ptrs)
     if (!aligned16(p)) return CSA2_ERR_INVALID_ARG;
+  return CSA2_OK;
+}
+
+// Reindex mode: score the listed blocks' positions into `scores` ([nq, n_cand_blocks * 8]),
+// then select.  topk_ws may be null (the selection then takes its one-CTA-per-query path,
+// which selects exactly the same set).  Shared by csa2_index_score_topk and the entry point
+// without a workspace, so both score and select the same way.
+cudaError_t reindex_launch(const void *q_idx, int q_dtype, const float *w, int nq, int Hi,
+                           int Di, const void *k_idx, int64_t k_rows, const float *k_scale,
+                           const int64_t *cu_ctx, const int32_t *q_seq, const int32_t *q_vis,
+                           const int32_t *cand_blocks, int n_cand_blocks, int topk,
+                           int32_t *out_idx, float *scores, void *topk_ws, cudaStream_t st) {
+  cudaError_t e =
+      cand_mma_supported()
+          ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx,
+                                  q_seq, q_vis, cand_blocks, n_cand_blocks, scores, st)
+          : launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq,
+                              q_vis, cand_blocks, n_cand_blocks, scores, st);
+  if (e == cudaSuccess)
+    e = launch_topk(scores, (int64_t)n_cand_blocks * kBlock, (int64_t)n_cand_blocks * kBlock,
+                    cand_blocks, n_cand_blocks, 1, q_vis, nq, topk, out_idx, st, nullptr, 0,
+                    topk_ws);
+  return e;
+}
+
+// csa2_index_score_topk and csa2_index_score_topk_pool (n_pool > 0: Full mode with the pool).
+int index_score_topk_impl(const void *q_idx, int q_dtype, const float *w, int nq, int Hi, int Di,
+                          const void *k_idx, int k_dtype, int64_t k_rows, const float *k_scale,
+                          const int64_t *cu_ctx, int B, const int32_t *q_seq,
+                          const int32_t *q_vis, int64_t max_vis, const int32_t *cand_blocks,
+                          int n_cand_blocks, int topk, int32_t *out_idx, float *out_block_max,
+                          int n_pool, int32_t *out_pool, void *workspace, size_t ws_bytes,
+                          void *stream, void *pool_event = nullptr) {
+  if (int r = index_args_ok(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_dtype, k_rows, k_scale, cu_ctx,
+                            B, q_seq, q_vis, max_vis, cand_blocks, n_cand_blocks, topk, out_idx,
+                            out_block_max, n_pool, out_pool))
+    return r;
+  if (nq == 0)  // nothing to select; the (empty) pool is complete
+    return pool_event ? cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(pool_event),
+                                                    static_cast<cudaStream_t>(stream)))
+                      : CSA2_OK;
   if (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) return CSA2_ERR_INVALID_ARG;
   ScoreWs need = score_ws(nullptr, nq, max_vis, n_cand_blocks, topk, n_pool);
   if (ws_bytes < need.bytes || (need.bytes && !workspace)) return CSA2_ERR_WORKSPACE;
@@ -136,19 +175,11 @@ int index_score_topk_impl(const void *q_idx, int q_dtype, const float *w, int nq
   ScoreWs ws = score_ws(workspace, nq, max_vis, n_cand_blocks, topk, n_pool);
   const bool mma = index_mma_supported(nq);
   const bool multi = !mma && index_multi_supported(nq, Hi, B);
-  const bool cand_mma = cand_mma_supported();
   cudaError_t e;
-  if (cand_blocks) {  // Reindex: score the listed blocks, select
-    e = cand_mma ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx,
-                                    q_seq, q_vis, cand_blocks, n_cand_blocks, ws.scores, st)
-            : launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq,
-                                q_vis, cand_blocks, n_cand_blocks, ws.scores, st);
-    if (e == cudaSuccess)
-      e = launch_topk(ws.scores, (int64_t)n_cand_blocks * kBlock, (int64_t)n_cand_blocks * kBlock,
-                      cand_blocks, n_cand_blocks, 1, q_vis, nq, topk, out_idx, st, nullptr, 0,
-                      ws.topk);
-    return cuda_status(e);
-  }
+  if (cand_blocks)  // Reindex: score the listed blocks, select
+    return cuda_status(reindex_launch(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_rows, k_scale,
+                                      cu_ctx, q_seq, q_vis, cand_blocks, n_cand_blocks, topk,
+                                      out_idx, ws.scores, ws.topk, st));
   // Full: block maxima over every visible position; the Top-K positions lie inside the Top-K
   // blocks by block maximum (each block ahead of a selected position's block holds a position
   // ranked ahead of it), so select those blocks first, then select among their positions.  A

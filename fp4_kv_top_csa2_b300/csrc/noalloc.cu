@@ -46,42 +46,23 @@ extern "C" int csa2_index_score_topk_reindex_noalloc(
     const int32_t *q_seq, const int32_t *q_vis, int64_t max_vis, const int32_t *cand_blocks,
     int n_cand_blocks, int topk, int32_t *out_idx, void *stream) {
   using namespace csa2;
-  if (nq < 0 || nq > 65535 || B < 1 || Hi < 1 || Hi > 16 || topk < 1 || topk > 4096 ||
-      max_vis < 0 || max_vis > (int64_t)1 << 30 || k_rows < 0 || k_rows > INT32_MAX ||
-      n_cand_blocks < 1 || n_cand_blocks > 65536)
-    return CSA2_ERR_INVALID_ARG;
-  if (q_dtype != k_dtype) return CSA2_ERR_INVALID_ARG;
-  if (!((q_dtype == CSA2_BF16 && Di == 64) || (q_dtype == CSA2_E4M3 && Di == 128)))
-    return CSA2_ERR_INVALID_ARG;
+  // the same checks as csa2_index_score_topk in Reindex mode
+  if (n_cand_blocks < 1) return CSA2_ERR_INVALID_ARG;
+  if (int r = index_args_ok(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_dtype, k_rows, k_scale, cu_ctx,
+                            B, q_seq, q_vis, max_vis, cand_blocks, n_cand_blocks, topk, out_idx,
+                            nullptr, 0, nullptr))
+    return r;
   if (nq == 0) return CSA2_OK;
-  if (!q_idx || !w || !k_idx || !cu_ctx || !q_seq || !q_vis || !cand_blocks || !out_idx)
-    return CSA2_ERR_INVALID_ARG;
-  const void *ptrs[] = {q_idx, w, k_idx, k_scale, cu_ctx, q_seq, q_vis, cand_blocks, out_idx};
-  for (const void *p : ptrs)
-    if (reinterpret_cast<uintptr_t>(p) & 15u) return CSA2_ERR_INVALID_ARG;
   const int64_t slots = (int64_t)nq * n_cand_blocks * kBlock;
   if (slots > kNoAllocSlots) return CSA2_ERR_WORKSPACE;  // beyond the static scratch
-  {
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return CSA2_ERR_CUDA;
-    if (major != 10 || minor != 3) return CSA2_ERR_UNSUPPORTED;
-  }
+  if (int r = check_device()) return r;
   float *scores = nullptr;
   if (noalloc_scratch(&scores) != cudaSuccess) return CSA2_ERR_CUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   // Every slot the selection reads is written by the scoring kernel of the same call, so the
-  // scratch needs no clearing between calls.
-  cudaError_t e = index_mma_supported(nq)
-                      ? launch_score_cand_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale,
-                                              cu_ctx, q_seq, q_vis, cand_blocks, n_cand_blocks,
-                                              scores, st)
-                      : launch_score_cand(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx,
-                                          q_seq, q_vis, cand_blocks, n_cand_blocks, scores, st);
-  if (e == cudaSuccess)
-    e = launch_topk(scores, (int64_t)n_cand_blocks * kBlock, (int64_t)n_cand_blocks * kBlock,
-                    cand_blocks, n_cand_blocks, 1, q_vis, nq, topk, out_idx, st);
-  return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+  // scratch needs no clearing between calls.  The selection runs without a workspace: for
+  // pools over 2,048 blocks it takes the one-CTA-per-query path, which selects exactly the set
+  // the workspace version's two-kernel path selects.
+  return cuda_status(reindex_launch(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_rows, k_scale, cu_ctx,
+                                    q_seq, q_vis, cand_blocks, n_cand_blocks, topk, out_idx,
+                                    scores, nullptr, static_cast<cudaStream_t>(stream)));
 }
