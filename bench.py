@@ -30,6 +30,11 @@ HEADLINE = "hier_decode_l1m"
 PREFILL = "prefill_t4096_p262144"
 METRIC = "sparse-attn decode tokens/s + HBM GB/s vs 8 TB/s at 1M ctx; prefill TFLOP/s"
 HBM_TARGET_GBS = 8000.0
+DECODE_CONFIGS = ("decode_b1_l4096_bf16idx", "decode_b8_l65536", "decode_ragged_b32")
+# DRAM bytes (read + write) of one launch of the Full scan as csa2_index_block_max runs it, from
+# one ncu capture (profiles/index_mma_scan_hier_decode_l1m.md); None when the kernel has changed
+# since.
+SCAN_TRAFFIC = None
 ROOT = os.path.dirname(os.path.abspath(__file__))
 
 
@@ -243,14 +248,14 @@ def run_ours(args, rank, world):
 
     # per-call device times: each call captured as its own graph, replayed with events
     parts = profile_calls(st, args.steps, flush)
-    dom_name, dom_ms, dom_bytes = ("csa2_index_score_topk_pool (Full + pool, 1,048,576 keys)",
-                                   parts["full_index"], by["index_keys_full"])
-    # DRAM bytes (read + write) of that call's kernels in one ncu capture of the current code:
-    # scan 134.27 + 4.31 MB, pool filter 0.55 MB, pool select 0.11 MB, position Top-K 0.33 MB.
-    # Reset to None whenever those kernels change.
-    dom_traffic = 139_563_264
-    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-
+    # The dominant kernel is the Full layer's scan (134 MB of the step's 145 MB of algorithmic
+    # bytes).  Its own time: csa2_index_block_max (that scan alone, one launch) captured as its
+    # own graph and replayed between events, L2 flushed before each replay.
+    full = next(L for L in st.layers if L["mode"] == "full")
+    scan_ms = time_graph(lambda s: st.block_max(full, st.bm, stream=s), args.steps, flush)
+    dom_bytes = by["index_keys_full"]
+    achieved = dom_bytes / (scan_ms / 1e3) / 1e9
+    call_gbs = dom_bytes / (parts["full_index"] / 1e3) / 1e9
     # end to end through the C ABI with host buffers (direct calls, no graph), and with the graph
     e2e = run_e2e(st, args.steps, dev, world, graph=False)
     e2e_graph = run_e2e(st, args.steps, dev, world, graph=True)
@@ -269,17 +274,28 @@ def run_ours(args, rank, world):
         "hbm": {"algorithmic_bytes_per_step": by["total"], "gbs": round(step_gbs, 1),
                 "frac_of_8tbs": round(step_gbs / HBM_TARGET_GBS, 4),
                 "frac_of_measured": round(step_gbs / peaks["hbm_gbs"], 4), "bytes_by_part": by},
-        "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "peak_source": peaks["source"] + " (burst copy)", "traffic": dom_traffic,
-                     "ms_per_launch": round(dom_ms, 5), "algorithmic_bytes": dom_bytes},
+        "roofline": {"kernel": "index_mma_kernel<E4M3, SCAN> (Full scan, 1,048,576 keys)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "frac_of_8tbs": round(achieved / HBM_TARGET_GBS, 4),
+                     "peak_source": peaks["source"] + " (burst copy)", "traffic": SCAN_TRAFFIC,
+                     "ms_per_launch": round(scan_ms, 5), "algorithmic_bytes": dom_bytes,
+                     "timed_as": "csa2_index_block_max alone, one CUDA graph per replay, L2 "
+                                 "flushed before each",
+                     "call": {"name": "csa2_index_score_topk_pool (scan + pool + Top-K)",
+                              "ms": round(parts["full_index"], 5), "gbs": round(call_gbs, 1),
+                              "frac": round(call_gbs / peaks["hbm_gbs"], 4)}},
         "breakdown_ms": {k: round(v, 5) for k, v in parts.items()},
         "timing": "step = one CUDA-graph replay of all calls; CUDA events on the launching stream",
         "e2e": e2e, "e2e_graph": e2e_graph, "gpu_launches": launches,
         "gpu_launches_per_step": launches_per_step, "wall_s_timed": round(wall, 4),
         "clocks": clk.summary(tw0, tw1),
     }
+    del st
+    torch.cuda.empty_cache()
+    if args.configs and rank == 0:
+        line["decode_configs"] = {name: run_decode_config(name, args, dev, peaks, flush)
+                                  for name in DECODE_CONFIGS}
     if args.prefill and rank == 0:
         line["prefill"] = run_prefill(args, dev, peaks)
     if rank == 0 and args.cpu_baseline:
@@ -336,6 +352,75 @@ def profile_calls(st, steps, flush):
             torch.cuda.synchronize()
             tms.append(a.elapsed_time(b))
         out[name] = sum(tms) / len(tms)
+    return out
+
+
+def time_graph(fn, steps, flush):
+    """Mean device time (ms) of fn(stream) captured as one CUDA graph and replayed `steps`
+    times between CUDA events on the launching stream, L2 flushed before each replay."""
+    import torch
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+            fn(side)
+    stream.wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    tms = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        tms.append(a.elapsed_time(b))
+    return sum(tms) / len(tms)
+
+
+def run_decode_config(name, args, dev, peaks, flush):
+    """One of the non-hierarchical decode workloads: its whole step (new rows' quantisation,
+    Full selection, attention) as one CUDA graph, timed like the headline step."""
+    import torch
+    from fp4_kv_top_csa2_b300 import synth
+    from fp4_kv_top_csa2_b300.step import Step
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w)
+    st = Step(inp, device=dev)
+    st.drop_source_rows()
+    inp["kv_bf16"] = None
+    launches = launches_of(st)
+    st.capture()
+    for _ in range(args.warmup):
+        st.replay()
+    stream = torch.cuda.current_stream()
+    tms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        st.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        tms.append(a.elapsed_time(b))
+    ms = sum(tms) / len(tms)
+    by = st.algorithmic_bytes()
+    gbs = by["total"] / (ms / 1e3) / 1e9
+    out = {"batch": w.B, "context": (list(inp["lengths"]) if w.ragged else w.L[0]),
+           "context_total": int(sum(inp["lengths"])), "heads": w.H,
+           "indexer": f"{w.Hi}x{w.Di} {'bf16' if w.idx_dtype == 0 else 'e4m3'}", "topk": w.topk,
+           "ms_per_step": round(ms, 5), "tokens_per_s": round(w.B / (ms / 1e3), 1),
+           "algorithmic_bytes_per_step": by["total"], "gbs": round(gbs, 1),
+           "frac_of_8tbs": round(gbs / HBM_TARGET_GBS, 4),
+           "frac_of_measured": round(gbs / peaks["hbm_gbs"], 4), "gpu_launches_per_step": launches,
+           "l2": "flushed between timed steps"}
+    if w.ragged:
+        out["context"] = f"{min(inp['lengths'])}..{max(inp['lengths'])} (ragged, {w.B} sequences)"
+    del st
+    torch.cuda.empty_cache()
     return out
 
 
@@ -403,12 +488,38 @@ def run_prefill(args, dev, peaks):
     f_idx = 2.0 * pairs * w.Hi * w.Di
     f_attn = 4.0 * w.T * w.topk * w.H * 512
     mi, ma, mq = (statistics.median(x) for x in (ti, ta, tq))
+    bf16 = peaks["bf16_tflops"]
+    p_fp8 = 2.0 * bf16  # nominal dense fp8 / bf16 ratio 4.5 / 2.25
+    p_fp4 = 6.0 * bf16  # nominal dense fp4 / bf16 ratio 13.5 / 2.25
+    # Attention's FLOP-weighted peak if QK^T ran as block-scaled FP4 and PV as f16 (half the
+    # FLOPs each): 1 / (0.5 / P_fp4 + 0.5 / P_f16).
+    p_mixed = 1.0 / (0.5 / p_fp4 + 0.5 / bf16)
+    ta_fl = f_attn / (ma / 1e3) / 1e12
+    ti_fl = f_idx / (mi / 1e3) / 1e12
+    src = peaks["source"]
     return {"workload": PREFILL, "tokens": w.T, "cached": P0, "topk": w.topk, "heads": w.H,
             "ms_indexer": round(mi, 4), "ms_attention": round(ma, 4), "ms_kv_quant": round(mq, 4),
-            "indexer_tflops": round(f_idx / (mi / 1e3) / 1e12, 2),
-            "attention_tflops": round(f_attn / (ma / 1e3) / 1e12, 2),
+            "indexer_tflops": round(ti_fl, 2), "attention_tflops": round(ta_fl, 2),
             "tokens_per_s": round(w.T / ((mi + ma + mq) / 1e3), 1),
-            "flops_indexer": f_idx, "flops_attention": f_attn}
+            "flops_indexer": f_idx, "flops_attention": f_attn,
+            "roofline": {
+                "kernel": "csa2_sparse_attn_prefill (FP4 query quantisation + attn_prefill_kernel)",
+                "bound": "tensor", "achieved": round(ta_fl, 1), "peak": bf16, "unit": "TFLOP/s",
+                "frac": round(ta_fl / bf16, 4),
+                "peak_source": f"{src} bf16 burst; the contraction runs as tcgen05 kind::f16, "
+                               "whose dense rate equals bf16's",
+                "frac_of_mixed_fp4_f16_peak": round(ta_fl / p_mixed, 4),
+                "mixed_peak": round(p_mixed, 1),
+                "mixed_peak_source": f"{src} bf16 burst x 6 for QK^T (nominal fp4 / bf16 13.5 / "
+                                     "2.25) and x 1 for PV, weighted by their equal FLOPs",
+                "traffic": None},
+            "indexer_roofline": {
+                "kernel": "csa2_index_score_topk (index_multi_kernel scan + block and position "
+                          "Top-K)",
+                "bound": "tensor", "achieved": round(ti_fl, 1), "peak": round(p_fp8, 1),
+                "unit": "TFLOP/s", "frac": round(ti_fl / p_fp8, 4),
+                "peak_source": f"{src} bf16 burst x 2 (nominal fp8 / bf16 4.5 / 2.25)",
+                "traffic": None}}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -518,6 +629,8 @@ def main():
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--prefill-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip timing the three non-hierarchical decode workloads")
     ap.add_argument("--cpu-steps", type=int, default=2)
     ap.add_argument("--profile-step", default=None,
                     help="run only this workload's step (--steps times) for a profiler capture")
@@ -529,6 +642,16 @@ def main():
         print(json.dumps(profile_step(args.profile_step, args.steps, args.prefill_tokens)),
               flush=True)
         return
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # N replicas, one process per GPU, launched the way the multi-GPU contract runs them
+        import socket
+        with socket.socket() as so:
+            so.bind(("127.0.0.1", 0))
+            port = so.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+               "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        os.execv(sys.executable, cmd)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     sys.path.insert(0, ROOT)

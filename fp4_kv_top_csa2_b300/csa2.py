@@ -38,6 +38,7 @@ def _load() -> ctypes.CDLL:
                                       P, P, SZ, P]),
         "csa2_index_score_topk_reindex_noalloc": (I, [P, I, P, I, I, I, P, I, I64, P, P, I, P, P,
                                                       I64, P, I, I, P, P]),
+        "csa2_index_block_max": (I, [P, I, P, I, I, I, P, I, I64, P, P, I, P, P, I64, P, P]),
         "csa2_index_score_topk_pool_workspace_size": (SZ, [I, I64, I, I]),
         "csa2_index_score_topk_pool": (I, [P, I, P, I, I, I, P, I, I64, P, P, I, P, P, I64, I, P,
                                            P, I, I, P, P, SZ, P, P]),
@@ -127,6 +128,17 @@ def csa2_index_score_topk_reindex_noalloc(q_idx, q_dtype, w, k_idx, cu_ctx, q_se
         _ptr(q_idx), q_dtype, _ptr(w), nq, Hi, Di, _ptr(k_idx), q_dtype, k_idx.shape[0],
         _ptr(k_scale), _ptr(cu_ctx), B, _ptr(q_seq), _ptr(q_vis), max_vis, _ptr(cand_blocks),
         cand_blocks.shape[1], topk, _ptr(out_idx), _stream(stream)))
+
+
+def csa2_index_block_max(q_idx, q_dtype, w, k_idx, cu_ctx, q_seq, q_vis, max_vis, out_block_max,
+                         k_scale=None, stream=None):
+    """Full-mode block maxima only (the scan of csa2_index_score_topk without a selection)."""
+    nq, Hi, Di = q_idx.shape
+    B = cu_ctx.numel() - 1
+    _check("csa2_index_block_max", lib.csa2_index_block_max(
+        _ptr(q_idx), q_dtype, _ptr(w), nq, Hi, Di, _ptr(k_idx), q_dtype, k_idx.shape[0],
+        _ptr(k_scale), _ptr(cu_ctx), B, _ptr(q_seq), _ptr(q_vis), max_vis, _ptr(out_block_max),
+        _stream(stream)))
 
 
 def csa2_index_score_topk_pool_workspace_size(nq, max_vis, topk, n_pool_blocks):

@@ -288,6 +288,35 @@ int csa2_index_score_topk_pool(const void *q_idx, int q_dtype, const float *w, i
                                stream, pool_event);
 }
 
+int csa2_index_block_max(const void *q_idx, int q_dtype, const float *w, int nq, int Hi, int Di,
+                         const void *k_idx, int k_dtype, int64_t k_rows, const float *k_scale,
+                         const int64_t *cu_ctx, int B, const int32_t *q_seq, const int32_t *q_vis,
+                         int64_t max_vis, float *out_block_max, void *stream) {
+  // the Full-mode checks of csa2_index_score_topk; topk plays no part here (1), and the block
+  // maxima, this call's only output, take the place of out_idx in the presence checks
+  if (nq > 0 && !out_block_max) return CSA2_ERR_INVALID_ARG;
+  if (int r = index_args_ok(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_dtype, k_rows, k_scale, cu_ctx,
+                            B, q_seq, q_vis, max_vis, nullptr, 0, 1,
+                            reinterpret_cast<const int32_t *>(out_block_max), out_block_max, 0,
+                            nullptr))
+    return r;
+  if (nq == 0 || max_vis == 0) return CSA2_OK;
+  if (int r = check_device()) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t nb = (max_vis + kBlock - 1) / kBlock;
+  cudaError_t e;
+  if (index_mma_supported(nq))
+    e = launch_score_scan_mma(q_idx, q_dtype, w, nq, Hi, k_idx, k_rows, k_scale, cu_ctx, q_seq,
+                              q_vis, max_vis, out_block_max, nb, nullptr, 0, st);
+  else if (index_multi_supported(nq, Hi, B))
+    e = launch_score_scan_multi(q_idx, q_dtype, w, nq, k_idx, k_rows, k_scale, q_vis, max_vis,
+                                out_block_max, nb, nullptr, 0, st);
+  else
+    e = launch_score_scan(q_idx, q_dtype, w, nq, Hi, Di, k_idx, k_scale, cu_ctx, q_seq, q_vis,
+                          max_vis, out_block_max, nb, st);
+  return cuda_status(e);
+}
+
 size_t csa2_hier_candidate_pool_workspace_size(int nq, int64_t max_blocks, int n_pool_blocks) {
   (void)n_pool_blocks;
   if (nq < 0 || max_blocks < 0) return 0;

@@ -169,6 +169,13 @@ class Step:
                                          self.scale, layer["out"], layer["lse"],
                                          ws=layer["ws_attn"], stream=stream)
 
+    def block_max(self, layer, out, stream=None):
+        """The Full layer's scan alone: block maxima of every visible position into `out`
+        (csa2_index_block_max)."""
+        csa2.csa2_index_block_max(layer["q_idx"], self.w.idx_dtype, layer["w"], self.k_idx,
+                                  self.cu_ctx, self.q_seq, self.q_vis, self.max_vis, out,
+                                  stream=stream)
+
     def index_with_pool(self, layer, stream=None, pool_event=None):
         """The first Full layer of the hierarchical decoder: its selection and the candidate
         pool in one call (csa2_index_score_topk_pool)."""

@@ -158,6 +158,21 @@ int csa2_index_score_topk_reindex_noalloc(const void *q_idx, int q_dtype, const 
                                           const int32_t *cand_blocks, int n_cand_blocks, int topk,
                                           int32_t *out_idx, void *stream);
 
+/*
+ * csa2_index_block_max -- the Full-mode scan alone: block maxima of the index score over every
+ * causally visible position, without a selection.  [WIKI] "Compressed Sparse Attention 2": the
+ * first Full layer of the hierarchical indexer ranks blocks of eight positions by the largest
+ * index score they contain; these maxima are what csa2_hier_candidate_pool ranks.
+ * Arguments as csa2_index_score_topk in Full mode (no topk, cand_blocks or workspace);
+ * out_block_max [nq, ceil(max_vis/8)] fp32 is required and receives exactly the values
+ * csa2_index_score_topk writes there (entries b >= ceil(q_vis[n]/8) are left undefined).
+ * One kernel launch; no scratch memory.
+ */
+int csa2_index_block_max(const void *q_idx, int q_dtype, const float *w, int nq, int Hi, int Di,
+                         const void *k_idx, int k_dtype, int64_t k_rows, const float *k_scale,
+                         const int64_t *cu_ctx, int B, const int32_t *q_seq, const int32_t *q_vis,
+                         int64_t max_vis, float *out_block_max, void *stream);
+
 /* ------------------------------------------------------------------------------------------ */
 /* 3. Hierarchical candidate pool                                                               */
 /* ------------------------------------------------------------------------------------------ */

@@ -154,6 +154,29 @@ def test_full_topk_and_block_max(csa2, dtype, Hi, lengths, topk, dup):
         np.testing.assert_allclose(bmh[n, :nbn], ref[n]["bm"], rtol=2e-6, atol=1e-6)
 
 
+@pytest.mark.parametrize("dtype,Hi,lengths", [(1, 8, [5, 3001, 20000]), (0, 4, [4096, 700]),
+                                              (1, 8, [1 << 17])])
+def test_block_max_call_equals_full_selection_block_max(csa2, dtype, Hi, lengths):
+    """csa2_index_block_max writes the block maxima csa2_index_score_topk writes (bit for bit),
+    which are the oracle's within the fp32 accumulation band."""
+    k, q, w, cu, kn, qn = _index_case(lengths, dtype, Hi, 7 + sum(lengths))
+    vis = list(lengths)
+    nq, max_vis = len(vis), max(vis)
+    nb = (max_vis + 7) // 8
+    bm1 = torch.full((nq, nb), float("nan"), device="cuda")
+    _run_index(csa2, k, q, w, cu, vis, dtype, 64, bm=bm1)
+    bm2 = torch.full((nq, nb), float("nan"), device="cuda")
+    csa2.csa2_index_block_max(q.cuda(), dtype, w.cuda(), k.cuda(), cu.cuda(),
+                              torch.arange(nq, dtype=torch.int32, device="cuda"),
+                              torch.tensor(vis, dtype=torch.int32, device="cuda"), max_vis, bm2)
+    ref = oracle.index_score_topk(qn, dtype, w.numpy(), kn, cu.numpy(), np.arange(nq),
+                                  np.array(vis), 1)
+    for n in range(nq):
+        nbn = (vis[n] + 7) // 8
+        assert torch.equal(bm1[n, :nbn], bm2[n, :nbn])
+        np.testing.assert_allclose(bm2[n, :nbn].cpu().numpy(), ref[n]["bm"], rtol=2e-6, atol=1e-6)
+
+
 def test_full_short_and_empty_visibility(csa2):
     k, q, w, cu, kn, qn = _index_case([1000, 1000, 1000], 1, 8, 5)
     vis = [0, 3, 999]  # nothing visible / fewer candidates than K / ragged
@@ -404,6 +427,34 @@ def test_pool_selection_cluster_sizes(csa2, nb, kind, vis_frac):
         got = pool.cpu().numpy()
         for n in range(B):
             assert np.array_equal(got[n], ref[n]), (n_pool, n)
+
+
+@pytest.mark.parametrize("kind", ["two_values", "all_equal", "one_group"])
+def test_pool_selection_many_queries_global_fallback(csa2, kind):
+    """More than 64 queries over more than 16,384 block maxima each take the one-CTA-per-query
+    selection; with heavy ties the keys at or above its sampled threshold overflow the staging
+    room (or fall short of k), and it selects over global memory instead.  Exact against the
+    oracle on the same fp32 values."""
+    g = torch.Generator().manual_seed({"two_values": 1, "all_equal": 2, "one_group": 3}[kind])
+    nq, nb = 80, 40000
+    if kind == "two_values":     # ~20,000 keys equal the sampled threshold
+        bm = torch.randint(0, 2, (nq, nb), generator=g).float()
+    elif kind == "all_equal":    # every key ties; signed zeros mixed in
+        bm = torch.where(torch.rand(nq, nb, generator=g) < 0.5, 0.0, -0.0)
+    else:                        # a few large values, a plateau of ties below them
+        bm = torch.full((nq, nb), 3.0)
+        hot = torch.rand(nq, nb, generator=g) < 0.02
+        bm[hot] = 5.0 + torch.rand(int(hot.sum()), generator=g)
+    vis = [nb * 8 - 3 * i for i in range(nq)]
+    vis_t = torch.tensor(vis, dtype=torch.int32, device="cuda")
+    bmd = bm.cuda()
+    for n_pool in (2048, 3000):
+        pool = torch.empty((nq, n_pool), dtype=torch.int32, device="cuda")
+        csa2.csa2_hier_candidate_pool(bmd, vis_t, n_pool, pool, ws=_pool_ws(csa2, bmd, n_pool))
+        got = pool.cpu().numpy()
+        for n in (0, 1, 37, nq - 1):
+            assert np.array_equal(got[n], oracle.candidate_pool(bm[n].numpy()[:(vis[n] + 7) // 8],
+                                                                n_pool)), (n_pool, n)
 
 
 def test_prefill_indexer_many_queries(csa2):

@@ -4,8 +4,8 @@ the same launch configuration) that bench.py times, checked against the oracle.
 Each check uses the GPU's own upstream result as the oracle's input where a step depends on an
 earlier one (the pool is rebuilt by the oracle from the GPU's block maxima, attention is
 recomputed by the oracle on the GPU's indices), so every call is judged on its own; the
-upstream results are themselves checked against the oracle.  Chunked prefill is checked on 24
-query tokens spread over the chunk (first and last included): the oracle scores all 262,144+
+upstream results are themselves checked against the oracle.  Chunked prefill is checked on 64
+query tokens spread evenly over the chunk (first and last included): the oracle scores all 262,144+
 visible positions for each of them.
 """
 import numpy as np
@@ -76,7 +76,7 @@ def test_workload_full_size(mods, name):
     codes, sf = st.codes.cpu().numpy(), st.sf.cpu().numpy()
     if w.kind == "prefill":
         nq = w.T
-        queries = sorted(set(np.linspace(0, nq - 1, 22).astype(int).tolist() + [1, nq - 2]))
+        queries = sorted(set(np.linspace(0, nq - 1, 62).astype(int).tolist() + [1, nq - 2]))
     else:
         queries = list(range(w.B))
 
