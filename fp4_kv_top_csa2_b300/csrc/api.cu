@@ -385,9 +385,10 @@ int csa2_sparse_attn_decode(const void *q_bf16, int B, int H, const uint8_t *cod
 
 size_t csa2_sparse_attn_prefill_workspace_size(int T, int H, int topk) {
   if (T < 0 || H < 1 || topk < 1) return 0;
+  if (attn_prefill_supported(H)) return 0;  // the tensor-core kernel quantises the query itself
   const size_t rows = (size_t)T * H;
   return align_up(rows * kCodeBytes) + align_up(rows * kSfBytes) +
-         (attn_prefill_supported(H) ? 0 : align_up(attn_workspace_bytes(T, H, topk)));
+         align_up(attn_workspace_bytes(T, H, topk));
 }
 
 int csa2_sparse_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_seq,
@@ -402,22 +403,23 @@ int csa2_sparse_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_
   if (T == 0) return CSA2_OK;
   if (!q_seq || !aligned16(q_seq)) return CSA2_ERR_INVALID_ARG;
   const size_t need = csa2_sparse_attn_prefill_workspace_size(T, H, topk);
-  if (ws_bytes < need || !workspace) return CSA2_ERR_WORKSPACE;
+  if (ws_bytes < need || (need && !workspace)) return CSA2_ERR_WORKSPACE;
   if (int r = check_device()) return r;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the query is quantised per (token, head) row with the main-KV FP4 rule: inside the
+  // tensor-core kernel, or by the quantisation kernel ahead of the CUDA-core one
+  if (attn_prefill_supported(H))
+    return cuda_status(launch_attn_prefill(q_bf16, T, H, q_seq, codes, sf, cu_ctx, idx, topk,
+                                           softmax_scale, out_bf16, lse, st));
   WsCursor c(workspace);
   const size_t rows = (size_t)T * H;
   uint8_t *q_codes = c.take<uint8_t>(rows * kCodeBytes);
   uint8_t *q_sf = c.take<uint8_t>(rows * kSfBytes);
-  const bool mma = attn_prefill_supported(H);
-  void *attn_ws = mma ? nullptr : c.take<char>(attn_workspace_bytes(T, H, topk));
-  // the query is quantised per (token, head) row with the main-KV FP4 rule
+  void *attn_ws = c.take<char>(attn_workspace_bytes(T, H, topk));
   cudaError_t e = launch_kv_quant(q_bf16, (int64_t)rows, kD, nullptr, q_codes, q_sf, st);
   if (e == cudaSuccess)
-    e = mma ? launch_attn_prefill(q_codes, q_sf, T, H, q_seq, codes, sf, cu_ctx, idx, topk,
-                                  softmax_scale, out_bf16, lse, st)
-            : launch_attn(nullptr, q_codes, q_sf, T, H, q_seq, codes, sf, cu_ctx, idx, topk,
-                          softmax_scale, out_bf16, lse, attn_ws, st);
+    e = launch_attn(nullptr, q_codes, q_sf, T, H, q_seq, codes, sf, cu_ctx, idx, topk,
+                    softmax_scale, out_bf16, lse, attn_ws, st);
   return cuda_status(e);
 }
 

@@ -204,12 +204,13 @@ cudaError_t launch_attn(const void *q_bf16, const uint8_t *q_codes, const uint8_
                         void *out_bf16, float *lse, void *workspace, cudaStream_t st);
 size_t attn_workspace_bytes(int nq, int H, int topk);
 
-// Tensor-core prefill attention (attn_prefill.cu): one CTA per query token, H <= 64.
+// Tensor-core prefill attention (attn_prefill.cu): one CTA per query token, H <= 64; the query
+// is FP4-quantised inside the kernel.
 bool attn_prefill_supported(int H);
-cudaError_t launch_attn_prefill(const uint8_t *q_codes, const uint8_t *q_sf, int T, int H,
-                                const int32_t *q_seq, const uint8_t *codes, const uint8_t *sf,
-                                const int64_t *cu_ctx, const int32_t *idx, int topk, float scale,
-                                void *out_bf16, float *lse, cudaStream_t st);
+cudaError_t launch_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_seq,
+                                const uint8_t *codes, const uint8_t *sf, const int64_t *cu_ctx,
+                                const int32_t *idx, int topk, float scale, void *out_bf16,
+                                float *lse, cudaStream_t st);
 
 // Tensor-core decode attention (attn_mma.cu): H <= 64, one CTA per 32 selected rows and 32
 // heads.

@@ -311,7 +311,8 @@ def test_decode_attention(csa2, B, H, n_rows, topk):
 @pytest.mark.parametrize("T,H,topk", [(5, 64, 2048), (3, 16, 100), (2, 64, 40), (2, 64, 90),
                                       (3, 32, 200), (2, 64, 4000), (2, 128, 300)])
 def test_prefill_attention(csa2, T, H, topk):
-    """Tile counts from one to 63 (64 rows per tile, ragged last tiles), every 11th slot empty."""
+    """Tile counts from one to 32 (128 rows per tile, ragged last tiles), every 11th slot empty;
+    more than 64 heads take the CUDA-core kernel."""
     n_rows = 4000
     x, _, _, _ = _attn_case(1, H, n_rows, topk, T)
     g = torch.Generator().manual_seed(T + 7)
@@ -334,6 +335,46 @@ def test_prefill_attention(csa2, T, H, topk):
     ob, lh = _bits(out), lse.cpu().numpy()
     for i in range(T):
         check_attn(ob[i], lh[i], ref[i][0], ref[i][1], oracle.double_to_bf16(ref[i][0]), f"tok {i}")
+
+
+@pytest.mark.parametrize("order,H", [("rising", 64), ("falling", 64), ("rising", 16)])
+def test_prefill_attention_moving_maximum(csa2, order, H):
+    """The prefill kernel's softmax keeps a per-head reference maximum that moves only when a
+    score exceeds it by a wide margin.  Slots ordered by rising score (all heads share one
+    direction, scores spanning hundreds of units) move it on every tile and rescale the running
+    output; falling order never moves it after the first tile.  Token 1 starts with two empty
+    tiles, token 2 has no valid slot at all."""
+    n_rows, topk, T = 3000, 1000, 3
+    x, _, _, _ = _attn_case(1, H, n_rows, topk, 77)
+    g = torch.Generator().manual_seed(78)
+    v = torch.randn(512, generator=g) * 40
+    c = 1 + 2 * torch.rand(T, H, 1, generator=g)
+    q = (c * v).to(torch.bfloat16)
+    codes = torch.empty((n_rows, 256), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((n_rows, 32), dtype=torch.uint8, device="cuda")
+    csa2.csa2_kv_quant_fp4(x.cuda(), codes, sf)
+    kv = oracle.kv_dequant_fp4(codes.cpu().numpy(), sf.cpu().numpy())
+    key = kv @ v.double().numpy()
+    rows = np.argsort(key if order == "rising" else -key)
+    idx = np.stack([rows[np.sort(np.random.default_rng(i).choice(n_rows, topk, replace=False))]
+                    for i in range(T)]).astype(np.int32)
+    idx[1, :256] = -1
+    idx[2, :] = -1
+    idx = torch.from_numpy(idx)
+    cu = torch.tensor([0, n_rows], dtype=torch.int64)
+    q_seq = torch.zeros(T, dtype=torch.int32)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, H), device="cuda")
+    ws = csa2.workspace(csa2.csa2_sparse_attn_prefill_workspace_size(T, H, topk))
+    scale = 1 / math.sqrt(512)
+    csa2.csa2_sparse_attn_prefill(q.cuda(), q_seq.cuda(), codes, sf, cu.cuda(), idx.cuda(), scale,
+                                  out, lse, ws=ws)
+    ref = oracle.sparse_attn_prefill(_bits(q), q_seq.numpy(), codes.cpu().numpy(),
+                                     sf.cpu().numpy(), cu.numpy(), idx.numpy(), scale)
+    ob, lh = _bits(out), lse.cpu().numpy()
+    for i in range(T):
+        check_attn(ob[i], lh[i], ref[i][0], ref[i][1], oracle.double_to_bf16(ref[i][0]), f"tok {i}")
+    assert not out[2].float().any() and torch.isneginf(lse[2]).all()
 
 
 @pytest.mark.parametrize("dtype", [1, 0])
