@@ -14,8 +14,10 @@
 //   CAND: scores of the positions of listed blocks (each 8-row block one TMA box).
 // Both modes run the same MMA sequence and epilogue, so a position gets the same fp32 score.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
-// warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31).  Work = chunks of up to CT
+// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
+// warps 2..9 = two epilogue groups of four (warp w reads TMEM lanes 32*(w%4)..+31); group g
+// drains the accumulators of the tiles with an even (g = 0) or odd (g = 1) running index, so
+// two tiles' epilogues are in flight at once.  Work = chunks of up to CT
 // consecutive 128-key tiles of one query, dealt round-robin to a persistent grid.
 #include "sm100.cuh"
 
@@ -30,7 +32,8 @@ constexpr int kAccCols = 16;                          // N
 constexpr int kTmemCols = kAccBufs * kAccCols;        // 64
 constexpr int kQRows = 16;
 constexpr int kQBytes = kQRows * kKeyRowBytes;        // 2 KB
-constexpr int kIdxThreads = 192;
+constexpr int kIdxEpiGroups = 2;                   // epilogue groups, alternate accumulators
+constexpr int kIdxThreads = 64 + kIdxEpiGroups * 128;
 constexpr int kMaxScanQueries = 1024;
 
 struct IdxSmem {
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_mma_kernel(
     }
   } else {
     // ------------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;
+    const int quarter = warp & 3, group = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     uint32_t acc = 0;
@@ -246,6 +249,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_mma_kernel(
         }
       }
       for (int t = c.t0; t < c.t1; ++t, ++acc) {
+        if ((int)(acc % kIdxEpiGroups) != group) continue;  // the other group's tile
         const uint32_t a = acc % kAccBufs, aph = (acc / kAccBufs) & 1;
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.tfull[a], aph));
         if (!ok) break;
