@@ -11,7 +11,8 @@ Sources (prose only on the pages):
     scale per 16 channels).
   * "DeepSeek V4.1-Flash" (aiwiki.ai), section "Compressed Sparse Attention 2" -- per-mode
     recomputation, block selection by maximum index score, pool of 2,048 blocks x 8 positions,
-    Reindex selecting 512; section "KV-cache formats and bounded replay" -- FP4 main global KV.
+    Reindex selecting 512, every layer's own local sliding-window keys and values; section
+    "KV-cache formats and bounded replay" -- FP4 main global KV, FP8 local sliding-window KV.
 
 Every batch-level function below loops over queries in Python and calls the per-query C
 routines; there is no blocking, fusion or reordering beyond the definitions.
@@ -71,6 +72,8 @@ def _load():
     lib.orc_candidate_pool.restype = i32
     lib.orc_candidate_pool.argtypes = [P, i64, i32, P]
     lib.orc_sparse_attn.argtypes = [P, i32, i32, P, P, P, i32, ctypes.c_double, P, P]
+    lib.orc_fp8_quant.argtypes = [P, i64, P]
+    lib.orc_sparse_swa_attn.argtypes = [P, i32, i32, P, P, P, i32, P, i32, ctypes.c_double, P, P]
     lib.orc_bf16_to_double.argtypes = [P, i64, P]
     lib.orc_double_to_bf16_array.argtypes = [P, i64, P]
     _lib = lib
@@ -270,4 +273,55 @@ def sparse_attn_prefill(q_bf16, q_seq, codes, sf, cu_ctx, idx, scale, tokens=Non
         lo, hi = int(cu_ctx[b]), int(cu_ctx[b + 1])
         qhat = quantize_query_fp4(np.ascontiguousarray(q_bf16[i]))
         res[i] = sparse_attn(qhat, codes[lo:hi], sf[lo:hi], idx[i], scale)
+    return res
+
+
+# ----------------------------------------------------------------------------------------------
+# f1: the local sliding-window branch (FP8 local KV, one softmax over both sets of rows)
+# ----------------------------------------------------------------------------------------------
+def fp8_quant(x_bf16: np.ndarray) -> np.ndarray:
+    """bf16 bits -> E4M3 bytes (round to nearest even, saturating at +-448, no scale)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().orc_fp8_quant(_p(x), x.size, _p(out))
+    return out
+
+
+def window_positions(vis: int, n_win: int) -> np.ndarray:
+    """The positions of a query's local window: the last n_win of the vis positions it sees."""
+    return np.arange(max(0, vis - n_win), vis, dtype=np.int64)
+
+
+def sparse_swa_attn(q: np.ndarray, codes_seq, sf_seq, idx, loc_rows, scale):
+    """One query set q [H, d] float64 over the selected FP4 rows of one sequence and the local
+    E4M3 rows loc_rows [n_loc, d]: (out [H, d], lse [H])."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    H, d = q.shape
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    loc = np.ascontiguousarray(loc_rows, dtype=np.uint8).reshape(-1, d)
+    codes_seq = np.ascontiguousarray(codes_seq, dtype=np.uint8)
+    sf_seq = np.ascontiguousarray(sf_seq, dtype=np.uint8)
+    out = np.empty((H, d), dtype=np.float64)
+    lse = np.empty(H, dtype=np.float64)
+    _load().orc_sparse_swa_attn(_p(q), H, d, _p(codes_seq), _p(sf_seq), _p(idx), idx.shape[0],
+                                _p(loc), loc.shape[0], float(scale), _p(out), _p(lse))
+    return out, lse
+
+
+def sparse_swa_attn_queries(q_bf16, q_seq, q_vis, codes, sf, cu_ctx, idx, swa_kv, ring, n_win,
+                            scale, queries=None, quantize_query=False):
+    """Batch form of the sparse + local-window attention calls.  Query n (sequence b = q_seq[n],
+    visible length q_vis[n]) attends to its selected rows idx[n] and to the local rows of the
+    last n_win visible positions, position t of sequence b at local row b * ring + t % ring.
+    quantize_query: the prefill rule (the query quantised to FP4 first)."""
+    res = {}
+    queries = range(q_bf16.shape[0]) if queries is None else queries
+    for n in queries:
+        b = int(q_seq[n])
+        lo, hi = int(cu_ctx[b]), int(cu_ctx[b + 1])
+        win = window_positions(int(q_vis[n]), n_win)
+        loc = swa_kv[b * ring + win % ring]
+        qn = np.ascontiguousarray(q_bf16[n])
+        q = quantize_query_fp4(qn) if quantize_query else bf16_to_double(qn)
+        res[n] = sparse_swa_attn(q, codes[lo:hi], sf[lo:hi], idx[n], loc, scale)
     return res

@@ -13,8 +13,9 @@
  *   [WIKI] "DeepSeek V4.1-Flash" (aiwiki.ai), section "Compressed Sparse Attention 2": what each
  *          mode recomputes; the first Full layer scores all causally visible positions, selects
  *          blocks by their maximum index score, pool = 2,048 blocks of 8 positions; Reindex
- *          layers search that pool and select 512 positions.  Section "KV-cache formats and
- *          bounded replay": main global KV stored in FP4.
+ *          layers search that pool and select 512 positions; every layer also has its own local
+ *          sliding-window keys and values.  Section "KV-cache formats and bounded replay": main
+ *          global KV stored in FP4, local sliding-window KV in FP8.
  *   [SPEC] readings taken where the pages are silent (rounding rules, score formula, tie rule,
  *          softmax scale, packing); each is stated beside the function that uses it.
  *
@@ -329,4 +330,67 @@ void orc_bf16_to_double(const uint16_t *x, int64_t n, double *out)
 void orc_double_to_bf16_array(const double *x, int64_t n, uint16_t *out)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_double_to_bf16(x[i]);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* f1: the local sliding-window branch ([WIKI] "Compressed Sparse Attention 2": every CSA2     */
+/* layer creates its own local sliding-window keys and values; "KV-cache formats and bounded  */
+/* replay": the local sliding-window KV is stored in FP8)                                      */
+/* ------------------------------------------------------------------------------------------ */
+
+/* [SPEC] local KV encoding: each bf16 element -> E4M3 "fn" (round to nearest, ties to even,
+ * saturating at +-448, sign kept), no scale. */
+void orc_fp8_quant(const uint16_t *x, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float v = orc_bf16_to_float(x[i]);
+        int mag = orc_e4m3_encode(fabsf(v));
+        out[i] = (uint8_t)((signbit(v) ? 0x80 : 0) | mag);
+    }
+}
+
+/* [SPEC] one softmax over the union of the selected global rows (dequantised FP4, as
+ * orc_sparse_attn) and n_loc local rows (E4M3, decoded exactly); K = V = each row.  For each
+ * head h:  s = scale * <q_h, row> over every row of the union,
+ *   out_h = sum softmax(s) * row,   lse_h = log sum exp(s)   (no row: out 0, lse -inf). */
+void orc_sparse_swa_attn(const double *q, int H, int d, const uint8_t *codes, const uint8_t *sf,
+                         const int32_t *idx, int K, const uint8_t *loc, int n_loc, double scale,
+                         double *out, double *lse)
+{
+    int nv = 0;
+    for (int j = 0; j < K; ++j) nv += idx[j] >= 0;
+    int n = nv + n_loc;
+    double *rows = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+    double *s = (double *)malloc(sizeof(double) * (n > 0 ? n : 1));
+    int v = 0;
+    for (int j = 0; j < K; ++j) {
+        if (idx[j] < 0) continue;
+        orc_kv_dequant_fp4(codes + (int64_t)idx[j] * (d / 2), sf + (int64_t)idx[j] * (d / 16), 1,
+                           d, rows + (size_t)v * d);
+        ++v;
+    }
+    for (int j = 0; j < n_loc; ++j, ++v)
+        for (int c = 0; c < d; ++c) rows[(size_t)v * d + c] = orc_e4m3_value(loc[(size_t)j * d + c]);
+    for (int h = 0; h < H; ++h) {
+        double *o = out + (size_t)h * d;
+        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        if (n == 0) { lse[h] = -INFINITY; continue; }
+        double m = -INFINITY;
+        for (int j = 0; j < n; ++j) {
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c) dot += q[(size_t)h * d + c] * rows[(size_t)j * d + c];
+            s[j] = scale * dot;
+            if (s[j] > m) m = s[j];
+        }
+        double l = 0.0;
+        for (int j = 0; j < n; ++j) {
+            double p = exp(s[j] - m);
+            l += p;
+            for (int c = 0; c < d; ++c) o[c] += p * rows[(size_t)j * d + c];
+        }
+        for (int c = 0; c < d; ++c) o[c] /= l;
+        lse[h] = m + log(l);
+    }
+    free(rows);
+    free(s);
 }
