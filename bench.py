@@ -27,7 +27,9 @@ import threading
 import time
 
 HEADLINE = "hier_decode_l1m"
+HEADLINE_SWA = "hier_decode_l1m_swa128"
 PREFILL = "prefill_t4096_p262144"
+PREFILL_HIER = "prefill_hier_t4096_p262144"
 METRIC = "sparse-attn decode tokens/s + HBM GB/s vs 8 TB/s at 1M ctx; prefill TFLOP/s"
 HBM_TARGET_GBS = 8000.0
 DECODE_CONFIGS = ("decode_b1_l4096_bf16idx", "decode_b8_l65536", "decode_ragged_b32")
@@ -312,8 +314,11 @@ def run_ours(args, rank, world):
     if args.configs and rank == 0:
         line["decode_configs"] = {name: run_decode_config(name, args, dev, peaks, flush)
                                   for name in DECODE_CONFIGS}
+        # the headline step with every layer's local sliding window (128 FP8 local rows)
+        line["hier_decode_swa"] = run_decode_config(HEADLINE_SWA, args, dev, peaks, flush)
     if args.prefill and rank == 0:
         line["prefill"] = run_prefill(args, dev, peaks)
+        line["prefill_hier"] = run_prefill_hier(args, dev)
     if rank == 0 and args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, w, args.cpu_steps)
     return line
@@ -435,6 +440,9 @@ def run_decode_config(name, args, dev, peaks, flush):
            "l2": L2Flush.WHAT}
     if w.ragged:
         out["context"] = f"{min(inp['lengths'])}..{max(inp['lengths'])} (ragged, {w.B} sequences)"
+    if w.n_win:
+        out["local_window"] = w.n_win
+        out["modes"] = list(w.modes)
     del st
     torch.cuda.empty_cache()
     return out
@@ -536,6 +544,49 @@ def run_prefill(args, dev, peaks):
                 "unit": "TFLOP/s", "frac": round(ti_fl / p_fp8, 4),
                 "peak_source": f"{src} bf16 burst x 2 (nominal fp8 / bf16 4.5 / 2.25)",
                 "traffic": None}}
+
+
+def run_prefill_hier(args, dev):
+    """Chunked prefill through the hierarchical indexer (a candidate pool per query token, three
+    Reindex layers, two Reuse layers, six sparse attentions): each call kind and the whole step,
+    timed with CUDA events on the launching stream."""
+    import torch
+    from fp4_kv_top_csa2_b300 import synth
+    from fp4_kv_top_csa2_b300.step import Step
+    w = synth.WORKLOADS[PREFILL_HIER]
+    inp = synth.make_inputs(w)
+    st = Step(inp, device=dev)
+    st.drop_source_rows()
+    inp["kv_bf16"] = None
+    stream = torch.cuda.current_stream()
+    full = st.layers[0]
+    reidx = next(L for L in st.layers if L["mode"] == "reindex")
+    calls = {"step": lambda: st.run(),
+             "full_index_with_pool": lambda: st.index_with_pool(full),
+             "reindex_index": lambda: st.index(reidx, cand=st.pool),
+             "attention": lambda: st.attend(full, full["idx"])}
+    st.run()
+    torch.cuda.synchronize()
+    ms = {}
+    for name, fn in calls.items():
+        ts = []
+        for _ in range(args.prefill_steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms[name] = round(statistics.median(ts), 4)
+    out = {"workload": PREFILL_HIER, "tokens": w.T, "cached": w.L[0], "topk": w.topk,
+           "pool": f"{w.n_pool_blocks}x8 per query token", "modes": list(w.modes),
+           "ms_per_step": ms["step"], "tokens_per_s": round(w.T / (ms["step"] / 1e3), 1),
+           "ms_by_call": {k: v for k, v in ms.items() if k != "step"},
+           "reindex_tflops": round(2.0 * w.T * w.n_pool_blocks * 8 * w.Hi * w.Di /
+                                   (ms["reindex_index"] / 1e3) / 1e12, 2)}
+    del st
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------------------------------------

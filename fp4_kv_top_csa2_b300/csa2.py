@@ -48,6 +48,12 @@ def _load() -> ctypes.CDLL:
         "csa2_sparse_attn_decode": (I, [P, I, I, P, P, P, P, I, F, P, P, P, SZ, P]),
         "csa2_sparse_attn_prefill_workspace_size": (SZ, [I, I, I]),
         "csa2_sparse_attn_prefill": (I, [P, I, I, P, P, P, P, I, P, I, F, P, P, P, SZ, P]),
+        "csa2_swa_kv_quant_fp8": (I, [P, I64, I, P, P, P]),
+        "csa2_sparse_swa_attn_decode_workspace_size": (SZ, [I, I, I, I]),
+        "csa2_sparse_swa_attn_decode": (I, [P, I, I, P, P, P, P, I, P, I, I, F, P, P, P, SZ, P]),
+        "csa2_sparse_swa_attn_prefill_workspace_size": (SZ, [I, I, I, I]),
+        "csa2_sparse_swa_attn_prefill": (I, [P, I, I, P, P, P, P, P, I, P, I, P, I, I, F, P, P,
+                                             P, SZ, P]),
         "csa2_device_status": (I, [P, I, P]),
         "csa2_kernel_launches": (ctypes.c_uint64, []),
     }
@@ -202,6 +208,42 @@ def csa2_sparse_attn_prefill(q_bf16, q_seq, codes, sf, cu_ctx, idx, softmax_scal
     _check("csa2_sparse_attn_prefill", lib.csa2_sparse_attn_prefill(
         _ptr(q_bf16), T, H, _ptr(q_seq), _ptr(codes), _ptr(sf), _ptr(cu_ctx), B, _ptr(idx), topk,
         float(softmax_scale), _ptr(out_bf16), _ptr(lse), wp, wn, _stream(stream)))
+
+
+def csa2_swa_kv_quant_fp8(x_bf16, swa_kv, out_rows=None, stream=None):
+    n, d = x_bf16.shape
+    _check("csa2_swa_kv_quant_fp8", lib.csa2_swa_kv_quant_fp8(_ptr(x_bf16), n, d, _ptr(out_rows),
+                                                              _ptr(swa_kv), _stream(stream)))
+
+
+def csa2_sparse_swa_attn_decode_workspace_size(B, H, topk, n_win):
+    return lib.csa2_sparse_swa_attn_decode_workspace_size(B, H, topk, n_win)
+
+
+def csa2_sparse_swa_attn_decode(q_bf16, codes, sf, cu_ctx, idx, swa_kv, ring, n_win,
+                                softmax_scale, out_bf16, lse=None, ws=None, stream=None):
+    B, H, _ = q_bf16.shape
+    topk = idx.shape[1]
+    wp, wn = _ws(ws)
+    _check("csa2_sparse_swa_attn_decode", lib.csa2_sparse_swa_attn_decode(
+        _ptr(q_bf16), B, H, _ptr(codes), _ptr(sf), _ptr(cu_ctx), _ptr(idx), topk, _ptr(swa_kv),
+        ring, n_win, float(softmax_scale), _ptr(out_bf16), _ptr(lse), wp, wn, _stream(stream)))
+
+
+def csa2_sparse_swa_attn_prefill_workspace_size(T, H, topk, n_win):
+    return lib.csa2_sparse_swa_attn_prefill_workspace_size(T, H, topk, n_win)
+
+
+def csa2_sparse_swa_attn_prefill(q_bf16, q_seq, q_vis, codes, sf, cu_ctx, idx, swa_kv, ring,
+                                 n_win, softmax_scale, out_bf16, lse=None, ws=None, stream=None):
+    T, H, _ = q_bf16.shape
+    topk = idx.shape[1]
+    B = cu_ctx.numel() - 1
+    wp, wn = _ws(ws)
+    _check("csa2_sparse_swa_attn_prefill", lib.csa2_sparse_swa_attn_prefill(
+        _ptr(q_bf16), T, H, _ptr(q_seq), _ptr(q_vis), _ptr(codes), _ptr(sf), _ptr(cu_ctx), B,
+        _ptr(idx), topk, _ptr(swa_kv), ring, n_win, float(softmax_scale), _ptr(out_bf16),
+        _ptr(lse), wp, wn, _stream(stream)))
 
 
 def csa2_device_status(reset=True, stream=None) -> int:

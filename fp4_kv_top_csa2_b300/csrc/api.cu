@@ -423,6 +423,80 @@ int csa2_sparse_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_
   return cuda_status(e);
 }
 
+// ---- the local sliding-window branch ------------------------------------------------------
+
+int csa2_swa_kv_quant_fp8(const void *x_bf16, int64_t n_rows, int d, const int64_t *out_rows,
+                          uint8_t *swa_kv, void *stream) {
+  if (n_rows < 0 || d < 16 || d > 4096 || d % 16 != 0) return CSA2_ERR_INVALID_ARG;
+  if (n_rows == 0) return CSA2_OK;
+  if (!x_bf16 || !swa_kv) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(swa_kv) || !aligned16(out_rows))
+    return CSA2_ERR_INVALID_ARG;
+  if (int r = check_device()) return r;
+  return cuda_status(launch_fp8_quant(x_bf16, n_rows, d, out_rows, swa_kv,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+// The window's extra checks: 0 <= n_win <= ring, a ring buffer when there is a window, and the
+// tensor-core kernels (H <= 64).
+static int swa_args_ok(int H, const uint8_t *swa_kv, int ring, int n_win) {
+  if (n_win < 0 || n_win > 8192 || ring < 1 || n_win > ring) return CSA2_ERR_INVALID_ARG;
+  if (n_win > 0 && (!swa_kv || !aligned16(swa_kv))) return CSA2_ERR_INVALID_ARG;
+  if (H > 64) return CSA2_ERR_UNSUPPORTED;
+  return CSA2_OK;
+}
+
+size_t csa2_sparse_swa_attn_decode_workspace_size(int B, int H, int topk, int n_win) {
+  if (B < 0 || H < 1 || topk < 1 || n_win < 0) return 0;
+  return align_up(attn_mma_workspace_bytes(B, H, topk, n_win));
+}
+
+int csa2_sparse_swa_attn_decode(const void *q_bf16, int B, int H, const uint8_t *codes,
+                                const uint8_t *sf, const int64_t *cu_ctx, const int32_t *idx,
+                                int topk, const uint8_t *swa_kv, int ring, int n_win,
+                                float softmax_scale, void *out_bf16, float *lse, void *workspace,
+                                size_t ws_bytes, void *stream) {
+  if (int r = attn_args_ok(B, H, codes, sf, cu_ctx, idx, topk, softmax_scale, q_bf16, out_bf16,
+                           lse, workspace))
+    return r;
+  if (int r = swa_args_ok(H, swa_kv, ring, n_win)) return r;
+  if (B == 0) return CSA2_OK;
+  if (!attn_mma_supported(H, topk, n_win)) return CSA2_ERR_UNSUPPORTED;
+  const size_t need = csa2_sparse_swa_attn_decode_workspace_size(B, H, topk, n_win);
+  if (ws_bytes < need || (need && !workspace)) return CSA2_ERR_WORKSPACE;
+  if (int r = check_device()) return r;
+  return cuda_status(launch_attn_mma(q_bf16, B, H, codes, sf, cu_ctx, idx, topk, softmax_scale,
+                                     out_bf16, lse, workspace, static_cast<cudaStream_t>(stream),
+                                     swa_kv, ring, n_win));
+}
+
+size_t csa2_sparse_swa_attn_prefill_workspace_size(int T, int H, int topk, int n_win) {
+  (void)T, (void)H, (void)topk, (void)n_win;
+  return 0;  // the tensor-core kernel keeps everything on chip
+}
+
+int csa2_sparse_swa_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_seq,
+                                 const int32_t *q_vis, const uint8_t *codes, const uint8_t *sf,
+                                 const int64_t *cu_ctx, int B, const int32_t *idx, int topk,
+                                 const uint8_t *swa_kv, int ring, int n_win, float softmax_scale,
+                                 void *out_bf16, float *lse, void *workspace, size_t ws_bytes,
+                                 void *stream) {
+  (void)ws_bytes;
+  if (int r = attn_args_ok(T, H, codes, sf, cu_ctx, idx, topk, softmax_scale, q_bf16, out_bf16,
+                           lse, workspace))
+    return r;
+  if (int r = swa_args_ok(H, swa_kv, ring, n_win)) return r;
+  if (B < 1) return CSA2_ERR_INVALID_ARG;
+  if (T == 0) return CSA2_OK;
+  if (!q_seq || !aligned16(q_seq) || !q_vis || !aligned16(q_vis)) return CSA2_ERR_INVALID_ARG;
+  if (!attn_prefill_supported(H)) return CSA2_ERR_UNSUPPORTED;
+  if (int r = check_device()) return r;
+  return cuda_status(launch_attn_prefill(q_bf16, T, H, q_seq, codes, sf, cu_ctx, idx, topk,
+                                         softmax_scale, out_bf16, lse,
+                                         static_cast<cudaStream_t>(stream), q_vis, swa_kv, ring,
+                                         n_win));
+}
+
 int csa2_device_status(int *status, int reset, void *stream) {
   if (!status) return CSA2_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

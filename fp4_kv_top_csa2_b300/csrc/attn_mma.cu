@@ -22,6 +22,11 @@
 //   6. Channels on TMEM lanes make the epilogue coalesced: a warp stores 32 consecutive channels
 //      of one head per instruction.  The unnormalised O rows and the per-head (max, sum) go to
 //      workspace; a combine kernel merges the tiles of each query.
+// With a local window (the sliding-window branch: "DeepSeek V4.1-Flash", aiwiki.ai, section
+// "Compressed Sparse Attention 2", every layer's own local keys and values; section "KV-cache
+// formats and bounded replay", stored in FP8), the tiles after the selected rows' hold the
+// window's local E4M3 rows instead (decoded exactly to bf16 through a table), so the combine's
+// merge of all tiles is one softmax over the selected rows and the window.
 #include <cstring>
 
 #include "sm100.cuh"
@@ -44,7 +49,9 @@ constexpr int kOffPlo = kOffPhi + 4096;
 constexpr int kOffRawC = kOffPlo + 4096;              // 32 rows x 256 B codes
 constexpr int kOffRawS = kOffRawC + kAttTS * 256;     // 32 rows x 32 B scales
 constexpr int kOffLut = kOffRawS + kAttTS * 32;       // 256 x u32
-constexpr int kOffMisc = kOffLut + 1024;
+constexpr int kOffLut8 = kOffLut + 1024;              // 256 x u16: E4M3 byte -> bf16
+constexpr int kOffRaw8 = kOffLut8 + 512;              // window tiles: 32 rows x 512 B of E4M3
+constexpr int kOffMisc = kOffRaw8 + kAttTS * 512;
 constexpr int kAttSmem = kOffMisc + 1024 + 1024;      // + alignment slack
 // The M=128 operand read of a Q chunk covers 128 rows of 128 B from the chunk's start, i.e. up
 // to 12 KB past its 32 real rows (into the following chunks and the row tile): readable, and it
@@ -79,7 +86,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
     const __grid_constant__ CUtensorMap qmap, int H, const uint8_t *__restrict__ codes,
     const uint8_t *__restrict__ sf, const int64_t *__restrict__ cu_ctx,
     const int32_t *__restrict__ idx, int topk, float scale_log2e, int n_tiles,
-    float *__restrict__ o_part, float *__restrict__ m_part, float *__restrict__ l_part) {
+    float *__restrict__ o_part, float *__restrict__ m_part, float *__restrict__ l_part,
+    const uint8_t *__restrict__ swa_kv, int ring, int n_win, int n_sel_tiles) {
   using namespace sm100;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -103,6 +111,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
   }
   // byte of two E2M1 codes -> bf16x2 of their values (exact)
   lut[tid] = pack_bf16x2(e2m1_to_float(tid & 15), e2m1_to_float(tid >> 4));
+  // E4M3 byte -> bf16 (exact: at most 4 significant bits, magnitudes 2^-9..448)
+  reinterpret_cast<uint16_t *>(sm + kOffLut8)[tid] =
+      __bfloat16_as_ushort(__float2bfloat16_rn(e4m3_to_float(tid)));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -117,34 +128,60 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
     for (int kc = 0; kc < 8; ++kc)
       tma_load_2d(sm + kOffQ + kc * kQChunkBytes, &qmap, &ms.bar_q, kc * 64, n * H + h0);
   }
-  // the 32 rows as 32 x 18 16-byte cp.async copies (256 B codes + 32 B scales per row) spread
-  // over all threads; an empty slot is a zero row (value 0, never NaN), masked in the softmax.
-  // A thread's row numbers are all loaded first, so their latencies overlap.
-  constexpr int kCopies = kAttTS * 18, kIters = (kCopies + kAttThreads - 1) / kAttThreads;
-  int rr[kIters];
+  const bool win = tile >= n_sel_tiles;  // a tile of the local window
+  if (!win) {
+    // the 32 rows as 32 x 18 16-byte cp.async copies (256 B codes + 32 B scales per row) spread
+    // over all threads; an empty slot is a zero row (value 0, never NaN), masked in the softmax.
+    // A thread's row numbers are all loaded first, so their latencies overlap.
+    constexpr int kCopies = kAttTS * 18, kIters = (kCopies + kAttThreads - 1) / kAttThreads;
+    int rr[kIters];
 #pragma unroll
-  for (int k = 0; k < kIters; ++k) {
-    const int i = tid + k * kAttThreads, slot = tile * kAttTS + i / 18;
-    rr[k] = (i < kCopies && slot < topk) ? idx[(int64_t)n * topk + slot] : -1;
-  }
+    for (int k = 0; k < kIters; ++k) {
+      const int i = tid + k * kAttThreads, slot = tile * kAttTS + i / 18;
+      rr[k] = (i < kCopies && slot < topk) ? idx[(int64_t)n * topk + slot] : -1;
+    }
 #pragma unroll
-  for (int k = 0; k < kIters; ++k) {
-    const int i = tid + k * kAttThreads;
-    if (i >= kCopies) break;
-    const int j = i / 18, part = i - j * 18;
-    const int r = rr[k];
-    if (part == 0) ms.slot_ok[j] = r >= 0;
-    uint8_t *dst = part < 16 ? sm + kOffRawC + j * 256 + part * 16
-                             : sm + kOffRawS + j * 32 + (part - 16) * 16;
-    if (r >= 0) {
-      const int64_t row = base + r;
-      const uint8_t *src = part < 16 ? codes + row * kCodeBytes + part * 16
-                                     : sf + row * kSfBytes + (part - 16) * 16;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
-                   "l"(reinterpret_cast<uint64_t>(src))
-                   : "memory");
-    } else {
-      *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    for (int k = 0; k < kIters; ++k) {
+      const int i = tid + k * kAttThreads;
+      if (i >= kCopies) break;
+      const int j = i / 18, part = i - j * 18;
+      const int r = rr[k];
+      if (part == 0) ms.slot_ok[j] = r >= 0;
+      uint8_t *dst = part < 16 ? sm + kOffRawC + j * 256 + part * 16
+                               : sm + kOffRawS + j * 32 + (part - 16) * 16;
+      if (r >= 0) {
+        const int64_t row = base + r;
+        const uint8_t *src = part < 16 ? codes + row * kCodeBytes + part * 16
+                                       : sf + row * kSfBytes + (part - 16) * 16;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                     "l"(reinterpret_cast<uint64_t>(src))
+                     : "memory");
+      } else {
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  } else {
+    // window tile: slots wi = 32 (tile - n_sel_tiles) + j of the last nw = min(n_win, L) positions
+    // t = L - nw + wi; position t's local row is n * ring + t % ring.  32 rows x 32 copies.
+    const int64_t L = cu_ctx[n + 1] - base;
+    const int64_t nw = L < n_win ? L : n_win;
+    const int w0 = (tile - n_sel_tiles) * kAttTS;
+#pragma unroll
+    for (int k = 0; k < kAttTS * 32 / kAttThreads; ++k) {
+      const int i = tid + k * kAttThreads, j = i >> 5, part = i & 31;
+      const int wi = w0 + j;
+      const bool ok_slot = wi < nw;
+      if (part == 0) ms.slot_ok[j] = ok_slot;
+      uint8_t *dst = sm + kOffRaw8 + j * 512 + part * 16;
+      if (ok_slot) {
+        const int64_t t = L - nw + wi;
+        const uint8_t *src = swa_kv + ((int64_t)n * ring + t % ring) * kD + part * 16;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                     "l"(reinterpret_cast<uint64_t>(src))
+                     : "memory");
+      } else {
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+      }
     }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -159,14 +196,23 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
     for (int v = tid; v < kAttTS * 32; v += kAttThreads) {
       const int j = v >> 5, rest = v & 31, kc = half * 4 + (rest >> 3), u = rest & 7;
       const int c0 = kc * 64 + u * 8;
-      const uint32_t cw = *reinterpret_cast<const uint32_t *>(sm + kOffRawC + j * 256 + c0 / 2);
-      const float sc = e4m3_to_float(sm[kOffRawS + j * 32 + c0 / 16]);
-      const uint32_t s2 = pack_bf16x2(sc, sc);
       uint4 w;
-      w.x = bf16x2_mul(lut[cw & 0xFF], s2);
-      w.y = bf16x2_mul(lut[(cw >> 8) & 0xFF], s2);
-      w.z = bf16x2_mul(lut[(cw >> 16) & 0xFF], s2);
-      w.w = bf16x2_mul(lut[cw >> 24], s2);
+      if (!win) {
+        const uint32_t cw = *reinterpret_cast<const uint32_t *>(sm + kOffRawC + j * 256 + c0 / 2);
+        const float sc = e4m3_to_float(sm[kOffRawS + j * 32 + c0 / 16]);
+        const uint32_t s2 = pack_bf16x2(sc, sc);
+        w.x = bf16x2_mul(lut[cw & 0xFF], s2);
+        w.y = bf16x2_mul(lut[(cw >> 8) & 0xFF], s2);
+        w.z = bf16x2_mul(lut[(cw >> 16) & 0xFF], s2);
+        w.w = bf16x2_mul(lut[cw >> 24], s2);
+      } else {
+        const uint16_t *lut8 = reinterpret_cast<const uint16_t *>(sm + kOffLut8);
+        const uint2 b = *reinterpret_cast<const uint2 *>(sm + kOffRaw8 + j * 512 + c0);
+        w.x = lut8[b.x & 0xFF] | ((uint32_t)lut8[(b.x >> 8) & 0xFF] << 16);
+        w.y = lut8[(b.x >> 16) & 0xFF] | ((uint32_t)lut8[b.x >> 24] << 16);
+        w.z = lut8[b.y & 0xFF] | ((uint32_t)lut8[(b.y >> 8) & 0xFF] << 16);
+        w.w = lut8[(b.y >> 16) & 0xFF] | ((uint32_t)lut8[b.y >> 24] << 16);
+      }
       *reinterpret_cast<uint4 *>(sm + kOffK + kc * kChunkBytes + j * 128 + ((u ^ (j & 7)) << 4)) =
           w;
     }
@@ -360,12 +406,13 @@ __global__ void __launch_bounds__(128) attn_mma_combine_kernel(
 // ------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------
-bool attn_mma_supported(int H, int topk) {
-  return H <= 64 && (topk + kAttTS - 1) / kAttTS <= 256 && encode_fn() != nullptr;
+bool attn_mma_supported(int H, int topk, int n_win) {
+  return H <= 64 && (topk + kAttTS - 1) / kAttTS + (n_win + kAttTS - 1) / kAttTS <= 256 &&
+         encode_fn() != nullptr;
 }
 
-size_t attn_mma_workspace_bytes(int nq, int H, int topk) {
-  const size_t tiles = (size_t)(topk + kAttTS - 1) / kAttTS;
+size_t attn_mma_workspace_bytes(int nq, int H, int topk, int n_win) {
+  const size_t tiles = (size_t)(topk + kAttTS - 1) / kAttTS + (size_t)(n_win + kAttTS - 1) / kAttTS;
   const size_t rows = (size_t)nq * tiles * H;
   return rows * kD * sizeof(float) + 2 * rows * sizeof(float) + 1024;
 }
@@ -386,9 +433,10 @@ static bool make_q_map(CUtensorMap *m, const void *q, int64_t rows) {
 cudaError_t launch_attn_mma(const void *q_bf16, int nq, int H, const uint8_t *codes,
                             const uint8_t *sf, const int64_t *cu_ctx, const int32_t *idx,
                             int topk, float scale, void *out_bf16, float *lse, void *workspace,
-                            cudaStream_t st) {
+                            cudaStream_t st, const uint8_t *swa_kv, int ring, int n_win) {
   if (nq == 0) return cudaSuccess;
-  const int n_tiles = (topk + kAttTS - 1) / kAttTS;
+  const int n_sel = (topk + kAttTS - 1) / kAttTS;
+  const int n_tiles = n_sel + (n_win + kAttTS - 1) / kAttTS;
   const size_t rows = (size_t)nq * n_tiles * H;
   float *o_part = static_cast<float *>(workspace);
   float *m_part = o_part + rows * kD;
@@ -403,7 +451,7 @@ cudaError_t launch_attn_mma(const void *q_bf16, int nq, int H, const uint8_t *co
   if (e != cudaSuccess) return e;
   e = launch_pdl(attn_mma_kernel, dim3(n_tiles, n_hg, nq), dim3(kAttThreads), (size_t)kAttSmem,
                  st, qm, H, codes, sf, cu_ctx, idx, topk, scale_log2e, n_tiles, o_part, m_part,
-                 l_part);
+                 l_part, swa_kv, ring, n_win, n_sel);
   note_launches(1);
   if (e != cudaSuccess) return e;
   e = launch_pdl(attn_mma_combine_kernel, dim3(kD / 128, H, nq), dim3(128), 0, st, H, n_tiles,

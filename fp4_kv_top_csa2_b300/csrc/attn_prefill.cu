@@ -26,6 +26,12 @@
 // the tile's maximum per head is reduced across rows, and that head's O^T column and partial sums
 // are rescaled.  The output is O / l in bf16, lse = (m_ref + log2 l) * ln 2.
 //
+// Local window (the sliding-window branch: "DeepSeek V4.1-Flash", aiwiki.ai, section "Compressed
+// Sparse Attention 2", every layer's own local keys and values, stored in FP8 per section
+// "KV-cache formats and bounded replay"): after the selected rows' tiles come tiles of 64 local
+// E4M3 rows (the last n_win positions the token sees; rows 64..127 of those tiles are empty),
+// decoded exactly to fp16, so one softmax covers the selected rows and the window.
+//
 // Roles: warps 0..7 load the next tile's rows from L2 into registers (16-byte loads, one tile
 // ahead, row numbers two tiles ahead), dequantise them into Khat one 128-channel chunk pair at a
 // time as the previous tile's O^T MMAs release it, run the softmax and the epilogue; warp 8
@@ -39,6 +45,7 @@ constexpr int kPfWorkers = 256;                // warps 0..7
 constexpr int kPfMmaWarp = 8;                  // warp 8: TMEM allocation and MMA issue
 constexpr int kPfThreads = kPfWorkers + 32;
 constexpr float kPfHeadroom = 8.0f;            // log2 headroom above the reference maximum
+constexpr int kPfWinRows = 64;                 // local rows per window tile
 
 constexpr int kPfQChunk = 64 * 128;            // one 64-channel chunk of Qhat: 64 heads x 128 B
 constexpr int kPfKChunk = kPfRows * 128;       // one 64-channel chunk of Khat: 128 rows x 128 B
@@ -78,6 +85,12 @@ __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   uint32_t r;
   asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(r) : "r"(byte));
+  return r;
+}
+// Two E4M3 bytes (low byte = lower channel) -> f16x2 of their values (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two));
   return r;
 }
 // One E4M3 scale byte -> f16x2 holding it twice (exact: E4M3 values are fp16 normals).
@@ -155,11 +168,15 @@ __device__ __forceinline__ void pf_bar_workers() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
+// WIN: the local window's tiles follow the selected rows' (compiled separately so the kernel
+// without a window keeps its registers).
+template <bool WIN>
 __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const uint16_t *__restrict__ q_bf16, int H, const int32_t *__restrict__ q_seq,
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf,
     const int64_t *__restrict__ cu_ctx, const int32_t *__restrict__ idx, int topk,
-    float scale_log2e, uint16_t *__restrict__ out, float *__restrict__ lse) {
+    float scale_log2e, uint16_t *__restrict__ out, float *__restrict__ lse,
+    const int32_t *__restrict__ q_vis, const uint8_t *__restrict__ swa_kv, int ring, int n_win) {
   using namespace sm100;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -168,7 +185,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = blockIdx.x;
   const int32_t *idx_n = idx + (int64_t)n * topk;
-  const int n_tiles = (topk + kPfRows - 1) / kPfRows;
+  const int n_sel = (topk + kPfRows - 1) / kPfRows;  // tiles of selected rows
+  const int n_tiles = n_sel + (WIN ? (n_win + kPfWinRows - 1) / kPfWinRows : 0);
 
   if (tid == 0) {
     mbar_init(&ms.bar_q, kPfWorkers);
@@ -256,18 +274,45 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     uint4 rc[8];     // codes of (chunk pair cp, row half) at 2 cp + half
     uint32_t rs[8];  // the two scales of each
     // Row numbers run two tiles ahead of the row data, so issuing a tile's data loads never
-    // waits for its index loads.
+    // waits for its index loads.  For a window tile, ri[0] is the local row of this thread's
+    // window slot (rows 64..127 of the tile are empty) and win_next is set.
     int ri[2], rrow = -1, rrow_next = -1;
+    bool win_ri = false;
+    const int64_t vis = WIN ? q_vis[n] : 0;
+    const int64_t nw = vis < n_win ? vis : n_win;  // window length of this token
+    const int64_t lbase = (int64_t)q_seq[n] * ring;
     auto load_idx = [&](int t) {
+      if (!WIN || t < n_sel) {
+        win_ri = false;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int slot = t * kPfRows + jr + 64 * hf;
-        ri[hf] = (t < n_tiles && slot < topk) ? __ldg(idx_n + slot) : -1;
+        for (int hf = 0; hf < 2; ++hf) {
+          const int slot = t * kPfRows + jr + 64 * hf;
+          ri[hf] = slot < topk ? __ldg(idx_n + slot) : -1;
+        }
+        const int slot = t * kPfRows + jrow;
+        rrow_next = slot < topk ? __ldg(idx_n + slot) : -1;
+      } else {  // window tile: slot wi of the last nw positions t = vis - nw + wi
+        win_ri = true;
+        const int64_t w0 = (int64_t)(t - n_sel) * kPfWinRows;
+        const int64_t wi = w0 + jr;
+        ri[0] = (t < n_tiles && wi < nw) ? (int)((vis - nw + wi) % ring) : -1;
+        ri[1] = -1;
+        rrow_next = (t < n_tiles && jrow < kPfWinRows && w0 + jrow < nw) ? 0 : -1;
       }
-      const int slot = t * kPfRows + jrow;
-      rrow_next = (t < n_tiles && slot < topk) ? __ldg(idx_n + slot) : -1;
     };
     auto load_rows = [&]() {
+      if (WIN && win_ri) {  // 32 channels of E4M3 per chunk pair: two 16-byte loads
+        const int64_t row = lbase + (ri[0] >= 0 ? ri[0] : 0);
+#pragma unroll
+        for (int cp = 0; cp < 4; ++cp) {
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            rc[2 * cp + k] = ri[0] >= 0 ? __ldg(reinterpret_cast<const uint4 *>(
+                                              swa_kv + row * kD + cp * 128 + seg * 32 + 16 * k))
+                                        : make_uint4(0, 0, 0, 0);
+        }
+        return;
+      }
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int64_t row = base + (ri[hf] >= 0 ? ri[hf] : 0);
@@ -338,17 +383,36 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       for (int cp = 0; cp < 4; ++cp) {
         if (t > 0) ok = mbar_wait(&ms.bar_pv[cp], (t - 1) & 1) && ok;
         const int kc = 2 * cp + (seg >> 1), u0 = (seg & 1) * 4;
+        if (!WIN || t < n_sel) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int j = jr + 64 * hf;
-          const uint4 c = rc[2 * cp + hf];
-          const uint32_t r = rs[2 * cp + hf];
-          const uint32_t sa = e4m3_to_f16x2_dup(r & 0xFF), sb = e4m3_to_f16x2_dup(r >> 8);
-          uint8_t *row = sm + kPfOffK + kc * kPfKChunk + j * 128;
-          *reinterpret_cast<uint4 *>(row + (((u0 + 0) ^ (j & 7)) << 4)) = dequant8(c.x, sa);
-          *reinterpret_cast<uint4 *>(row + (((u0 + 1) ^ (j & 7)) << 4)) = dequant8(c.y, sa);
-          *reinterpret_cast<uint4 *>(row + (((u0 + 2) ^ (j & 7)) << 4)) = dequant8(c.z, sb);
-          *reinterpret_cast<uint4 *>(row + (((u0 + 3) ^ (j & 7)) << 4)) = dequant8(c.w, sb);
+          for (int hf = 0; hf < 2; ++hf) {
+            const int j = jr + 64 * hf;
+            const uint4 c = rc[2 * cp + hf];
+            const uint32_t r = rs[2 * cp + hf];
+            const uint32_t sa = e4m3_to_f16x2_dup(r & 0xFF), sb = e4m3_to_f16x2_dup(r >> 8);
+            uint8_t *row = sm + kPfOffK + kc * kPfKChunk + j * 128;
+            *reinterpret_cast<uint4 *>(row + (((u0 + 0) ^ (j & 7)) << 4)) = dequant8(c.x, sa);
+            *reinterpret_cast<uint4 *>(row + (((u0 + 1) ^ (j & 7)) << 4)) = dequant8(c.y, sa);
+            *reinterpret_cast<uint4 *>(row + (((u0 + 2) ^ (j & 7)) << 4)) = dequant8(c.z, sb);
+            *reinterpret_cast<uint4 *>(row + (((u0 + 3) ^ (j & 7)) << 4)) = dequant8(c.w, sb);
+          }
+        } else {  // window tile: row jr from 32 E4M3 bytes, row jr + 64 empty
+          uint8_t *row = sm + kPfOffK + kc * kPfKChunk + jr * 128;
+          uint8_t *row2 = row + 64 * 128;
+          const uint32_t b[8] = {rc[2 * cp].x, rc[2 * cp].y, rc[2 * cp].z, rc[2 * cp].w,
+                                 rc[2 * cp + 1].x, rc[2 * cp + 1].y, rc[2 * cp + 1].z,
+                                 rc[2 * cp + 1].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 w;
+            w.x = e4m3x2_to_f16x2(b[2 * k] & 0xFFFF);
+            w.y = e4m3x2_to_f16x2(b[2 * k] >> 16);
+            w.z = e4m3x2_to_f16x2(b[2 * k + 1] & 0xFFFF);
+            w.w = e4m3x2_to_f16x2(b[2 * k + 1] >> 16);
+            *reinterpret_cast<uint4 *>(row + (((u0 + k) ^ (jr & 7)) << 4)) = w;
+            *reinterpret_cast<uint4 *>(row2 + (((u0 + k) ^ (jr & 7)) << 4)) =
+                make_uint4(0, 0, 0, 0);
+          }
         }
         fence_async_smem();
         mbar_arrive(&ms.bar_dq[cp]);
@@ -498,14 +562,18 @@ bool attn_prefill_supported(int H) { return H <= 64 && encode_fn() != nullptr; }
 cudaError_t launch_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_seq,
                                 const uint8_t *codes, const uint8_t *sf, const int64_t *cu_ctx,
                                 const int32_t *idx, int topk, float scale, void *out_bf16,
-                                float *lse, cudaStream_t st) {
+                                float *lse, cudaStream_t st, const int32_t *q_vis,
+                                const uint8_t *swa_kv, int ring, int n_win) {
   if (T == 0) return cudaSuccess;
-  cudaError_t e = set_smem_once(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kPfSmem);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(attn_prefill_kernel, dim3(T), dim3(kPfThreads), kPfSmem, st,
-                 static_cast<const uint16_t *>(q_bf16), H, q_seq, codes, sf, cu_ctx, idx, topk,
-                 scale * 1.4426950408889634f, static_cast<uint16_t *>(out_bf16), lse);
+  auto go = [&](auto kern) {
+    cudaError_t err = set_smem_once(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(kern, dim3(T), dim3(kPfThreads), kPfSmem, st,
+                      static_cast<const uint16_t *>(q_bf16), H, q_seq, codes, sf, cu_ctx, idx,
+                      topk, scale * 1.4426950408889634f, static_cast<uint16_t *>(out_bf16), lse,
+                      q_vis, swa_kv, ring, n_win);
+  };
+  const cudaError_t e = n_win > 0 ? go(attn_prefill_kernel<true>) : go(attn_prefill_kernel<false>);
   note_launches(1);
   return e;
 }

@@ -205,20 +205,27 @@ cudaError_t launch_attn(const void *q_bf16, const uint8_t *q_codes, const uint8_
 size_t attn_workspace_bytes(int nq, int H, int topk);
 
 // Tensor-core prefill attention (attn_prefill.cu): one CTA per query token, H <= 64; the query
-// is FP4-quantised inside the kernel.
+// is FP4-quantised inside the kernel.  With n_win > 0 the last n_win of the q_vis[i] positions
+// token i sees add their local rows (swa_kv, ring) to the same softmax.
 bool attn_prefill_supported(int H);
 cudaError_t launch_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_seq,
                                 const uint8_t *codes, const uint8_t *sf, const int64_t *cu_ctx,
                                 const int32_t *idx, int topk, float scale, void *out_bf16,
-                                float *lse, cudaStream_t st);
+                                float *lse, cudaStream_t st, const int32_t *q_vis = nullptr,
+                                const uint8_t *swa_kv = nullptr, int ring = 1, int n_win = 0);
 
 // Tensor-core decode attention (attn_mma.cu): H <= 64, one CTA per 32 selected rows and 32
-// heads.
-bool attn_mma_supported(int H, int topk);
-size_t attn_mma_workspace_bytes(int nq, int H, int topk);
+// heads; with n_win > 0 (swa_kv, ring) the window's local rows join the same softmax.
+bool attn_mma_supported(int H, int topk, int n_win = 0);
+size_t attn_mma_workspace_bytes(int nq, int H, int topk, int n_win = 0);
 cudaError_t launch_attn_mma(const void *q_bf16, int nq, int H, const uint8_t *codes,
                             const uint8_t *sf, const int64_t *cu_ctx, const int32_t *idx,
                             int topk, float scale, void *out_bf16, float *lse, void *workspace,
-                            cudaStream_t st);
+                            cudaStream_t st, const uint8_t *swa_kv = nullptr, int ring = 1,
+                            int n_win = 0);
+
+// FP8 (E4M3) local sliding-window rows: bf16 -> E4M3, round to nearest even, saturating.
+cudaError_t launch_fp8_quant(const void *x, int64_t n_rows, int d, const int64_t *out_rows,
+                             uint8_t *out, cudaStream_t st);
 
 }  // namespace csa2

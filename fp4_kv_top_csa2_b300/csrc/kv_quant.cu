@@ -90,3 +90,53 @@ cudaError_t launch_kv_quant(const void *x, int64_t n_rows, int d, const int64_t 
 }
 
 }  // namespace csa2
+
+// ------------------------------------------------------------------------------------------
+// FP8 local sliding-window rows ("DeepSeek V4.1-Flash", aiwiki.ai, section "KV-cache formats and
+// bounded replay": the local sliding-window KV is stored in FP8): every bf16 element -> E4M3
+// ("fn"), round to nearest even, saturating at +-448, sign kept, no scale.  One thread per 16
+// elements: two 16-byte loads, eight two-element conversions, one 16-byte store.
+// ------------------------------------------------------------------------------------------
+namespace csa2 {
+
+__device__ __forceinline__ uint32_t bf16x2_to_e4m3x2(uint32_t v) {
+  uint16_t r;
+  // the first source lands in the upper byte: channel 2i (low bf16) goes to the low byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(bf16_hi(v)), "f"(bf16_lo(v)));
+  return r;
+}
+
+__global__ void __launch_bounds__(256) fp8_quant_kernel(const uint16_t *__restrict__ x,
+                                                        int64_t n_rows, int d,
+                                                        const int64_t *__restrict__ out_rows,
+                                                        uint8_t *__restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int per_row = d >> 4;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_rows * per_row) return;
+  const int64_t row = i / per_row;
+  const int g = (int)(i - row * per_row);
+  const int64_t orow = out_rows ? out_rows[row] : row;
+  const uint4 *src = reinterpret_cast<const uint4 *>(x + row * d + 16 * g);
+  const uint4 a = __ldg(src), b = __ldg(src + 1);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    o[k] = bf16x2_to_e4m3x2(w[2 * k]) | (bf16x2_to_e4m3x2(w[2 * k + 1]) << 16);
+  *reinterpret_cast<uint4 *>(out + orow * d + 16 * g) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+cudaError_t launch_fp8_quant(const void *x, int64_t n_rows, int d, const int64_t *out_rows,
+                             uint8_t *out, cudaStream_t st) {
+  if (n_rows == 0) return cudaSuccess;
+  const int64_t threads = n_rows * (d >> 4);
+  const cudaError_t e = launch_pdl(fp8_quant_kernel, dim3((unsigned)((threads + 255) / 256)),
+                                   dim3(256), 0, st, static_cast<const uint16_t *>(x), n_rows, d,
+                                   out_rows, out);
+  note_launches(1);
+  return e;
+}
+
+}  // namespace csa2

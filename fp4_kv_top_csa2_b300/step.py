@@ -8,7 +8,9 @@ Decode (one token per sequence; every layer of the workload's mode list, in orde
   * Reindex layer: its own index query/weights over the pool, Top-K, sparse attention;
   * Reuse layer: sparse attention with the most recent layer's indices.
 Prefill: the T new rows are quantised into the cache, the indexer selects Top-K per query token
-(query i sees positions [0, P0 + i]), then sparse prefill attention.
+(query i sees positions [0, P0 + i]), then sparse prefill attention.  With Reindex layers in the
+mode list the first Full layer also builds a candidate pool per query token, which the Reindex
+layers search, exactly as in the hierarchical decoder.
 
 All device buffers (cache, queries, outputs, workspaces) are allocated once here with torch
 (caller-side allocation); `run()` only enqueues C-ABI calls.
@@ -33,7 +35,7 @@ import math
 import torch
 
 from . import csa2
-from .synth import BLOCK, D, new_token_rows
+from .synth import BLOCK, D, new_token_rows, swa_new_rows
 
 
 class _Arena:
@@ -78,6 +80,8 @@ class Step:
             if "q_idx" in L:
                 in_specs.append((f"q_idx{i}", tuple(L["q_idx"].shape), L["q_idx"].dtype))
                 in_specs.append((f"w{i}", tuple(L["w"].shape), L["w"].dtype))
+            if w.n_win:
+                in_specs.append((f"swa_new{i}", (self.nq, D), torch.bfloat16))
             out_specs.append((f"out{i}", (self.nq, w.H, D), torch.bfloat16))
         self.in_arena = _Arena(in_specs, dev)
         self.out_arena = _Arena(out_specs, dev)
@@ -86,8 +90,12 @@ class Step:
         if build_cache:  # the cache as it stands before the step (all rows), quantised on the GPU
             csa2.csa2_kv_quant_fp4(self.kv_bf16, self.codes, self.sf)
         self.layers = []
+        self.swa_ring = inputs.get("swa_ring", 1)
+        self.swa_rows = swa_new_rows(inputs).to(dev) if w.n_win else None
         nb = (self.max_vis + BLOCK - 1) // BLOCK
-        hier = w.kind == "hier"
+        # the hierarchical indexer: a candidate pool built by the first Full layer, searched by
+        # the Reindex layers (decode and chunked prefill alike)
+        hier = any(m == "reindex" for m in w.modes)
         for i, L in enumerate(inputs["layers"]):
             d = {"mode": L["mode"], "q_attn": self.in_arena.views[f"q_attn{i}"]}
             d["q_attn"].copy_(L["q_attn"])
@@ -97,6 +105,12 @@ class Step:
                 d["w"] = self.in_arena.views[f"w{i}"]
                 d["w"].copy_(L["w"])
                 d["idx"] = torch.empty((self.nq, w.topk), dtype=torch.int32, device=dev)
+            if w.n_win:  # the layer's local FP8 ring, as it stands before the step
+                d["swa_kv"] = torch.empty((L["swa_bf16"].shape[0], D), dtype=torch.uint8,
+                                          device=dev)
+                csa2.csa2_swa_kv_quant_fp8(L["swa_bf16"].to(dev), d["swa_kv"])
+                d["swa_new"] = self.in_arena.views[f"swa_new{i}"]
+                d["swa_new"].copy_(L["swa_new"])
             d["out"] = self.out_arena.views[f"out{i}"]
             d["lse"] = torch.empty((self.nq, w.H), dtype=torch.float32, device=dev)
             self.layers.append(d)
@@ -135,9 +149,13 @@ class Step:
         self.ws_pool = (csa2.workspace(csa2.csa2_hier_candidate_pool_workspace_size(
             self.nq, nb, w.n_pool_blocks), dev) if hier else None)
         if w.kind == "prefill":
-            ws_a = csa2.csa2_sparse_attn_prefill_workspace_size(self.nq, w.H, w.topk)
+            ws_a = (csa2.csa2_sparse_swa_attn_prefill_workspace_size(self.nq, w.H, w.topk, w.n_win)
+                    if w.n_win else
+                    csa2.csa2_sparse_attn_prefill_workspace_size(self.nq, w.H, w.topk))
         else:
-            ws_a = csa2.csa2_sparse_attn_decode_workspace_size(self.nq, w.H, w.topk)
+            ws_a = (csa2.csa2_sparse_swa_attn_decode_workspace_size(self.nq, w.H, w.topk, w.n_win)
+                    if w.n_win else
+                    csa2.csa2_sparse_attn_decode_workspace_size(self.nq, w.H, w.topk))
         self.ws_attn = csa2.workspace(ws_a, dev)
         for i, L in enumerate(self.layers):
             L["ws_attn"] = (csa2.workspace(ws_a, dev) if self.overlap_layers and i > 0
@@ -160,6 +178,21 @@ class Step:
             out_block_max=block_max, ws=layer["ws_index"], stream=stream)
 
     def attend(self, layer, idx, stream=None):
+        if self.w.n_win:  # the layer's local window joins the same softmax
+            # this step's tokens' local rows go into the ring first
+            csa2.csa2_swa_kv_quant_fp8(layer["swa_new"], layer["swa_kv"], out_rows=self.swa_rows,
+                                       stream=stream)
+            if self.w.kind == "prefill":
+                csa2.csa2_sparse_swa_attn_prefill(
+                    layer["q_attn"], self.q_seq, self.q_vis, self.codes, self.sf, self.cu_ctx,
+                    idx, layer["swa_kv"], self.swa_ring, self.w.n_win, self.scale, layer["out"],
+                    layer["lse"], ws=layer["ws_attn"], stream=stream)
+            else:
+                csa2.csa2_sparse_swa_attn_decode(
+                    layer["q_attn"], self.codes, self.sf, self.cu_ctx, idx, layer["swa_kv"],
+                    self.swa_ring, self.w.n_win, self.scale, layer["out"], layer["lse"],
+                    ws=layer["ws_attn"], stream=stream)
+            return
         if self.w.kind == "prefill":
             csa2.csa2_sparse_attn_prefill(layer["q_attn"], self.q_seq, self.codes, self.sf,
                                           self.cu_ctx, idx, self.scale, layer["out"],
@@ -266,6 +299,7 @@ class Step:
             "index_keys_reindex": n_re * self.nq * w.n_pool_blocks * BLOCK * key_row,
             "gathered_rows": n_att * self.nq * w.topk * row,
             "q_out": n_att * self.nq * w.H * D * 2 * 2,
+            "local_window_rows": n_att * self.nq * min(w.n_win, self.max_vis) * D if w.n_win else 0,
         }
         by["total"] = sum(by.values())
         return by

@@ -14,7 +14,9 @@ Workloads (all seeded, torch CPU generator):
   * attention queries: N(0,1) bf16, [heads, 512];
   * ragged decode: per-sequence context lengths U{lo..hi}; a fraction of index-key positions are
     near duplicates of a random earlier position of the same sequence (its float key plus
-    N(0, 1e-3) noise before the FP8 cast), which yields exact FP8 ties and 1-ulp near ties.
+    N(0, 1e-3) noise before the FP8 cast), which yields exact FP8 ties and 1-ulp near ties;
+  * local sliding-window rows (per layer): N(0,1) * sigma_c bf16, like the main-KV rows, for the
+    ring buffer as it stands before the step and for the step's new tokens.
 """
 from __future__ import annotations
 
@@ -44,6 +46,7 @@ class Workload:
     modes: tuple = ("full",)
     dup_frac: float = 0.0
     ragged: tuple | None = None  # (lo, hi) for ragged lengths drawn per sequence
+    n_win: int = 0  # local sliding window per layer (0: none)
     seed: int = 0
     extra: dict = field(default_factory=dict)
 
@@ -61,6 +64,15 @@ WORKLOADS = {
         modes=("full", "reindex", "reindex", "reindex", "reuse", "reuse")),
     "prefill_t4096_p262144": Workload("prefill_t4096_p262144", "prefill", B=1, L=(262144,),
                                       T=4096, H=64),
+    # chunked prefill through the hierarchical indexer: the first Full layer builds a 2,048-block
+    # candidate pool per query token, three Reindex layers rescore it, two Reuse layers reuse
+    # the hierarchical decoder with every layer's local sliding window (128 FP8 local rows)
+    "hier_decode_l1m_swa128": Workload(
+        "hier_decode_l1m_swa128", "hier", B=1, L=(1 << 20,), H=64,
+        modes=("full", "reindex", "reindex", "reindex", "reuse", "reuse"), n_win=128),
+    "prefill_hier_t4096_p262144": Workload(
+        "prefill_hier_t4096_p262144", "prefill", B=1, L=(262144,), T=4096, H=64,
+        modes=("full", "reindex", "reindex", "reindex", "reuse", "reuse")),
 }
 
 
@@ -153,15 +165,35 @@ def make_inputs(w: Workload, with_kv: bool = True) -> dict:
     out["q_vis"] = q_vis
     out["max_vis"] = int(q_vis.max()) if nq else 0
     layers = []
+    ring = swa_ring(w)
     for mode in w.modes:
         layer = {"mode": mode}
         if mode in ("full", "reindex"):
             layer["q_idx"] = _index_vectors((nq, w.Hi, w.Di), w.idx_dtype, g)
             layer["w"] = torch.rand((nq, w.Hi), generator=g)
         layer["q_attn"] = torch.randn((nq, w.H, D), generator=g).to(torch.bfloat16)
+        if w.n_win:
+            layer["swa_bf16"] = _kv_rows(len(lengths) * ring, sigma, g)  # the ring before
+            layer["swa_new"] = _kv_rows(nq, sigma, g)                    # this step's tokens
         layers.append(layer)
     out["layers"] = layers
+    out["swa_ring"] = ring
     return out
+
+
+def swa_ring(w: Workload) -> int:
+    """Local rows kept per sequence: the window, plus the chunk's own tokens for a prefill."""
+    if not w.n_win:
+        return 1
+    return w.n_win + (w.T - 1 if w.kind == "prefill" else 0)
+
+
+def swa_new_rows(inputs: dict) -> torch.Tensor:
+    """Ring rows the step's new tokens' local rows go to (query token n: sequence q_seq[n] at
+    position q_vis[n] - 1)."""
+    ring = inputs["swa_ring"]
+    pos = inputs["q_vis"].to(torch.int64) - 1
+    return inputs["q_seq"].to(torch.int64) * ring + pos % ring
 
 
 def new_token_rows(inputs: dict) -> torch.Tensor:

@@ -271,6 +271,54 @@ int csa2_sparse_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_
                              void *stream);
 
 /* ------------------------------------------------------------------------------------------ */
+/* 6. The local sliding-window branch                                                           */
+/* ------------------------------------------------------------------------------------------ */
+/*
+ * [WIKI] "Compressed Sparse Attention 2": every CSA2 layer creates, besides its query, its own
+ * local sliding-window keys and values; [WIKI] "KV-cache formats and bounded replay": the local
+ * sliding-window KV is stored in FP8 (the main global KV in FP4).  The pages give neither the
+ * window length nor how the two attentions combine; this library defines:
+ *   - local row: one 512-channel row per token and layer, each element E4M3 ("fn", round to
+ *     nearest even, saturating at +-448, sign kept), no scale.  K = V = the local row.
+ *   - ring buffer: sequence b's local rows occupy rows [b*ring, (b+1)*ring) of swa_kv; position t
+ *     is row b*ring + t % ring (so only the last `ring` positions are kept).
+ *   - window: a query that sees V positions attends to the local rows of its last
+ *     min(n_win, V) positions (its own included), n_win <= ring.
+ *   - one softmax over the union: s = softmax_scale * <q_h, row> over the selected FP4 rows
+ *     (as csa2_sparse_attn_decode / _prefill) and the window's local rows together; out and lse
+ *     are over the union (equivalently the two partial attentions merged by their lse).
+ */
+
+/* bf16 rows -> E4M3 local rows.  x_bf16 [n_rows, d] (d a multiple of 16, <= 4096); out_rows
+ * NULL (row i) or [n_rows] int64 destination rows of swa_kv [*, d] uint8.  Bit-exact. */
+int csa2_swa_kv_quant_fp8(const void *x_bf16, int64_t n_rows, int d, const int64_t *out_rows,
+                          uint8_t *swa_kv, void *stream);
+
+/* Decode: csa2_sparse_attn_decode plus the window of each sequence's last min(n_win, L_b)
+ * positions (L_b = cu_ctx[b+1] - cu_ctx[b]; the cache already holds the current token).
+ * swa_kv [B*ring, 512] uint8; 1 <= ring; 0 <= n_win <= ring (0: no window); H <= 64 (else
+ * CSA2_ERR_UNSUPPORTED); ceil(topk/32) + ceil(n_win/32) <= 256.  Workspace: see the size query. */
+size_t csa2_sparse_swa_attn_decode_workspace_size(int B, int H, int topk, int n_win);
+int csa2_sparse_swa_attn_decode(const void *q_bf16, int B, int H, const uint8_t *codes,
+                                const uint8_t *sf, const int64_t *cu_ctx, const int32_t *idx,
+                                int topk, const uint8_t *swa_kv, int ring, int n_win,
+                                float softmax_scale, void *out_bf16, float *lse, void *workspace,
+                                size_t ws_bytes, void *stream);
+
+/* Chunked prefill: csa2_sparse_attn_prefill plus, for token i, the window of the last
+ * min(n_win, q_vis[i]) positions of its sequence q_seq[i] (q_vis [T] int32 as given to the
+ * indexer: token i sees positions [0, q_vis[i])).  swa_kv [B*ring, 512] uint8 must already hold
+ * the local rows of every window position, the chunk's own tokens included, so ring >= n_win +
+ * T - 1 for a chunk of T tokens of one sequence.  H <= 64.  Needs no workspace (size 0). */
+size_t csa2_sparse_swa_attn_prefill_workspace_size(int T, int H, int topk, int n_win);
+int csa2_sparse_swa_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_seq,
+                                 const int32_t *q_vis, const uint8_t *codes, const uint8_t *sf,
+                                 const int64_t *cu_ctx, int B, const int32_t *idx, int topk,
+                                 const uint8_t *swa_kv, int ring, int n_win, float softmax_scale,
+                                 void *out_bf16, float *lse, void *workspace, size_t ws_bytes,
+                                 void *stream);
+
+/* ------------------------------------------------------------------------------------------ */
 /* Device status                                                                                */
 /* ------------------------------------------------------------------------------------------ */
 /*

@@ -1,4 +1,4 @@
-"""Full-size parity: the five workloads at their stated sizes, run through the same Step (and so
+"""Full-size parity: the seven workloads at their stated sizes, run through the same Step (and so
 the same launch configuration) that bench.py times, checked against the oracle.
 
 Each check uses the GPU's own upstream result as the oracle's input where a step depends on an
@@ -6,7 +6,9 @@ earlier one (the pool is rebuilt by the oracle from the GPU's block maxima, atte
 recomputed by the oracle on the GPU's indices), so every call is judged on its own; the
 upstream results are themselves checked against the oracle.  Chunked prefill is checked on 64
 query tokens spread evenly over the chunk (first and last included): the oracle scores all 262,144+
-visible positions for each of them.
+visible positions for each of them.  The hierarchical prefill (a candidate pool per query token,
+three Reindex and two Reuse layers) checks every layer's selection on the same 64 tokens and its
+six attentions on 16 of them.
 """
 import numpy as np
 import pytest
@@ -57,7 +59,8 @@ def _check_pool(gpu_pool, gpu_bm, ref_bm, vis, n_pool):
 
 @pytest.mark.parametrize("name", ["decode_b1_l4096_bf16idx", "decode_b8_l65536",
                                   "decode_ragged_b32", "hier_decode_l1m",
-                                  "prefill_t4096_p262144"])
+                                  "hier_decode_l1m_swa128", "prefill_t4096_p262144",
+                                  "prefill_hier_t4096_p262144"])
 def test_workload_full_size(mods, name):
     step, synth = mods
     w = synth.WORKLOADS[name]
@@ -79,6 +82,8 @@ def test_workload_full_size(mods, name):
         queries = sorted(set(np.linspace(0, nq - 1, 62).astype(int).tolist() + [1, nq - 2]))
     else:
         queries = list(range(w.B))
+    # attention: every sampled query of a one-layer step; with six layers every fourth one
+    attn_queries = queries if len(st.layers) == 1 or w.kind != "prefill" else queries[::4]
 
     last_idx = None
     for li, L in enumerate(st.layers):
@@ -91,7 +96,7 @@ def test_workload_full_size(mods, name):
                                           w.topk, cand_blocks=cand, queries=queries)
             for n in queries:
                 check_topk(gpu_idx[n], ref[n], w.topk, f"{name} layer {li} ({mode}) query {n}")
-            if mode == "full" and st.pool is not None and li == 0:
+            if mode == "full" and st.pool is not None and li == 0:  # the pool per query
                 gbm = st.bm.cpu().numpy()
                 gpool = st.pool.cpu().numpy()
                 for n in queries:
@@ -102,13 +107,21 @@ def test_workload_full_size(mods, name):
         # attention on the GPU's own indices
         q_attn = _np(inp["layers"][li]["q_attn"])
         out_b, lse = _bits(L["out"]), L["lse"].cpu().numpy()
-        if w.kind == "prefill":
+        if w.n_win:  # the layer's local window: its new FP8 rows, then one softmax over both
+            swa = L["swa_kv"].cpu().numpy()
+            new_rows = st.swa_rows.cpu().numpy()
+            assert np.array_equal(swa[new_rows],
+                                  oracle.fp8_quant(_np(inp["layers"][li]["swa_new"])))
+            ref_a = oracle.sparse_swa_attn_queries(
+                q_attn, q_seq, q_vis, codes, sf, cu, last_idx, swa, st.swa_ring, w.n_win,
+                st.scale, queries=attn_queries, quantize_query=w.kind == "prefill")
+        elif w.kind == "prefill":
             ref_a = oracle.sparse_attn_prefill(q_attn, q_seq, codes, sf, cu, last_idx,
-                                               st.scale, tokens=queries)
+                                               st.scale, tokens=attn_queries)
         else:
             ref_a = oracle.sparse_attn_decode(q_attn, codes, sf, cu, last_idx, st.scale,
-                                              seqs=queries)
-        for n in queries:
+                                              seqs=attn_queries)
+        for n in attn_queries:
             o, l = ref_a[n]
             check_attn(out_b[n], lse[n], o, l, oracle.double_to_bf16(o),
                        f"{name} layer {li} ({mode}) attention {n}")
