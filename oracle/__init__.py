@@ -74,6 +74,7 @@ def _load():
     lib.orc_sparse_attn.argtypes = [P, i32, i32, P, P, P, i32, ctypes.c_double, P, P]
     lib.orc_fp8_quant.argtypes = [P, i64, P]
     lib.orc_sparse_swa_attn.argtypes = [P, i32, i32, P, P, P, i32, P, i32, ctypes.c_double, P, P]
+    lib.orc_index_keys_from_kv.argtypes = [P, P, i64, i32, P, i32, P, P]
     lib.orc_bf16_to_double.argtypes = [P, i64, P]
     lib.orc_double_to_bf16_array.argtypes = [P, i64, P]
     _lib = lib
@@ -325,3 +326,20 @@ def sparse_swa_attn_queries(q_bf16, q_seq, q_vis, codes, sf, cu_ctx, idx, swa_kv
         q = quantize_query_fp4(qn) if quantize_query else bf16_to_double(qn)
         res[n] = sparse_swa_attn(q, codes[lo:hi], sf[lo:hi], idx[n], loc, scale)
     return res
+
+
+# ----------------------------------------------------------------------------------------------
+# f3: index keys derived from main-KV entries
+# ----------------------------------------------------------------------------------------------
+def index_keys_from_kv(codes: np.ndarray, sf: np.ndarray, W_bf16: np.ndarray):
+    """FP4 rows (codes [n, d/2], sf [n, d/16]) and a bf16 projection W [Di, d] (uint16 bits) ->
+    (keys [n, Di] E4M3 bytes, k_scale [n] fp32)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    W = np.ascontiguousarray(W_bf16, dtype=np.uint16)
+    n, d = codes.shape[0], codes.shape[1] * 2
+    Di = W.shape[0]
+    keys = np.empty((n, Di), dtype=np.uint8)
+    ks = np.empty(n, dtype=np.float32)
+    _load().orc_index_keys_from_kv(_p(codes), _p(sf), n, d, _p(W), Di, _p(keys), _p(ks))
+    return keys, ks

@@ -394,3 +394,41 @@ void orc_sparse_swa_attn(const double *q, int H, int d, const uint8_t *codes, co
     free(rows);
     free(s);
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* f3: index keys derived from main-KV entries ([WIKI] "Compressed Sparse Attention 2": CSA2    */
+/* derives index keys from main KV entries rather than through a separate hidden-state path)   */
+/* ------------------------------------------------------------------------------------------ */
+
+/* [SPEC] for each cached row t: x = the dequantised FP4 row (d channels), W the layer's index-key
+ * projection [Di, d] (bf16):
+ *   y_i   = fp32( sum_c W[i,c] * x[c] )     (exact in double: at most 8 x 6 significant bits per
+ *                                            product, then one rounding to fp32)
+ *   s     = fp32( max_i |y_i| / 448 )       (448 = largest E4M3 value; s = 1 if every y_i is 0)
+ *   key_i = E4M3( fp32(y_i / s) )           (round to nearest even, saturating, sign kept)
+ * keys [n, Di] E4M3 and k_scale [n] = s are the indexer's k_idx and k_scale: the score uses
+ * s * <q_h, key>. */
+void orc_index_keys_from_kv(const uint8_t *codes, const uint8_t *sf, int64_t n_rows, int d,
+                            const uint16_t *W, int Di, uint8_t *keys, float *k_scale)
+{
+    double *x = (double *)malloc(sizeof(double) * (size_t)d);
+    float *y = (float *)malloc(sizeof(float) * (size_t)Di);
+    for (int64_t r = 0; r < n_rows; ++r) {
+        orc_kv_dequant_fp4(codes + r * (d / 2), sf + r * (d / 16), 1, d, x);
+        float amax = 0.0f;
+        for (int i = 0; i < Di; ++i) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) acc += (double)orc_bf16_to_float(W[(size_t)i * d + c]) * x[c];
+            y[i] = (float)acc;
+            if (fabsf(y[i]) > amax) amax = fabsf(y[i]);
+        }
+        float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+        k_scale[r] = s;
+        for (int i = 0; i < Di; ++i) {
+            float v = y[i] / s;
+            keys[r * Di + i] = (uint8_t)((signbit(v) ? 0x80 : 0) | orc_e4m3_encode(fabsf(v)));
+        }
+    }
+    free(x);
+    free(y);
+}
