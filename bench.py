@@ -316,6 +316,7 @@ def run_ours(args, rank, world):
                                   for name in DECODE_CONFIGS}
         # the headline step with every layer's local sliding window (128 FP8 local rows)
         line["hier_decode_swa"] = run_decode_config(HEADLINE_SWA, args, dev, peaks, flush)
+        line["index_keys"] = run_index_keys(args, dev, peaks, flush)
     if args.prefill and rank == 0:
         line["prefill"] = run_prefill(args, dev, peaks)
         line["prefill_hier"] = run_prefill_hier(args, dev)
@@ -446,6 +447,28 @@ def run_decode_config(name, args, dev, peaks, flush):
     del st
     torch.cuda.empty_cache()
     return out
+
+
+def run_index_keys(args, dev, peaks, flush, n_rows=1 << 20):
+    """Index keys derived from a 1,048,576-row FP4 cache (the cache build of the 1M-context
+    workload): 2 * 128 * 512 FLOP per row on the tensor cores, 288 B read and 132 B written."""
+    import torch
+    from fp4_kv_top_csa2_b300 import csa2
+    g = torch.Generator(device=dev).manual_seed(0)
+    codes = torch.randint(0, 256, (n_rows, 256), dtype=torch.uint8, device=dev, generator=g)
+    sf = torch.randint(0x28, 0x48, (n_rows, 32), dtype=torch.uint8, device=dev, generator=g)
+    W = (torch.randn(128, 512, device=dev, generator=g) / 16).to(torch.bfloat16)
+    keys = torch.empty((n_rows, 128), dtype=torch.uint8, device=dev)
+    ks = torch.empty(n_rows, dtype=torch.float32, device=dev)
+    ms = time_graph(lambda s: csa2.csa2_index_keys_from_kv(codes, sf, W, keys, ks, stream=s),
+                    args.steps, flush)
+    flops = 2.0 * 128 * 512 * n_rows
+    by = n_rows * (288 + 128 + 4)
+    tf = flops / (ms / 1e3) / 1e12
+    return {"rows": n_rows, "ms": round(ms, 4), "rows_per_s": round(n_rows / (ms / 1e3), 1),
+            "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+            "gbs": round(by / (ms / 1e3) / 1e9, 1),
+            "frac_of_hbm": round(by / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
 
 
 def run_e2e(st, steps, dev, world=1, graph=False):

@@ -48,6 +48,7 @@ def _load() -> ctypes.CDLL:
         "csa2_sparse_attn_decode": (I, [P, I, I, P, P, P, P, I, F, P, P, P, SZ, P]),
         "csa2_sparse_attn_prefill_workspace_size": (SZ, [I, I, I]),
         "csa2_sparse_attn_prefill": (I, [P, I, I, P, P, P, P, I, P, I, F, P, P, P, SZ, P]),
+        "csa2_index_keys_from_kv": (I, [P, P, I64, P, P, I, P, P, P]),
         "csa2_swa_kv_quant_fp8": (I, [P, I64, I, P, P, P]),
         "csa2_sparse_swa_attn_decode_workspace_size": (SZ, [I, I, I, I]),
         "csa2_sparse_swa_attn_decode": (I, [P, I, I, P, P, P, P, I, P, I, I, F, P, P, P, SZ, P]),
@@ -208,6 +209,15 @@ def csa2_sparse_attn_prefill(q_bf16, q_seq, codes, sf, cu_ctx, idx, softmax_scal
     _check("csa2_sparse_attn_prefill", lib.csa2_sparse_attn_prefill(
         _ptr(q_bf16), T, H, _ptr(q_seq), _ptr(codes), _ptr(sf), _ptr(cu_ctx), B, _ptr(idx), topk,
         float(softmax_scale), _ptr(out_bf16), _ptr(lse), wp, wn, _stream(stream)))
+
+
+def csa2_index_keys_from_kv(codes, sf, w_bf16, k_idx, k_scale, rows=None, n_rows=None,
+                            stream=None):
+    """Index keys (E4M3) and their per-row scales derived from the FP4 cache rows."""
+    n = n_rows if n_rows is not None else (rows.numel() if rows is not None else codes.shape[0])
+    _check("csa2_index_keys_from_kv", lib.csa2_index_keys_from_kv(
+        _ptr(codes), _ptr(sf), n, _ptr(rows), _ptr(w_bf16), w_bf16.shape[0], _ptr(k_idx),
+        _ptr(k_scale), _stream(stream)))
 
 
 def csa2_swa_kv_quant_fp8(x_bf16, swa_kv, out_rows=None, stream=None):

@@ -423,6 +423,23 @@ int csa2_sparse_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_
   return cuda_status(e);
 }
 
+// ---- index keys derived from main-KV rows -------------------------------------------------
+
+int csa2_index_keys_from_kv(const uint8_t *codes, const uint8_t *sf, int64_t n_rows,
+                            const int64_t *rows, const void *w_bf16, int Di, uint8_t *k_idx,
+                            float *k_scale, void *stream) {
+  if (n_rows < 0 || n_rows > ((int64_t)1 << 31) || Di != 128) return CSA2_ERR_INVALID_ARG;
+  if (n_rows == 0) return CSA2_OK;
+  if (!codes || !sf || !w_bf16 || !k_idx || !k_scale) return CSA2_ERR_INVALID_ARG;
+  const void *ptrs[] = {codes, sf, rows, w_bf16, k_idx, k_scale};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return CSA2_ERR_INVALID_ARG;
+  if (int r = check_device()) return r;
+  if (!index_keys_supported()) return CSA2_ERR_UNSUPPORTED;
+  return cuda_status(launch_index_keys(codes, sf, n_rows, rows, w_bf16, k_idx, k_scale,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 // ---- the local sliding-window branch ------------------------------------------------------
 
 int csa2_swa_kv_quant_fp8(const void *x_bf16, int64_t n_rows, int d, const int64_t *out_rows,

@@ -224,6 +224,13 @@ cudaError_t launch_attn_mma(const void *q_bf16, int nq, int H, const uint8_t *co
                             cudaStream_t st, const uint8_t *swa_kv = nullptr, int ring = 1,
                             int n_win = 0);
 
+// Index keys derived from main-KV rows (index_keys.cu): keys [*, 128] E4M3 and k_scale of the
+// given cache rows (rows NULL: rows 0..n_rows-1), projection W [128, 512] bf16.
+bool index_keys_supported();
+cudaError_t launch_index_keys(const uint8_t *codes, const uint8_t *sf, int64_t n_rows,
+                              const int64_t *rows, const void *w_bf16, uint8_t *keys,
+                              float *k_scale, cudaStream_t st);
+
 // FP8 (E4M3) local sliding-window rows: bf16 -> E4M3, round to nearest even, saturating.
 cudaError_t launch_fp8_quant(const void *x, int64_t n_rows, int d, const int64_t *out_rows,
                              uint8_t *out, cudaStream_t st);

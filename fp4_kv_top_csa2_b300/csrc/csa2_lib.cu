@@ -8,5 +8,6 @@
 #include "attn_simt.cu"
 #include "attn_mma.cu"
 #include "attn_prefill.cu"
+#include "index_keys.cu"
 #include "api.cu"
 #include "noalloc.cu"
