@@ -75,6 +75,7 @@ def _load():
     lib.orc_fp8_quant.argtypes = [P, i64, P]
     lib.orc_sparse_swa_attn.argtypes = [P, i32, i32, P, P, P, i32, P, i32, ctypes.c_double, P, P]
     lib.orc_index_keys_from_kv.argtypes = [P, P, i64, i32, P, i32, P, P]
+    lib.orc_attn_fp4pv.argtypes = [P, i32, i32, P, P, P, i32, ctypes.c_double, P, P]
     lib.orc_bf16_to_double.argtypes = [P, i64, P]
     lib.orc_double_to_bf16_array.argtypes = [P, i64, P]
     _lib = lib
@@ -343,3 +344,33 @@ def index_keys_from_kv(codes: np.ndarray, sf: np.ndarray, W_bf16: np.ndarray):
     ks = np.empty(n, dtype=np.float32)
     _load().orc_index_keys_from_kv(_p(codes), _p(sf), n, d, _p(W), Di, _p(keys), _p(ks))
     return keys, ks
+
+
+# ----------------------------------------------------------------------------------------------
+# f4: the full-FP4 PV variant of prefill attention
+# ----------------------------------------------------------------------------------------------
+def attn_fp4pv(q: np.ndarray, codes_seq, sf_seq, idx, scale):
+    """One token's FP4-dequantised query q [H, d] over its selected slots idx [K] (blocks of 16
+    consecutive slots): (out [H, d], lse [H])."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    H, d = q.shape
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    codes_seq = np.ascontiguousarray(codes_seq, dtype=np.uint8)
+    sf_seq = np.ascontiguousarray(sf_seq, dtype=np.uint8)
+    out = np.empty((H, d), dtype=np.float64)
+    lse = np.empty(H, dtype=np.float64)
+    _load().orc_attn_fp4pv(_p(q), H, d, _p(codes_seq), _p(sf_seq), _p(idx), idx.shape[0],
+                           float(scale), _p(out), _p(lse))
+    return out, lse
+
+
+def sparse_attn_prefill_fp4pv(q_bf16, q_seq, codes, sf, cu_ctx, idx, scale, tokens=None):
+    """Batch form of the full-FP4 PV prefill call: {i: (out, lse)} for the listed tokens."""
+    res = {}
+    tokens = range(q_bf16.shape[0]) if tokens is None else tokens
+    for i in tokens:
+        b = int(q_seq[i])
+        lo, hi = int(cu_ctx[b]), int(cu_ctx[b + 1])
+        qhat = quantize_query_fp4(np.ascontiguousarray(q_bf16[i]))
+        res[i] = attn_fp4pv(qhat, codes[lo:hi], sf[lo:hi], idx[i], scale)
+    return res

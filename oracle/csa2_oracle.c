@@ -432,3 +432,95 @@ void orc_index_keys_from_kv(const uint8_t *codes, const uint8_t *sf, int64_t n_r
     free(x);
     free(y);
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* f4: the full-FP4 PV variant of prefill attention (the workload asks for the PV product as a */
+/* block-scaled FP4 contraction too)                                                           */
+/* ------------------------------------------------------------------------------------------ */
+
+/* [SPEC] block-scaled FP4 value of x within a block whose largest magnitude is amax, with the
+ * main-KV rule: sc = E4M3(fp32(amax / 6)), value = E2M1(fp32(x / sc)) * sc (0 if sc == 0). */
+static double fp4_block_value(float x, float amax)
+{
+    int scode = orc_e4m3_encode(amax / 6.0f);
+    float sc = (float)orc_e4m3_value(scode);
+    if (sc == 0.0f) return 0.0;
+    return orc_e2m1_value(orc_e2m1_encode(x / sc)) * (double)sc;
+}
+
+/* [SPEC] For one query token (q = its FP4-dequantised query [H, d]) and its K selected slots
+ * (idx[j] < 0: an empty slot, a zero row that takes part in the blocks):
+ *   s_j = scale * <q_h, khat_j>;  m_h = max over valid slots;  p_j = fp32(exp(s_j - m_h)) (0 for
+ *   empty slots);
+ *   P: slots in blocks of 16 consecutive slots; per (head, block) Pt_j = fp4_block_value(p_j,
+ *      max_block p);
+ *   V: per (channel c, block) Vt_jc = fp4_block_value(khat_jc, max_block |khat_.c|);
+ *   out_hc = sum_j Pt_j Vt_jc / sum_j Pt_j;   lse_h = m_h + log(sum_j Pt_j)
+ * (no valid slot: out 0, lse -inf). */
+void orc_attn_fp4pv(const double *q, int H, int d, const uint8_t *codes, const uint8_t *sf,
+                    const int32_t *idx, int K, double scale, double *out, double *lse)
+{
+    int nb = (K + 15) / 16;
+    int kp = nb * 16;
+    double *rows = (double *)calloc((size_t)kp * d, sizeof(double));
+    double *vt = (double *)calloc((size_t)kp * d, sizeof(double));
+    double *s = (double *)malloc(sizeof(double) * kp);
+    float *p = (float *)malloc(sizeof(float) * kp);
+    double *pt = (double *)malloc(sizeof(double) * kp);
+    int nv = 0;
+    for (int j = 0; j < K; ++j) {
+        if (idx[j] < 0) continue;
+        ++nv;
+        orc_kv_dequant_fp4(codes + (int64_t)idx[j] * (d / 2), sf + (int64_t)idx[j] * (d / 16), 1,
+                           d, rows + (size_t)j * d);
+    }
+    for (int b = 0; b < nb; ++b)
+        for (int c = 0; c < d; ++c) {
+            float amax = 0.0f;
+            for (int j = 16 * b; j < 16 * b + 16; ++j) {
+                float a = fabsf((float)rows[(size_t)j * d + c]);
+                if (a > amax) amax = a;
+            }
+            for (int j = 16 * b; j < 16 * b + 16; ++j)
+                vt[(size_t)j * d + c] = fp4_block_value((float)rows[(size_t)j * d + c], amax);
+        }
+    for (int h = 0; h < H; ++h) {
+        double *o = out + (size_t)h * d;
+        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        if (nv == 0) { lse[h] = -INFINITY; continue; }
+        double m = -INFINITY;
+        for (int j = 0; j < kp; ++j) {
+            s[j] = -INFINITY;
+            if (j >= K || idx[j] < 0) continue;
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c) dot += q[(size_t)h * d + c] * rows[(size_t)j * d + c];
+            s[j] = scale * dot;
+            if (s[j] > m) m = s[j];
+        }
+        for (int j = 0; j < kp; ++j) p[j] = (s[j] == -INFINITY) ? 0.0f : (float)exp(s[j] - m);
+        double l = 0.0;
+        for (int b = 0; b < nb; ++b) {
+            float amax = 0.0f;
+            for (int j = 16 * b; j < 16 * b + 16; ++j)
+                if (p[j] > amax) amax = p[j];
+            for (int j = 16 * b; j < 16 * b + 16; ++j) {
+                pt[j] = fp4_block_value(p[j], amax);
+                l += pt[j];
+            }
+        }
+        for (int j = 0; j < kp; ++j)
+            if (pt[j] != 0.0)
+                for (int c = 0; c < d; ++c) o[c] += pt[j] * vt[(size_t)j * d + c];
+        if (l > 0.0) {
+            for (int c = 0; c < d; ++c) o[c] /= l;
+            lse[h] = m + log(l);
+        } else {
+            lse[h] = -INFINITY;
+        }
+    }
+    free(rows);
+    free(vt);
+    free(s);
+    free(p);
+    free(pt);
+}
