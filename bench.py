@@ -506,7 +506,7 @@ def run_e2e(st, steps, dev, world=1, graph=False):
 
 def run_prefill(args, dev, peaks):
     import torch
-    from fp4_kv_top_csa2_b300 import synth
+    from fp4_kv_top_csa2_b300 import csa2, synth
     from fp4_kv_top_csa2_b300.step import Step
     w = synth.WORKLOADS[PREFILL]
     inp = synth.make_inputs(w)
@@ -516,9 +516,9 @@ def run_prefill(args, dev, peaks):
     for _ in range(max(1, args.warmup // 2)):
         st.run()
     torch.cuda.synchronize()
-    ti, ta, tq = [], [], []
+    ti, ta, tq, tf = [], [], [], []
     for _ in range(args.prefill_steps):
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         e[0].record(stream)
         st.quantize_new_rows()
         e[1].record(stream)
@@ -526,7 +526,11 @@ def run_prefill(args, dev, peaks):
         e[2].record(stream)
         st.attend(L, L["idx"])
         e[3].record(stream)
+        csa2.csa2_sparse_attn_prefill_fp4pv(L["q_attn"], st.q_seq, st.codes, st.sf, st.cu_ctx,
+                                            L["idx"], st.scale, L["out"], L["lse"])
+        e[4].record(stream)
         torch.cuda.synchronize()
+        tf.append(e[3].elapsed_time(e[4]))
         tq.append(e[0].elapsed_time(e[1]))
         ti.append(e[1].elapsed_time(e[2]))
         ta.append(e[2].elapsed_time(e[3]))
@@ -534,7 +538,7 @@ def run_prefill(args, dev, peaks):
     pairs = sum(P0 + i + 1 for i in range(w.T))
     f_idx = 2.0 * pairs * w.Hi * w.Di
     f_attn = 4.0 * w.T * w.topk * w.H * 512
-    mi, ma, mq = (statistics.median(x) for x in (ti, ta, tq))
+    mi, ma, mq, mf = (statistics.median(x) for x in (ti, ta, tq, tf))
     bf16 = peaks["bf16_tflops"]
     p_fp8 = 2.0 * bf16  # nominal dense fp8 / bf16 ratio 4.5 / 2.25
     p_fp4 = 6.0 * bf16  # nominal dense fp4 / bf16 ratio 13.5 / 2.25
@@ -549,6 +553,11 @@ def run_prefill(args, dev, peaks):
             "indexer_tflops": round(ti_fl, 2), "attention_tflops": round(ta_fl, 2),
             "tokens_per_s": round(w.T / ((mi + ma + mq) / 1e3), 1),
             "flops_indexer": f_idx, "flops_attention": f_attn,
+            "attention_fp4pv": {"ms": round(mf, 4),
+                                "tflops": round(f_attn / (mf / 1e3) / 1e12, 2),
+                                "what": "csa2_sparse_attn_prefill_fp4pv: P and V re-quantised to "
+                                        "block-scaled FP4 along the slots (two passes: S^T, then "
+                                        "S^T and PV)"},
             "roofline": {
                 "kernel": "csa2_sparse_attn_prefill (FP4 query quantisation + attn_prefill_kernel)",
                 "bound": "tensor", "achieved": round(ta_fl, 1), "peak": bf16, "unit": "TFLOP/s",

@@ -49,6 +49,7 @@ def _load() -> ctypes.CDLL:
         "csa2_sparse_attn_prefill_workspace_size": (SZ, [I, I, I]),
         "csa2_sparse_attn_prefill": (I, [P, I, I, P, P, P, P, I, P, I, F, P, P, P, SZ, P]),
         "csa2_index_keys_from_kv": (I, [P, P, I64, P, P, I, P, P, P]),
+        "csa2_sparse_attn_prefill_fp4pv": (I, [P, I, I, P, P, P, P, I, P, I, F, P, P, P]),
         "csa2_swa_kv_quant_fp8": (I, [P, I64, I, P, P, P]),
         "csa2_sparse_swa_attn_decode_workspace_size": (SZ, [I, I, I, I]),
         "csa2_sparse_swa_attn_decode": (I, [P, I, I, P, P, P, P, I, P, I, I, F, P, P, P, SZ, P]),
@@ -209,6 +210,17 @@ def csa2_sparse_attn_prefill(q_bf16, q_seq, codes, sf, cu_ctx, idx, softmax_scal
     _check("csa2_sparse_attn_prefill", lib.csa2_sparse_attn_prefill(
         _ptr(q_bf16), T, H, _ptr(q_seq), _ptr(codes), _ptr(sf), _ptr(cu_ctx), B, _ptr(idx), topk,
         float(softmax_scale), _ptr(out_bf16), _ptr(lse), wp, wn, _stream(stream)))
+
+
+def csa2_sparse_attn_prefill_fp4pv(q_bf16, q_seq, codes, sf, cu_ctx, idx, softmax_scale,
+                                   out_bf16, lse=None, stream=None):
+    """Prefill attention with the probability-value product in block-scaled FP4 too."""
+    T, H, _ = q_bf16.shape
+    topk = idx.shape[1]
+    B = cu_ctx.numel() - 1
+    _check("csa2_sparse_attn_prefill_fp4pv", lib.csa2_sparse_attn_prefill_fp4pv(
+        _ptr(q_bf16), T, H, _ptr(q_seq), _ptr(codes), _ptr(sf), _ptr(cu_ctx), B, _ptr(idx), topk,
+        float(softmax_scale), _ptr(out_bf16), _ptr(lse), _stream(stream)))
 
 
 def csa2_index_keys_from_kv(codes, sf, w_bf16, k_idx, k_scale, rows=None, n_rows=None,

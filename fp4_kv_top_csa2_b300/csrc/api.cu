@@ -423,6 +423,25 @@ int csa2_sparse_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_
   return cuda_status(e);
 }
 
+// ---- the full-FP4 PV variant of prefill attention -----------------------------------------
+
+int csa2_sparse_attn_prefill_fp4pv(const void *q_bf16, int T, int H, const int32_t *q_seq,
+                                   const uint8_t *codes, const uint8_t *sf, const int64_t *cu_ctx,
+                                   int B, const int32_t *idx, int topk, float softmax_scale,
+                                   void *out_bf16, float *lse, void *stream) {
+  if (int r = attn_args_ok(T, H, codes, sf, cu_ctx, idx, topk, softmax_scale, q_bf16, out_bf16,
+                           lse, nullptr))
+    return r;
+  if (B < 1) return CSA2_ERR_INVALID_ARG;
+  if (T == 0) return CSA2_OK;
+  if (!q_seq || !aligned16(q_seq)) return CSA2_ERR_INVALID_ARG;
+  if (!attn_prefill_supported(H)) return CSA2_ERR_UNSUPPORTED;
+  if (int r = check_device()) return r;
+  return cuda_status(launch_attn_fp4pv(q_bf16, T, H, q_seq, codes, sf, cu_ctx, idx, topk,
+                                       softmax_scale, out_bf16, lse,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 // ---- index keys derived from main-KV rows -------------------------------------------------
 
 int csa2_index_keys_from_kv(const uint8_t *codes, const uint8_t *sf, int64_t n_rows,

@@ -214,6 +214,12 @@ cudaError_t launch_attn_prefill(const void *q_bf16, int T, int H, const int32_t 
                                 float *lse, cudaStream_t st, const int32_t *q_vis = nullptr,
                                 const uint8_t *swa_kv = nullptr, int ring = 1, int n_win = 0);
 
+// The full-FP4 PV variant of prefill attention (attn_fp4pv.cu): H <= 64, no workspace.
+cudaError_t launch_attn_fp4pv(const void *q_bf16, int T, int H, const int32_t *q_seq,
+                              const uint8_t *codes, const uint8_t *sf, const int64_t *cu_ctx,
+                              const int32_t *idx, int topk, float scale, void *out_bf16,
+                              float *lse, cudaStream_t st);
+
 // Tensor-core decode attention (attn_mma.cu): H <= 64, one CTA per 32 selected rows and 32
 // heads; with n_win > 0 (swa_kv, ring) the window's local rows join the same softmax.
 bool attn_mma_supported(int H, int topk, int n_win = 0);

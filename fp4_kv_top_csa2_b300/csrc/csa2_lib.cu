@@ -8,6 +8,7 @@
 #include "attn_simt.cu"
 #include "attn_mma.cu"
 #include "attn_prefill.cu"
+#include "attn_fp4pv.cu"
 #include "index_keys.cu"
 #include "api.cu"
 #include "noalloc.cu"

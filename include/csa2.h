@@ -270,6 +270,27 @@ int csa2_sparse_attn_prefill(const void *q_bf16, int T, int H, const int32_t *q_
                              void *out_bf16, float *lse, void *workspace, size_t ws_bytes,
                              void *stream);
 
+/*
+ * csa2_sparse_attn_prefill_fp4pv -- the full-FP4 variant of csa2_sparse_attn_prefill: the
+ * workload asks for both prefill products, QK^T and PV, as block-scaled FP4 contractions.  The
+ * probability-value product then needs P and V in FP4 with their scales along the contraction
+ * axis (the slots), which the cache's per-channel scales are not.  Definition (per token and
+ * head; slots j of idx[t] in blocks of 16 consecutive slots, empty slots are zero rows):
+ *     s_j  = softmax_scale * <qhat_h, khat_j>      (qhat: the FP4-quantised query, as prefill)
+ *     p_j  = exp(s_j - max_j s_j)
+ *     Pt_j = FP4(p_j) in its block:   sc = E4M3(max p / 6),  Pt = E2M1(p / sc) * sc
+ *     Vt_j = FP4(khat_j) per channel in its block, the same rule
+ *     out  = sum_j Pt_j Vt_j / sum_j Pt_j,   lse = max_j s_j + log(sum_j Pt_j)
+ * (fp32 divisions, round to nearest even, saturating; no valid slot: out 0, lse -inf).  Arguments
+ * as csa2_sparse_attn_prefill without a workspace; H <= 64.  The numerators come from the
+ * special-function unit's 2^x, so a numerator code can differ from an exactly computed one where
+ * p / sc lies within a few ulps of an E2M1 rounding boundary.
+ */
+int csa2_sparse_attn_prefill_fp4pv(const void *q_bf16, int T, int H, const int32_t *q_seq,
+                                   const uint8_t *codes, const uint8_t *sf, const int64_t *cu_ctx,
+                                   int B, const int32_t *idx, int topk, float softmax_scale,
+                                   void *out_bf16, float *lse, void *stream);
+
 /* ------------------------------------------------------------------------------------------ */
 /* 5b. Index keys derived from main-KV rows                                                     */
 /* ------------------------------------------------------------------------------------------ */
