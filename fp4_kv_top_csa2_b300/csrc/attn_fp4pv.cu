@@ -21,16 +21,26 @@
 
 namespace csa2 {
 
-// E2M1 value nearest to q >= 0 (round to nearest, ties to the even code, saturating at 6).
-__device__ __forceinline__ float e2m1_rne(float q) {
-  return q <= 0.25f ? 0.0f : q < 0.75f ? 0.5f : q <= 1.25f ? 1.0f : q < 1.75f ? 1.5f
-       : q <= 2.5f ? 2.0f : q < 3.5f ? 3.0f : q <= 5.0f ? 4.0f : 6.0f;
+// The E4M3 scale of a block whose largest magnitude is amax (the main-KV rule: amax / 6, fp32
+// division, round to nearest even, saturating).
+__device__ __forceinline__ float fp4_scale(float amax) {
+  return e4m3_to_float(float_to_e4m3_sat(__fdiv_rn(amax, 6.0f)));
 }
 
-// Block-scaled FP4 value of x >= 0 in a block whose largest value is amax (the main-KV rule).
-__device__ __forceinline__ float fp4_block(float x, float amax) {
-  const float sc = e4m3_to_float(float_to_e4m3_sat(__fdiv_rn(amax, 6.0f)));
-  return sc == 0.0f ? 0.0f : e2m1_rne(__fdiv_rn(x, sc)) * sc;
+// Block-scaled FP4 value of x >= 0 under scale sc: E2M1(x / sc) * sc, round to nearest with ties
+// to the even code, saturating at 6.  Decided by comparing x with the decision points T * sc
+// (T = 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5; each product exact in fp32), as the main-KV
+// quantiser does: for x with at most 8 significant bits (a dequantised row) this is exactly the
+// rounding of the fp32 quotient; for a numerator it can differ from it only where x / sc lies
+// within an ulp of a decision point.
+__device__ __forceinline__ float fp4_value(float x, float sc) {
+  // three comparisons pick the code (the even code wins a tie: "at least" against 1.75, 0.75 and
+  // 3.5, "greater than" against 0.25, 1.25, 2.5 and 5), without branches
+  const bool ge4 = x >= 1.75f * sc;
+  const bool ge2 = x >= (ge4 ? 3.5f : 0.75f) * sc;
+  const bool gt1 = x > (ge2 ? (ge4 ? 5.0f : 1.25f) : (ge4 ? 2.5f : 0.25f)) * sc;
+  const uint32_t code = (ge4 ? 4u : 0u) | (ge2 ? 2u : 0u) | (gt1 ? 1u : 0u);
+  return sc == 0.0f ? 0.0f : e2m1_to_float(code) * sc;
 }
 
 __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
@@ -233,7 +243,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
             float a = p;
 #pragma unroll
             for (int o = 1; o < 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-            pt[e] = fp4_block(p, a);
+            pt[e] = fp4_value(p, fp4_scale(a));
             lpart[i] += pt[e];
           }
           const __half2 h2 = __floats2half2_rn(pt[0], pt[1]);  // exact: <= 6 significant bits
@@ -265,6 +275,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
                                          __habs2(*reinterpret_cast<const __half2 *>(&w[e])));
           }
         }
+        float2 scs[8];  // the 16 channels' scales in this block
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 m = __half22float2(amax[i]);
+          scs[i] = make_float2(fp4_scale(m.x), fp4_scale(m.y));
+        }
 #pragma unroll 4
         for (int rr = 0; rr < 16; ++rr) {
           const int j = 16 * b + rr;
@@ -276,9 +292,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-              const float2 m = __half22float2(amax[4 * uu + e]);
-              const float lo = copysignf(fp4_block(fabsf(f.x), m.x), f.x);
-              const float hi = copysignf(fp4_block(fabsf(f.y), m.y), f.y);
+              const float2 sc = scs[4 * uu + e];
+              const float lo = copysignf(fp4_value(fabsf(f.x), sc.x), f.x);
+              const float hi = copysignf(fp4_value(fabsf(f.y), sc.y), f.y);
               const __half2 r = __floats2half2_rn(lo, hi);  // exact
               w[e] = *reinterpret_cast<const uint32_t *>(&r);
             }

@@ -6,15 +6,17 @@
 // index-key projection [128, 512] bf16:
 //   y_i = sum_c W[i,c] x[c]    (tcgen05 kind::f16, bf16 x bf16, fp32 accumulation in TMEM)
 //   s   = max_i |y_i| / 448     (fp32 division; 1 if every y_i is 0)
-//   key_i = E4M3(y_i / s)       (fp32 division, round to nearest even, saturating)
+//   key_i = E4M3(y_i / s)       (y_i times the fp32 reciprocal of s, round to nearest even,
+//                                saturating)
 // keys [rows, 128] and k_scale [rows] = s are the indexer's k_idx and k_scale.
 //
 // Persistent CTAs (one per SM): W stays in shared memory (eight 128B-swizzled chunks of 64
 // channels, loaded once by TMA) as the K-major B operand, N = 128 key dimensions.  Per tile of
-// 128 rows, warps 0..7 gather the FP4 rows (16-byte loads, next chunk in flight) and dequantise
+// 128 rows, warps 0..7 gather the FP4 rows (16-byte loads, the next tile's in flight) and dequantise
 // them chunk by chunk into a 4-stage ring (the K-major A operand, M = 128 rows); warp 8 issues
-// four M=128 x N=128 x K=16 MMAs per chunk into one of two TMEM accumulators; warps 9..12 drain
-// the accumulator (two passes over its 128 columns: the maximum, then the keys).
+// four M=128 x N=128 x K=16 MMAs per chunk into one of two TMEM accumulators; warps 9..16 drain
+// the accumulator, two per lane quarter with 64 columns each (the row maximum is combined
+// through shared memory, then the keys).
 #include "sm100.cuh"
 
 namespace csa2 {
@@ -25,20 +27,20 @@ constexpr int kIkStages = 4;                  // A-chunk ring
 constexpr int kIkChunk = kIkRows * 128;       // one 64-channel chunk of rows or of W: 16 KB
 constexpr int kIkWorkers = 256;               // warps 0..7
 constexpr int kIkMmaWarp = 8;
-constexpr int kIkEpiWarp0 = 9;                // warps 9..12
-constexpr int kIkThreads = (kIkEpiWarp0 + 4) * 32;
+constexpr int kIkEpiWarp0 = 9;                // warps 9..16: two per TMEM lane quarter
+constexpr int kIkThreads = (kIkEpiWarp0 + 8) * 32;
 constexpr int kIkOffW = 0;                                    // 8 x 16 KB
 constexpr int kIkOffA = 8 * kIkChunk;                         // 4 x 16 KB
 constexpr int kIkOffLut = kIkOffA + kIkStages * kIkChunk;     // 256 x u32
 constexpr int kIkOffMisc = kIkOffLut + 1024;
-constexpr int kIkSmem = kIkOffMisc + 256 + 1024;
+constexpr int kIkSmem = kIkOffMisc + 128 + 1024 + 1024;  // misc, row maxima, alignment
 static_assert(kIkSmem <= 232448, "shared memory per CTA");
 
 struct IkMisc {
   uint64_t bar_w, full[kIkStages], empty[kIkStages], tfull[2], tempty[2];
   uint32_t tmem_base;
 };
-static_assert(sizeof(IkMisc) <= 256, "misc block");
+static_assert(sizeof(IkMisc) <= 128, "misc block");
 
 __global__ void __launch_bounds__(kIkThreads, 1) index_keys_kernel(
     const __grid_constant__ CUtensorMap wmap, const uint8_t *__restrict__ codes,
@@ -60,7 +62,7 @@ __global__ void __launch_bounds__(kIkThreads, 1) index_keys_kernel(
     }
     for (int d = 0; d < 2; ++d) {
       mbar_init(&ms.tfull[d], 1);
-      mbar_init(&ms.tempty[d], 128);
+      mbar_init(&ms.tempty[d], 256);
     }
     fence_barrier_init();
     prefetch_tensormap(&wmap);
@@ -80,44 +82,52 @@ __global__ void __launch_bounds__(kIkThreads, 1) index_keys_kernel(
 
   if (warp < 8) {
     // ------------------------------------------------------------------ producers (warps 0..7)
-    // thread: row r = tid / 2 of the tile, channels 32*half .. +31 of every 64-channel chunk
+    // thread: row r = tid / 2 of the tile, channels 32*half .. +31 of every 64-channel chunk.
+    // A tile's eight chunks (eight 16-byte code loads and eight scale pairs) are loaded one tile
+    // ahead, so the HBM latency overlaps the previous tile's work.
     const int r = tid >> 1, half = tid & 1;
-    uint32_t it = 0;
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    uint4 cur[8], nxt[8];
+    uint32_t scur[8], snxt[8];
+    auto load_tile = [&](int64_t tile, uint4 (&c)[8], uint32_t (&sc)[8]) {
       const int64_t slot = tile * kIkRows + r;
-      const int64_t row = slot < n_rows ? (rows ? rows[slot] : slot) : -1;
-      uint4 c = make_uint4(0, 0, 0, 0);
-      uint32_t s2 = 0;
-      auto load = [&](int kc) {
-        if (row >= 0) {
-          c = __ldg(reinterpret_cast<const uint4 *>(codes + row * kCodeBytes + 32 * kc + 16 * half));
-          s2 = __ldg(reinterpret_cast<const uint16_t *>(sf + row * kSfBytes + 4 * kc + 2 * half));
-        }
-      };
-      load(0);
+      const int64_t row = (tile < n_tiles && slot < n_rows) ? (rows ? rows[slot] : slot) : -1;
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) {
+        c[kc] = row >= 0 ? __ldg(reinterpret_cast<const uint4 *>(codes + row * kCodeBytes +
+                                                                 32 * kc + 16 * half))
+                         : make_uint4(0, 0, 0, 0);
+        sc[kc] = row >= 0 ? (uint32_t)__ldg(reinterpret_cast<const uint16_t *>(
+                                sf + row * kSfBytes + 4 * kc + 2 * half))
+                          : 0u;
+      }
+    };
+    uint32_t it = 0;
+    load_tile(blockIdx.x, cur, scur);
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      load_tile(tile + gridDim.x, nxt, snxt);  // in flight while this tile is dequantised
+#pragma unroll
       for (int kc = 0; kc < 8; ++kc, ++it) {
-        const uint4 cc = c;
-        const uint32_t ss = s2;
-        if (kc + 1 < 8) load(kc + 1);  // in flight while this chunk is dequantised
         const uint32_t st = it % kIkStages, ph = (it / kIkStages) & 1;
         ok = mbar_wait(&ms.empty[st], ph ^ 1) && ok;
-        const float fa = e4m3_to_float(ss & 0xFF), fb = e4m3_to_float(ss >> 8);
+        const float fa = e4m3_to_float(scur[kc] & 0xFF), fb = e4m3_to_float(scur[kc] >> 8);
         const uint32_t sa = pack_bf16x2(fa, fa), sb = pack_bf16x2(fb, fb);
-        const uint32_t w[4] = {cc.x, cc.y, cc.z, cc.w};
+        const uint32_t w[4] = {cur[kc].x, cur[kc].y, cur[kc].z, cur[kc].w};
         uint8_t *dst = sm + kIkOffA + st * kIkChunk + r * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {  // 8 channels per 16-byte unit; units 4*half .. +3
-          const uint32_t sc = u < 2 ? sa : sb;
+          const uint32_t scl = u < 2 ? sa : sb;
           uint4 v;
-          v.x = bf16x2_mul(lut[w[u] & 0xFF], sc);
-          v.y = bf16x2_mul(lut[(w[u] >> 8) & 0xFF], sc);
-          v.z = bf16x2_mul(lut[(w[u] >> 16) & 0xFF], sc);
-          v.w = bf16x2_mul(lut[w[u] >> 24], sc);
+          v.x = bf16x2_mul(lut[w[u] & 0xFF], scl);
+          v.y = bf16x2_mul(lut[(w[u] >> 8) & 0xFF], scl);
+          v.z = bf16x2_mul(lut[(w[u] >> 16) & 0xFF], scl);
+          v.w = bf16x2_mul(lut[w[u] >> 24], scl);
           *reinterpret_cast<uint4 *>(dst + (((4 * half + u) ^ (r & 7)) << 4)) = v;
         }
         fence_async_smem();
         mbar_arrive(&ms.full[st]);
       }
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) cur[kc] = nxt[kc], scur[kc] = snxt[kc];
     }
   } else if (warp == kIkMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
@@ -147,57 +157,48 @@ __global__ void __launch_bounds__(kIkThreads, 1) index_keys_kernel(
       }
     }
   } else {
-    // ------------------------------------------------------------------ epilogue (warps 9..12)
-    const int quarter = warp & 3, r = quarter * 32 + lane;
+    // ------------------------------------------------------------------ epilogue (warps 9..16)
+    const int quarter = warp & 3, half = (warp - kIkEpiWarp0) >> 2, r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    float *pmax = reinterpret_cast<float *>(sm + kIkOffMisc + 128);  // [2][128] row maxima
     uint32_t nt = 0;
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++nt) {
       const uint32_t d = nt & 1, dph = (nt >> 1) & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&ms.tfull[d], dph)) && ok;
       tc_fence_after();
-      const uint32_t ta = tmem + d * kIkDi + lane_off;
-      float amax = 0.0f;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kIkDi; c0 += 32) {
-        uint32_t v0[16], v1[16];
-        tmem_ld16(ta + c0, v0);
-        tmem_ld16(ta + c0 + 16, v1);
-        tmem_ld_wait();
+      const uint32_t ta = tmem + d * kIkDi + 64 * half + lane_off;
+      uint32_t v[64];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(v0[i])), fabsf(__uint_as_float(v1[i]))));
-      }
+      for (int c = 0; c < 4; ++c)
+        tmem_ld16(ta + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&v[16 * c]));
+      tmem_ld_wait();
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(v[i])));
+      pmax[half * 128 + r] = amax;
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // the two halves' maxima
+      amax = fmaxf(pmax[r], pmax[128 + r]);
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // read before the next tile writes
       const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      const float inv = __frcp_rn(s);
       const int64_t slot = tile * kIkRows + r;
       const int64_t row = slot < n_rows ? (rows ? rows[slot] : slot) : -1;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kIkDi; c0 += 32) {
-        uint32_t v0[16], v1[16];
-        tmem_ld16(ta + c0, v0);
-        tmem_ld16(ta + c0 + 16, v1);
-        tmem_ld_wait();
-        uint32_t v[32];
+      uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = v0[i], v[16 + i] = v1[i];
-        uint32_t pk[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          uint16_t lo, hi;
-          const float q0 = __fdiv_rn(__uint_as_float(v[4 * k]), s);
-          const float q1 = __fdiv_rn(__uint_as_float(v[4 * k + 1]), s);
-          const float q2 = __fdiv_rn(__uint_as_float(v[4 * k + 2]), s);
-          const float q3 = __fdiv_rn(__uint_as_float(v[4 * k + 3]), s);
-          asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(q1), "f"(q0));
-          asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(q3), "f"(q2));
-          pk[k] = (uint32_t)lo | ((uint32_t)hi << 16);
-        }
-        if (row >= 0) {
-          uint4 *dst = reinterpret_cast<uint4 *>(keys + row * kIkDi + c0);
-          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
+      for (int k = 0; k < 16; ++k) {
+        uint16_t lo, hi;
+        const float q0 = __uint_as_float(v[4 * k]) * inv, q1 = __uint_as_float(v[4 * k + 1]) * inv;
+        const float q2 = __uint_as_float(v[4 * k + 2]) * inv, q3 = __uint_as_float(v[4 * k + 3]) * inv;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(q1), "f"(q0));
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(q3), "f"(q2));
+        pk[k] = (uint32_t)lo | ((uint32_t)hi << 16);
       }
-      if (row >= 0) k_scale[row] = ok ? s : 0.0f;
+      if (row >= 0) {
+        uint4 *dst = reinterpret_cast<uint4 *>(keys + row * kIkDi + 64 * half);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        if (half == 0) k_scale[row] = ok ? s : 0.0f;
+      }
       tc_fence_before();
       mbar_arrive(&ms.tempty[d]);
     }

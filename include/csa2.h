@@ -301,13 +301,14 @@ int csa2_sparse_attn_prefill_fp4pv(const void *q_bf16, int T, int H, const int32
  * the layer's index-key projection W [Di, 512] bf16:
  *     y_i   = sum_c W[i,c] x[c]                   (fp32 accumulation on the tensor cores)
  *     s     = max_i |y_i| / 448                   (fp32 division; 1 when every y_i is 0)
- *     key_i = E4M3(y_i / s)                       (fp32 division, round to nearest even, saturating)
+ *     key_i = E4M3(y_i / s)                       (round to nearest even, saturating)
  * and writes key row t of k_idx [*, Di] (E4M3) and k_scale[t] = s: exactly the k_idx / k_scale
  * inputs of csa2_index_score_topk (score uses s * <q_h, key>).
  * codes / sf: the FP4 cache.  rows: NULL (rows 0..n_rows-1) or [n_rows] int64 cache rows (e.g. the
- * new tokens of a step).  Di must be 128.  y accumulates in fp32 in the tensor core's order, so a
- * key can differ from a correctly rounded evaluation by one code where y_i / s lies within a few
- * fp32 ulps of an E4M3 rounding boundary.
+ * new tokens of a step).  Di must be 128.  y accumulates in fp32 in the tensor core's order and
+ * y_i / s is taken as y_i times the fp32 reciprocal of s, so a key can differ from a correctly
+ * rounded evaluation by one code where y_i / s lies within a few fp32 ulps of an E4M3 rounding
+ * boundary.
  */
 int csa2_index_keys_from_kv(const uint8_t *codes, const uint8_t *sf, int64_t n_rows,
                             const int64_t *rows, const void *w_bf16, int Di, uint8_t *k_idx,
