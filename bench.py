@@ -36,7 +36,7 @@ DECODE_CONFIGS = ("decode_b1_l4096_bf16idx", "decode_b8_l65536", "decode_ragged_
 # DRAM bytes (read + write) of one launch of the Full scan as csa2_index_block_max runs it, from
 # one ncu capture (profiles/index_mma_scan_hier_decode_l1m.md); None when the kernel has changed
 # since.
-SCAN_TRAFFIC = None
+SCAN_TRAFFIC = 137_131_008
 ROOT = os.path.dirname(os.path.abspath(__file__))
 
 
@@ -700,10 +700,12 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
-def profile_step(name, steps, prefill_tokens=0):
+def profile_step(name, steps, prefill_tokens=0, block_max_only=False):
     """A short run for profiler captures: build one workload's step (optionally a prefill with
     fewer new tokens), run it `steps` times, print one JSON line.  The bf16 source rows are dropped
-    once the cache is quantised, so the device holds only what the step reads."""
+    once the cache is quantised, so the device holds only what the step reads.  block_max_only:
+    run the Full layer's scan alone (csa2_index_block_max, the kernel the headline roofline
+    times) instead of the step."""
     import torch
     from fp4_kv_top_csa2_b300 import synth
     from fp4_kv_top_csa2_b300.step import Step
@@ -712,8 +714,12 @@ def profile_step(name, steps, prefill_tokens=0):
         w = synth.scaled(w, T=prefill_tokens)
     st = Step(synth.make_inputs(w), device="cuda")
     st.drop_source_rows()
+    full = next(L for L in st.layers if L["mode"] == "full")
     for _ in range(steps):
-        st.run()
+        if block_max_only:
+            st.block_max(full, st.bm)
+        else:
+            st.run()
     torch.cuda.synchronize()
     return {"profile_step": name, "steps": steps, "T": w.T,
             "device_bytes": torch.cuda.memory_allocated()}
@@ -735,11 +741,13 @@ def main():
                     help="run only this workload's step (--steps times) for a profiler capture")
     ap.add_argument("--prefill-tokens", type=int, default=0,
                     help="with --profile-step on the prefill workload: new tokens per step")
+    ap.add_argument("--block-max-only", action="store_true",
+                    help="with --profile-step: run the Full layer's scan alone")
     args = ap.parse_args()
     if args.profile_step:
         sys.path.insert(0, ROOT)
-        print(json.dumps(profile_step(args.profile_step, args.steps, args.prefill_tokens)),
-              flush=True)
+        print(json.dumps(profile_step(args.profile_step, args.steps, args.prefill_tokens,
+                                      args.block_max_only)), flush=True)
         return
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         # N replicas, one process per GPU, launched the way the multi-GPU contract runs them
