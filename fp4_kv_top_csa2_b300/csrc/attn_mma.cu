@@ -462,6 +462,8 @@ bool attn_mma_supported(int H, int topk, int n_win) {
 }
 
 size_t attn_mma_workspace_bytes(int nq, int H, int topk, int n_win) {
+  if (attn_small_preferred(nq, H, topk, n_win))
+    return attn_small_workspace_bytes(nq, H, topk, n_win);
   const size_t tiles =
       (size_t)(topk + kAttRows - 1) / kAttRows + (size_t)(n_win + kAttRows - 1) / kAttRows;
   const size_t rows = (size_t)nq * tiles * H;
@@ -486,6 +488,9 @@ cudaError_t launch_attn_mma(const void *q_bf16, int nq, int H, const uint8_t *co
                             int topk, float scale, void *out_bf16, float *lse, void *workspace,
                             cudaStream_t st, const uint8_t *swa_kv, int ring, int n_win) {
   if (nq == 0) return cudaSuccess;
+  if (attn_small_preferred(nq, H, topk, n_win))
+    return launch_attn_small(q_bf16, nq, H, codes, sf, cu_ctx, idx, topk, scale, out_bf16, lse,
+                             workspace, st, swa_kv, ring, n_win);
   const int n_sel = (topk + kAttRows - 1) / kAttRows;
   const int n_tiles = n_sel + (n_win + kAttRows - 1) / kAttRows;
   const size_t rows = (size_t)nq * n_tiles * H;
@@ -494,21 +499,15 @@ cudaError_t launch_attn_mma(const void *q_bf16, int nq, int H, const uint8_t *co
   float *l_part = m_part + rows;
   const float scale_log2e = scale * 1.4426950408889634f;
   cudaError_t e;
-  if (attn_cluster_preferred(nq, n_tiles)) {
-    e = launch_attn_cluster_tiles(q_bf16, nq, H, codes, sf, cu_ctx, idx, topk, scale_log2e,
-                                  n_tiles, n_sel, o_part, m_part, l_part, swa_kv, ring, n_win,
-                                  st);
-  } else {
-    CUtensorMap qm;
-    memset(&qm, 0, sizeof(qm));
-    if (!make_q_map(&qm, q_bf16, (int64_t)nq * H)) return cudaErrorInvalidValue;
-    e = set_smem_once(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttSmem);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(attn_mma_kernel, dim3(n_tiles, nq), dim3(kAttThreads), (size_t)kAttSmem, st,
-                   qm, H, codes, sf, cu_ctx, idx, topk, scale_log2e, n_tiles, o_part, m_part,
-                   l_part, swa_kv, ring, n_win, n_sel);
-    note_launches(1);
-  }
+  CUtensorMap qm;
+  memset(&qm, 0, sizeof(qm));
+  if (!make_q_map(&qm, q_bf16, (int64_t)nq * H)) return cudaErrorInvalidValue;
+  e = set_smem_once(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttSmem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(attn_mma_kernel, dim3(n_tiles, nq), dim3(kAttThreads), (size_t)kAttSmem, st, qm,
+                 H, codes, sf, cu_ctx, idx, topk, scale_log2e, n_tiles, o_part, m_part, l_part,
+                 swa_kv, ring, n_win, n_sel);
+  note_launches(1);
   if (e != cudaSuccess) return e;
   e = launch_pdl(attn_mma_combine_kernel, dim3(H, nq), dim3(kD / 4), 0, st, H, n_tiles,
                  (const float *)o_part, (const float *)m_part, (const float *)l_part,

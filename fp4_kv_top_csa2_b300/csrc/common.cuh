@@ -222,8 +222,7 @@ cudaError_t launch_attn_fp4pv(const void *q_bf16, int T, int H, const int32_t *q
 
 // Tensor-core decode attention (attn_mma.cu): H <= 64, tiles of 128 selected rows, partial
 // results merged by a combine kernel; with n_win > 0 (swa_kv, ring) the window's local rows join
-// the same softmax.  Few tiles in all: one cluster of 8 CTAs per tile, a 64-channel slice each
-// (attn_cluster.cu); many: one CTA per tile.
+// the same softmax.  Few tiles in all go to the small-tile kernel of attn_small.cu instead.
 bool attn_mma_supported(int H, int topk, int n_win = 0);
 size_t attn_mma_workspace_bytes(int nq, int H, int topk, int n_win = 0);
 cudaError_t launch_attn_mma(const void *q_bf16, int nq, int H, const uint8_t *codes,
@@ -232,15 +231,14 @@ cudaError_t launch_attn_mma(const void *q_bf16, int nq, int H, const uint8_t *co
                             cudaStream_t st, const uint8_t *swa_kv = nullptr, int ring = 1,
                             int n_win = 0);
 
-// The cluster form of the decode attention's tile kernel (attn_cluster.cu): the same partials
-// (o_part [nq][n_tiles][H][512], m_part / l_part [nq][n_tiles][H]) as attn_mma's tile kernel.
-bool attn_cluster_preferred(int nq, int n_tiles);
-cudaError_t launch_attn_cluster_tiles(const void *q_bf16, int nq, int H, const uint8_t *codes,
-                                      const uint8_t *sf, const int64_t *cu_ctx,
-                                      const int32_t *idx, int topk, float scale_log2e,
-                                      int n_tiles, int n_sel_tiles, float *o_part, float *m_part,
-                                      float *l_part, const uint8_t *swa_kv, int ring, int n_win,
-                                      cudaStream_t st);
+// The decode attention for few tiles (attn_small.cu): tiles of 32 rows x 32 heads, chosen by
+// launch_attn_mma when they fit in about one wave; the same arguments and result.
+bool attn_small_preferred(int nq, int H, int topk, int n_win);
+size_t attn_small_workspace_bytes(int nq, int H, int topk, int n_win);
+cudaError_t launch_attn_small(const void *q_bf16, int nq, int H, const uint8_t *codes,
+                              const uint8_t *sf, const int64_t *cu_ctx, const int32_t *idx,
+                              int topk, float scale, void *out_bf16, float *lse, void *workspace,
+                              cudaStream_t st, const uint8_t *swa_kv, int ring, int n_win);
 
 // Index keys derived from main-KV rows (index_keys.cu): keys [*, 128] E4M3 and k_scale of the
 // given cache rows (rows NULL: rows 0..n_rows-1), projection W [128, 512] bf16.

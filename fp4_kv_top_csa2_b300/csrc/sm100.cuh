@@ -131,75 +131,6 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// ---------------------------------------------------------------- thread-block clusters
-// Rank of this CTA in its cluster.
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster: shared-memory writes before it (local or remote)
-// are visible to every thread of the cluster after it.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// The two halves of cluster_sync, for work in between: every arrive is matched by one wait
-// before the next arrive.
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-// An arrive without release ordering: for execution order alone, or after a fence that already
-// releases what the peers need (fence.mbarrier_init.release.cluster for barrier initialisation).
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from this CTA's shared
-// memory to a cluster peer's (dst: shared::cluster address); completion is signalled as
-// transaction bytes on the peer's mbarrier `bar_cluster` (shared::cluster address).
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void *src,
-                                                  uint32_t bytes, uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-      "[%3];" ::"r"(dst_cluster),
-      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
-      : "memory");
-}
-// The shared::cluster address of the same byte offset in CTA `rank`'s shared memory.
-__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float4 dsmem_ld_f4(uint32_t a) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(a)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ float dsmem_ld_f32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ void dsmem_st_f32(uint32_t a, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
-}
-__device__ __forceinline__ void dsmem_st_v2(uint32_t a, uint32_t x, uint32_t y) {
-  asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
-}
-// Order this thread's generic-proxy shared-memory writes (in any CTA of the cluster) before
-// later async-proxy (tensor core) reads of them.
-__device__ __forceinline__ void fence_proxy_async_all() {
-  asm volatile("fence.proxy.async;" ::: "memory");
-}
-
 // Shared-memory matrix descriptor: K-major operand stored as rows of 128 bytes with the 128-byte
 // swizzle (the layout a SWIZZLE_128B TMA box of 128-byte rows produces), 8-row groups 1024
 // bytes apart.  `addr` is the shared address of the first row (1024-byte aligned) plus the byte

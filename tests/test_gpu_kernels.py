@@ -444,14 +444,20 @@ def test_topk_over_many_blocks(csa2, kind):
 @pytest.mark.parametrize("nb,kind,vis_frac", [
     (131072, "normal", 1.0), (131069, "ties", 1.0), (131072, "ties", 0.37), (16384, "normal", 1.0),
     (16385, "ties", 1.0), (5, "normal", 1.0), (40000, "normal", 0.001),
+    (16384, "strided", 1.0), (9001, "strided", 1.0), (16384, "ties", 1.0),
 ])
 def test_pool_selection_cluster_sizes(csa2, nb, kind, vis_frac):
     """Candidate pool straight from given block maxima, at the element counts where one query's
     selection spans 1 to 8 cooperating CTAs (and ragged tails), with heavy ties and signed zeros.
+    "strided": every 64th value is far above the rest, so regularly strided samples overstate
+    the k-th value and a sampled threshold keeps fewer than k (the selection must recover).
     The selection must equal the oracle's on the same fp32 values exactly."""
     g = torch.Generator().manual_seed(nb + int(vis_frac * 100))
     B = 3
-    if kind == "normal":
+    if kind == "strided":
+        bm = torch.randn(B, nb, generator=g)
+        bm[:, ::64] += 100.0
+    elif kind == "normal":
         bm = torch.randn(B, nb, generator=g) * 12 + 40
     else:
         bm = torch.randint(-3, 4, (B, nb), generator=g).float() * 0.5
