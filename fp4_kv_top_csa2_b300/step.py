@@ -51,6 +51,8 @@ class _Arena:
         self.buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
         self.views = {name: self.buf[o:o + nb].view(dtype).view(shape)
                       for name, o, shape, dtype, nb in placed}
+        self.offsets = {name: o for name, o, _, _, _ in placed}  # byte offset of each view
+        self.size = self.buf.numel()
 
 
 class Step:
@@ -114,6 +116,15 @@ class Step:
             d["out"] = self.out_arena.views[f"out{i}"]
             d["lse"] = torch.empty((self.nq, w.H), dtype=torch.float32, device=dev)
             self.layers.append(d)
+        # byte ranges of each layer's inputs (layer 0's also holds the new rows) and output in
+        # the arenas, for copies that overlap the step (run(io=...))
+        n_l = len(self.layers)
+        starts = [0] + [self.in_arena.offsets[f"q_attn{i}"] for i in range(1, n_l)]
+        self.in_ranges = [(starts[i], starts[i + 1] if i + 1 < n_l else self.in_arena.size)
+                          for i in range(n_l)]
+        self.out_ranges = [(self.out_arena.offsets[f"out{i}"],
+                            self.out_arena.offsets[f"out{i}"] + self.layers[i]["out"].numel() * 2)
+                           for i in range(n_l)]
         self.bm = torch.empty((self.nq, nb), dtype=torch.float32, device=dev) if hier else None
         self.pool = (torch.empty((self.nq, w.n_pool_blocks), dtype=torch.int32, device=dev)
                      if hier else None)
@@ -134,6 +145,10 @@ class Step:
         self.qstream = torch.cuda.Stream(device=dev)
         self.ev_start = torch.cuda.Event()
         self.ev_ready = torch.cuda.Event()
+        self.h2d_stream = torch.cuda.Stream(device=dev)
+        self.d2h_stream = torch.cuda.Stream(device=dev)
+        self.ev_in = [torch.cuda.Event() for _ in self.layers]
+        self.ev_out = [torch.cuda.Event() for _ in self.layers]
         self.side = []
         if self.overlap_layers:
             self.side = [torch.cuda.Stream(device=dev) for _ in self.layers[1:]]
@@ -227,10 +242,28 @@ class Step:
         elif L["mode"] == "reindex":
             self.index(L, cand=self.pool, stream=stream)
 
-    def run(self, stream=None):
+    def run(self, stream=None, io=None):
         """One step: quantise the new rows, then every layer (see the module docstring for the
-        order of the calls)."""
+        order of the calls).  io = (host_in, host_out), pinned host buffers laid out like the
+        input and output arenas: the step's inputs are copied in and its outputs out as part of
+        the step, overlapped with the computation.  Layer 0's inputs (with the new rows) cross
+        first on the step's stream; the other layers' inputs follow on a copy stream while
+        layer 0 computes, and layer 1 waits for them.  The outputs of all layers but the last
+        leave on a copy stream while the last layer computes, and the last one on the step's
+        stream, which then waits for both copies."""
         main = stream if stream is not None else torch.cuda.current_stream()
+        n_l = len(self.layers)
+        if io is not None:
+            assert not self.overlap_layers, "the host copies follow the model order"
+            host_in, host_out = io
+            h2d, d2h = self.h2d_stream, self.d2h_stream
+            _, b0 = self.in_ranges[0]
+            self.in_arena.buf[:b0].copy_(host_in[:b0], non_blocking=True)
+            if n_l > 1:
+                h2d.wait_stream(main)  # the previous step has finished with the arena
+                with torch.cuda.stream(h2d):
+                    self.in_arena.buf[b0:].copy_(host_in[b0:], non_blocking=True)
+                self.ev_in[1].record(h2d)
         # the new rows go into the cache beside layer 0's selection (which does not read it)
         self.ev_start.record(main)
         self.qstream.wait_event(self.ev_start)
@@ -238,10 +271,23 @@ class Step:
         self.ev_ready.record(self.qstream)
         if not self.overlap_layers:
             for i, L in enumerate(self.layers):
+                if io is not None and i == 1:
+                    main.wait_event(self.ev_in[1])
                 self._select(i, L, main)
                 if i == 0:
                     main.wait_event(self.ev_ready)
                 self.attend(L, self.layers[self.src[i]]["idx"], stream=main)
+                if io is not None and i == n_l - 2:  # every output but the last one's
+                    self.ev_out[i].record(main)
+                    d2h.wait_event(self.ev_out[i])
+                    e = self.out_ranges[i][1]
+                    with torch.cuda.stream(d2h):
+                        host_out[:e].copy_(self.out_arena.buf[:e], non_blocking=True)
+            if io is not None:
+                a = self.out_ranges[n_l - 2][1] if n_l > 1 else 0
+                host_out[a:].copy_(self.out_arena.buf[a:], non_blocking=True)
+                if n_l > 1:
+                    main.wait_stream(d2h)
             return
         streams = [main] + self.side
         for i, L in enumerate(self.layers):
@@ -263,21 +309,24 @@ class Step:
             main.wait_event(self.ev_done[i])
 
     # ------------------------------------------------------------------------------------------
-    def capture(self):
-        """Record one step (the same C-ABI calls as run()) into a CUDA graph; replay() then
-        re-issues the whole step with one launch.  Inputs and outputs stay in the buffers above,
-        so a caller refreshes inputs in place between replays."""
-        self.run()  # first calls on this device: one-time set-up outside the capture
+    def capture(self, io=None):
+        """Record one step (the same C-ABI calls as run(), with the host copies when io is
+        given) into a CUDA graph; replay() then re-issues the whole step with one launch.
+        Without io, inputs and outputs stay in the buffers above, so a caller refreshes inputs
+        in place between replays; with io, the graph copies from and to those host buffers."""
+        self.run(io=io)  # first calls on this device: one-time set-up outside the capture
         torch.cuda.synchronize()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
-        self.graph = torch.cuda.CUDAGraph()
+        graph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(side):
-            with torch.cuda.graph(self.graph, stream=side, capture_error_mode="thread_local"):
-                self.run(stream=side)
+            with torch.cuda.graph(graph, stream=side, capture_error_mode="thread_local"):
+                self.run(stream=side, io=io)
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
-        return self.graph
+        if io is None:
+            self.graph = graph
+        return graph
 
     def replay(self):
         self.graph.replay()

@@ -163,3 +163,37 @@ def test_overlapped_layers_match_model_order(mods, B, L):
             M["out"].zero_()
         con.replay()
         same()
+
+
+@pytest.mark.parametrize("name,B,L", [("hier_decode_l1m", 1, 65536),
+                                      ("hier_decode_l1m_swa128", 2, 30000)])
+def test_step_with_host_copies_matches_device_step(mods, name, B, L):
+    """The step with its inputs copied in and its outputs copied out layer by layer, overlapped
+    with the computation (Step.run(io=...), as bench.py's end-to-end timing runs it), directly
+    and as a replayed graph: the host output buffer holds exactly the device step's outputs,
+    and a changed host input reaches the device (the copies are not skipped)."""
+    step, synth = mods
+    w = synth.scaled(synth.WORKLOADS[name], B=B, L=(L,) * B)
+    st = step.Step(synth.make_inputs(w))
+    st.run()
+    torch.cuda.synchronize()
+    want = st.out_arena.buf.clone().cpu()
+    host_in = st.in_arena.buf.cpu().pin_memory()
+    host_out = torch.zeros(st.out_arena.size, dtype=torch.uint8).pin_memory()
+    st.run(io=(host_in, host_out))
+    torch.cuda.synchronize()
+    assert torch.equal(host_out, want)
+    g = st.capture(io=(host_in, host_out))
+    for _ in range(2):
+        host_out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(host_out, want)
+    # a different last-layer attention query on the host changes only the last layer's output
+    qa = st.in_arena.offsets[f"q_attn{len(st.layers) - 1}"]
+    host_in[qa:qa + 64] = 0
+    g.replay()
+    torch.cuda.synchronize()
+    oa, ob = st.out_ranges[-1]
+    assert torch.equal(host_out[:oa], want[:oa])
+    assert not torch.equal(host_out[oa:ob], want[oa:ob])
