@@ -20,11 +20,12 @@
 //   4. O = [P_hi; P_lo] Vhat: M=128 x N=256 channels x K=16 rows per MMA, the same dequantised
 //      chunks read as the MN-major B operand (channels contiguous), two channel halves into TMEM
 //      columns 0..255 and 256..511 (the second half reuses S's columns once it is read): 16 MMAs
-//      for the whole tile.  TMEM lanes 0..63 hold the hi products, 64..127 the lo products.
-//   5. The lo plane is added to the hi plane in shared memory (Q's and the rows' space, free
-//      once the last MMA is done), and the tile's unnormalised O [H x 512] fp32 goes to workspace
-//      in whole-row coalesced stores, with the per-head (max, sum); a combine kernel merges the
-//      tiles with the softmax weights and normalises.
+//      for the whole tile.  The M rows put each lane quarter's 16 heads' hi rows, then their lo
+//      rows, so a head's two products sit 16 TMEM lanes apart in one warp.
+//   5. One shuffle adds a head's hi and lo products in registers, and the tile's unnormalised
+//      O [H x 512] fp32 goes to workspace (each pair of lanes fills whole 128-byte lines), with
+//      the per-head (max, sum); a combine kernel merges the tiles with the softmax weights and
+//      normalises.
 // With a local window (the sliding-window branch: "DeepSeek V4.1-Flash", aiwiki.ai, section
 // "Compressed Sparse Attention 2", every layer's own local keys and values; section "KV-cache
 // formats and bounded replay", stored in FP8), the tiles after the selected rows' hold the
@@ -296,8 +297,11 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
       m = fmaxf(ms.mx[0][h], ms.mx[1][h]);
       const float mm = m == -INFINITY ? 0.0f : m;  // no valid slot: every numerator 0
       float l = 0.0f;
-      uint8_t *phi = sm + kAttOffP + c2 * kAttPChunk + h * 128;
-      uint8_t *plo = phi + 64 * 128;  // row 64 + h
+      // M rows: lane quarter h / 16 holds heads 16 (h / 16) .. + 15, their hi rows then their lo
+      // rows (row & 7 == h & 7 for both, so the swizzle below keeps h & 7)
+      const int mr_hi = 32 * (h >> 4) + (h & 15);
+      uint8_t *phi = sm + kAttOffP + c2 * kAttPChunk + mr_hi * 128;
+      uint8_t *plo = phi + 16 * 128;  // row mr_hi + 16
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         uint32_t hi[4], lo[4];
@@ -324,47 +328,37 @@ __global__ void __launch_bounds__(kAttThreads, 1) attn_mma_kernel(
     tc_fence_before();
     mbar_arrive(&ms.bar_p);
 
-    // ---- epilogue: O = hi plane (TMEM lanes 0..63) + lo plane (lanes 64..127), added in the
-    // shared memory that Q and the rows held (free once the last MMA has completed), then stored
-    // with whole-row coalesced writes.  stage = [64 heads][128 float4], the float4 index XORed
-    // with (head & 7) so that 32 heads writing one column hit 8 different bank groups.
+    // ---- epilogue: warp = (lane quarter q: heads 16 q .. + 15, hi products in lanes 0..15 and
+    // lo in 16..31; channel half c2).  One shuffle adds a head's hi and lo values: the hi lane
+    // keeps columns 0..15 of each 32-column block, the lo lane 16..31, and each stores its 64
+    // bytes of the head's partial row (two lanes fill one 128-byte line).
     ok = __all_sync(0xffffffffu, mbar_wait(&ms.bar_o, 0)) && ok;
     tc_fence_after();
-    float4 *stage = reinterpret_cast<float4 *>(sm + kAttOffQ);
-    const int hq = (quarter & 1) * 32 + lane;
-    const uint32_t ta = tmem + 256 * c2 + lane_off;
+    {
+      const bool lo = lane >= 16;
+      const int ho = 16 * quarter + (lane & 15);
+      const uint32_t ta = tmem + 256 * c2 + lane_off;
+      float *orow = o_part + (((int64_t)n * n_tiles + tile) * H + ho) * kD + 256 * c2 + 16 * lo;
 #pragma unroll 1
-    for (int phase = 0; phase < 2; ++phase) {
-      if ((quarter >> 1) == 1 - phase) {  // phase 0: the lo plane; phase 1: the hi plane adds
-#pragma unroll 1
-        for (int c0 = 0; c0 < 256; c0 += 32) {
-          uint32_t r0[16], r1[16];
-          tmem_ld16(ta + c0, r0);
-          tmem_ld16(ta + c0 + 16, r1);
-          tmem_ld_wait();
+      for (int c0 = 0; c0 < 256; c0 += 32) {
+        uint32_t v0[16], v1[16];
+        tmem_ld16(ta + c0, v0);
+        tmem_ld16(ta + c0 + 16, v1);
+        tmem_ld_wait();
+        float o[16];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t *r = k < 4 ? r0 + 4 * k : r1 + 4 * (k - 4);
-            float4 v = make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]),
-                                   __uint_as_float(r[2]), __uint_as_float(r[3]));
-            float4 *dst = stage + hq * 128 + (((64 * c2 + c0 / 4 + k)) ^ (hq & 7));
-            if (phase == 1) {
-              const float4 lo = *dst;
-              v.x += lo.x;
-              v.y += lo.y;
-              v.z += lo.z;
-              v.w += lo.w;
-            }
-            *dst = v;
-          }
+        for (int k = 0; k < 16; ++k) {
+          const float send = __uint_as_float(lo ? v0[k] : v1[k]);
+          const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+          o[k] = __uint_as_float(lo ? v1[k] : v0[k]) + recv;
+        }
+        if (ho < H) {
+          float4 *d = reinterpret_cast<float4 *>(orow + c0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            d[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
         }
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-    }
-    float4 *op = reinterpret_cast<float4 *>(o_part + ((int64_t)n * n_tiles + tile) * H * kD);
-    for (int i = tid; i < H * 128; i += kAttWorkers) {
-      const int hh = i >> 7;
-      op[i] = stage[hh * 128 + ((i & 127) ^ (hh & 7))];
     }
   }
   tc_fence_before();
