@@ -55,6 +55,7 @@ def _cache(lengths, seed):
     ([4000], 64, 100, 1, 1),                  # the current token's local row only
     ([2000, 3000], 64, 2048, 200, 256),
     ([700], 64, 33, 0, 16),                   # no window: the plain sparse attention
+    ([4000, 3500, 3000, 2500, 2100], 16, 2048, 100, 128),  # 128-row tiles, 16 heads
 ])
 def test_swa_decode(csa2, lengths, H, topk, n_win, ring):
     x, sigma, g = _cache(lengths, sum(lengths) + n_win)
