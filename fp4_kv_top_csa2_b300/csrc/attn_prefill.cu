@@ -69,10 +69,6 @@ static_assert(offsetof(PfMisc, mref) % 16 == 0 && offsetof(PfMisc, factor) % 16 
               "float4 reads of mref / factor");
 static_assert(sizeof(PfMisc) <= 1024, "misc block");
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  return (uint32_t)__half_as_ushort(__float2half_rn(lo)) |
-         ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
-}
 __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
   __half2 x = *reinterpret_cast<__half2 *>(&a);
   __half2 y = *reinterpret_cast<__half2 *>(&b);
