@@ -284,11 +284,12 @@ def _attn_case(B, H, n_rows, topk, seed, holes=True):
                                               (1, 80, 500, 300),
                                               (1, 64, 20000, 16384),  # largest topk
                                               (3, 16, 5000, 4096),    # 128-row tiles, 16 heads
-                                              (5, 48, 3000, 2048)])   # 128-row tiles, 48 heads
+                                              (5, 48, 3000, 2048),    # 128-row tiles, 48 heads
+                                              (6, 64, 3000, 1000)])   # 128-row tiles, ragged
 def test_decode_attention(csa2, B, H, n_rows, topk):
     """Batches of 1 to 5 sequences, 16 to 64 heads, Top-K 1 to 16,384 with empty slots (and one
     sequence with none).  Calls whose 32-row x 32-head tiles fit one wave take that kernel, the
-    others (the first, the last three H <= 64 cases) the 128-row tiles with all heads per CTA;
+    others (the first, the last four H <= 64 cases) the 128-row tiles with all heads per CTA;
     with 16 or 48 heads the 64 rows of a CTA's query and TMEM lanes are partly padding.  Two
     calls on one workspace must give the same result."""
     x, q, idx, cu = _attn_case(B, H, n_rows, topk, B * 1000 + topk)
