@@ -43,6 +43,10 @@ __device__ __forceinline__ float fp4_value(float x, float sc) {
   return sc == 0.0f ? 0.0f : e2m1_to_float(code) * sc;
 }
 
+// The E2M1 decision points in units of the scale, in increasing order (the packed re-quantisation
+// adds 0.5, 0.5, 0.5, 0.5, 1, 1, 2 as x passes them).
+__device__ constexpr float kFp4Cut[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+
 __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
     const uint16_t *__restrict__ q_bf16, int H, const int32_t *__restrict__ q_seq,
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf,
@@ -228,75 +232,104 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
         }
         continue;
       }
-      // ---- pass 2: numerators, FP4 per (head, 16-slot block) = 16 lanes
+      // ---- pass 2: numerators, FP4 per (head, 16-slot block) = 16 lanes.  Per 16 heads the
+      //      block maxima are reduce-scattered over the half-warp (lane l ends with head l's),
+      //      each lane rounds one scale, and the scales are broadcast back by shuffles.
       const float *mref = &ms.mref[32 * hh];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint32_t hv[4];
+      for (int hb = 0; hb < 2; ++hb) {
+        float p[16], t[16];
 #pragma unroll
-        for (int k = 0; k < 8; k += 2) {
-          float pt[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int i = 8 * u + k + e;
-            const float p = row_ok ? ex2_approx(x[i] - mref[i]) : 0.0f;
-            float a = p;
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-            pt[e] = fp4_value(p, fp4_scale(a));
-            lpart[i] += pt[e];
-          }
-          const __half2 h2 = __floats2half2_rn(pt[0], pt[1]);  // exact: <= 6 significant bits
-          hv[k / 2] = *reinterpret_cast<const uint32_t *>(&h2);
+        for (int i = 0; i < 16; ++i) {
+          p[i] = row_ok ? ex2_approx(x[16 * hb + i] - mref[16 * hb + i]) : 0.0f;
+          t[i] = p[i];
         }
-        const int off = jrow * 128 + (((4 * hh + u) ^ (jrow & 7)) << 4);
-        *reinterpret_cast<uint4 *>(sm + kPfOffPhi + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) {
+          const bool upper = lane & o;
+#pragma unroll
+          for (int i = 0; i < o; ++i) {
+            const float keep = upper ? t[i + o] : t[i], send = upper ? t[i] : t[i + o];
+            t[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+          }
+        }
+        const float sc_mine = fp4_scale(t[0]);
+#pragma unroll
+        for (int uh = 0; uh < 2; ++uh) {
+          uint32_t hv[4];
+#pragma unroll
+          for (int k = 0; k < 8; k += 2) {
+            float pt[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = 8 * uh + k + e;
+              const float sc = __shfl_sync(0xffffffffu, sc_mine, (lane & 16) | i);
+              pt[e] = fp4_value(p[i], sc);
+              lpart[16 * hb + i] += pt[e];
+            }
+            const __half2 h2 = __floats2half2_rn(pt[0], pt[1]);  // exact: <= 6 significant bits
+            hv[k / 2] = *reinterpret_cast<const uint32_t *>(&h2);
+          }
+          const int u = 2 * hb + uh;
+          const int off = jrow * 128 + (((4 * hh + u) ^ (jrow & 7)) << 4);
+          *reinterpret_cast<uint4 *>(sm + kPfOffPhi + off) =
+              make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        }
       }
-      // ---- V re-quantised in place: thread = 16 channels of one 16-row block.  S^T(t) is
-      //      complete (its commit arrived), so Khat is no longer read by it.
+      // ---- V re-quantised in place: thread = 16 channels of one 16-row block, 8 channels at a
+      //      time.  S^T(t) is complete (its commit arrived), so Khat is no longer read by it.
+      //      Every Khat value, scale and decision point T * sc is exact in fp16, so the code is
+      //      decided by packed fp16 comparisons and the level sc * E2M1 built by accumulation.
       {
-        const int b = tid >> 5;                      // 16-row block 0..7
+        const int b = tid >> 5;                         // 16-row block 0..7
         const int kc = lane >> 2, u0 = (lane & 3) * 2;  // chunk and its 16-byte units u0, u0+1
         uint8_t *chunk = sm + kPfOffK + kc * kPfKChunk;
-        __half2 amax[8];
+#pragma unroll 1
+        for (int uu = 0; uu < 2; ++uu) {
+          const int u = u0 + uu;
+          __half2 amax[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax[i] = __float2half2_rn(0.0f);
+          for (int e = 0; e < 4; ++e) amax[e] = __float2half2_rn(0.0f);
 #pragma unroll 4
-        for (int rr = 0; rr < 16; ++rr) {
-          const int j = 16 * b + rr;
-#pragma unroll
-          for (int uu = 0; uu < 2; ++uu) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(chunk + j * 128 +
-                                                             (((u0 + uu) ^ (j & 7)) << 4));
+          for (int rr = 0; rr < 16; ++rr) {
+            const int j = 16 * b + rr;
+            const uint4 v = *reinterpret_cast<const uint4 *>(chunk + j * 128 + ((u ^ (j & 7)) << 4));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              amax[4 * uu + e] = __hmax2(amax[4 * uu + e],
-                                         __habs2(*reinterpret_cast<const __half2 *>(&w[e])));
+              amax[e] = __hmax2(amax[e], __habs2(*reinterpret_cast<const __half2 *>(&w[e])));
           }
-        }
-        float2 scs[8];  // the 16 channels' scales in this block
+          __half2 sc2[4], th[4][7];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float2 m = __half22float2(amax[i]);
-          scs[i] = make_float2(fp4_scale(m.x), fp4_scale(m.y));
-        }
+          for (int e = 0; e < 4; ++e) {
+            const float2 m = __half22float2(amax[e]);
+            sc2[e] = __floats2half2_rn(fp4_scale(m.x), fp4_scale(m.y));  // exact: E4M3 values
+#pragma unroll
+            for (int k = 0; k < 7; ++k) th[e][k] = __hmul2(sc2[e], __float2half2_rn(kFp4Cut[k]));
+          }
+          const __half2 half = __float2half2_rn(0.5f), one = __float2half2_rn(1.0f),
+                        two = __float2half2_rn(2.0f);
 #pragma unroll 4
-        for (int rr = 0; rr < 16; ++rr) {
-          const int j = 16 * b + rr;
-#pragma unroll
-          for (int uu = 0; uu < 2; ++uu) {
-            uint4 *pv = reinterpret_cast<uint4 *>(chunk + j * 128 + (((u0 + uu) ^ (j & 7)) << 4));
+          for (int rr = 0; rr < 16; ++rr) {
+            const int j = 16 * b + rr;
+            uint4 *pv = reinterpret_cast<uint4 *>(chunk + j * 128 + ((u ^ (j & 7)) << 4));
             const uint4 v = *pv;
             uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-              const float2 sc = scs[4 * uu + e];
-              const float lo = copysignf(fp4_value(fabsf(f.x), sc.x), f.x);
-              const float hi = copysignf(fp4_value(fabsf(f.y), sc.y), f.y);
-              const __half2 r = __floats2half2_rn(lo, hi);  // exact
-              w[e] = *reinterpret_cast<const uint32_t *>(&r);
+              const __half2 a = __habs2(*reinterpret_cast<const __half2 *>(&w[e]));
+              // ties to the even code: "greater than" at 0.25, 1.25, 2.5, 5; "at least" at
+              // 0.75, 1.75, 3.5 (as fp4_value)
+              __half2 lv = __hmul2(__hgt2(a, th[e][0]), half);
+              lv = __hfma2(__hge2(a, th[e][1]), half, lv);
+              lv = __hfma2(__hgt2(a, th[e][2]), half, lv);
+              lv = __hfma2(__hge2(a, th[e][3]), half, lv);
+              lv = __hfma2(__hgt2(a, th[e][4]), one, lv);
+              lv = __hfma2(__hge2(a, th[e][5]), one, lv);
+              lv = __hfma2(__hgt2(a, th[e][6]), two, lv);
+              const __half2 q = __hmul2(lv, sc2[e]);  // exact: <= 6 significant bits
+              w[e] = (*reinterpret_cast<const uint32_t *>(&q) & 0x7FFF7FFFu) |
+                     (w[e] & 0x80008000u);
             }
             *pv = make_uint4(w[0], w[1], w[2], w[3]);
           }

@@ -52,3 +52,44 @@ def test_ties_go_to_the_even_code():
     s = np.float32(1.0)
     x = MIDS.astype(np.float32)
     assert _threshold_code(x, s).tolist() == [0, 2, 2, 4, 4, 6, 6]
+
+
+E2M1_LEVELS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _fp16_ladder(a16, s16):
+    """The full-FP4 PV attention's re-quantisation of a dequantised row value |v| (fp16) under a
+    block scale s (fp16): the level grows by 0.5, 0.5, 0.5, 0.5, 1, 1, 2 as |v| passes the
+    decision points T * s (fp16 products), ties to the even code, then is multiplied by s."""
+    th = [np.float16(m) * s16 for m in MIDS]
+    half, one, two = np.float16(0.5), np.float16(1.0), np.float16(2.0)
+    lv = (a16 > th[0]).astype(np.float16) * half
+    lv = lv + (a16 >= th[1]).astype(np.float16) * half
+    lv = lv + (a16 > th[2]).astype(np.float16) * half
+    lv = lv + (a16 >= th[3]).astype(np.float16) * half
+    lv = lv + (a16 > th[4]).astype(np.float16) * one
+    lv = lv + (a16 >= th[5]).astype(np.float16) * one
+    lv = lv + (a16 > th[6]).astype(np.float16) * two
+    return th, lv * s16
+
+
+def test_fp16_requantisation_of_dequantised_rows_is_exact():
+    """Every dequantised cache value (E2M1 magnitude x positive E4M3 scale) and every decision
+    point T * s is exactly representable as a normal fp16 number, so packed fp16 comparisons
+    decide the FP4 code of v / s as rounding the exact quotient does, and the level times s is
+    exact too.  Checked for every such value against every positive E4M3 scale."""
+    e4 = _e4m3_positive()
+    vals = np.unique(np.outer(E2M1_LEVELS, e4).ravel())
+    a16 = vals.astype(np.float16)
+    assert (a16.astype(np.float64) == vals).all()
+    assert (vals[vals > 0] >= 2.0 ** -14).all()  # no fp16 subnormals
+    for s in e4:
+        s16 = np.float16(s)
+        assert float(s16) == s
+        th, q = _fp16_ladder(a16, s16)
+        assert all(float(t) == m * s and float(t) >= 2.0 ** -14 for t, m in zip(th, MIDS))
+        ref = E2M1_LEVELS[_rne_code(vals / s)] * s
+        assert (q.astype(np.float64) == ref).all(), s
+    # a block of zeros has scale 0 and stays zero
+    _, q0 = _fp16_ladder(np.zeros(3, np.float16), np.float16(0.0))
+    assert (q0 == 0).all()
