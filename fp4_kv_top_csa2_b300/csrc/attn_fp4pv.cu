@@ -9,9 +9,11 @@
 //   out_h = sum_j Pt_j Vt_j / sum_j Pt_j,   lse_h = m_h + ln sum_j Pt_j
 // The maximum must be known before any numerator is quantised, so the kernel makes two passes
 // over the token's tiles: the first computes S^T only and keeps each head's maximum; the second
-// recomputes S^T, quantises P (block maxima by half-warp shuffles: a 16-slot block is 16 lanes)
-// and re-quantises the tile's rows in place in shared memory (a thread per 16 channels of a
-// 16-row block), then issues O^T = Vt^T Pt^T.  Pt and Vt are exact in fp16 (at most 6
+// recomputes S^T, quantises P (a 16-slot block is 16 lanes: block maxima by a half-warp
+// reduce-scatter, one scale rounded per lane) and re-quantises the tile's rows in place in shared
+// memory with packed fp16 comparisons (a thread per 8 channels of a 16-row block), in two steps of
+// two 128-channel blocks, so the MMAs O^T += Vt^T Pt^T of the first two blocks run while the
+// last two are re-quantised.  Pt and Vt are exact in fp16 (at most 6
 // significant bits), so O^T is one kind::f16 MMA per (channel block, 16 rows): the products a
 // block-scaled FP4 MMA would form, accumulated in fp32.
 //
@@ -69,6 +71,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
       mbar_init(&ms.bar_dq[c], kPfWorkers);
       mbar_init(&ms.bar_pv[c], 1);
     }
+    mbar_init(&ms.bar_v[0], kPfWorkers);
+    mbar_init(&ms.bar_v[1], kPfWorkers);
     fence_barrier_init();
   }
   if (warp == kPfMmaWarp) {
@@ -106,11 +110,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
           if (!second) mma_commit(&ms.bar_pv[cp]);  // pass 1: the chunk pair is free again
         }
         mma_commit(&ms.bar_s);
-        ok = mbar_wait(&ms.bar_p, g & 1) && ok;  // S^T read (and, pass 2, Pt and Vt written)
+        ok = mbar_wait(&ms.bar_p, g & 1) && ok;  // S^T read (and, pass 2, Pt written)
         tc_fence_after();
         if (second) {
           const int t = g - n_tiles;
           for (int qb = 0; qb < 4; ++qb) {
+            if ((qb & 1) == 0) {  // Vt of channel blocks qb, qb + 1 written
+              ok = mbar_wait(&ms.bar_v[qb >> 1], t & 1) && ok;
+              tc_fence_after();
+            }
 #pragma unroll
             for (int ks = 0; ks < kPfRows / 16; ++ks)
               mma_f16(tmem + qb * 64,
@@ -276,17 +284,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
               make_uint4(hv[0], hv[1], hv[2], hv[3]);
         }
       }
-      // ---- V re-quantised in place: thread = 16 channels of one 16-row block, 8 channels at a
-      //      time.  S^T(t) is complete (its commit arrived), so Khat is no longer read by it.
-      //      Every Khat value, scale and decision point T * sc is exact in fp16, so the code is
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&ms.bar_p);
+      // ---- V re-quantised in place, in two steps of two 128-channel blocks (the PV MMAs of
+      //      blocks 0-1 run during the second step): thread = 8 channels of one 16-row block.
+      //      S^T(t) is complete (its commit arrived), so Khat is no longer read by it.  Every
+      //      Khat value, scale and decision point T * sc is exact in fp16, so the code is
       //      decided by packed fp16 comparisons and the level sc * E2M1 built by accumulation.
       {
-        const int b = tid >> 5;                         // 16-row block 0..7
-        const int kc = lane >> 2, u0 = (lane & 3) * 2;  // chunk and its 16-byte units u0, u0+1
-        uint8_t *chunk = sm + kPfOffK + kc * kPfKChunk;
+        const int b = tid >> 5;  // 16-row block 0..7
+        const int u = lane & 7;  // 16-byte unit of the chunk
 #pragma unroll 1
-        for (int uu = 0; uu < 2; ++uu) {
-          const int u = u0 + uu;
+        for (int step = 0; step < 2; ++step) {
+          const int kc = 4 * step + (lane >> 3);  // chunks 0..3, then 4..7
+          uint8_t *chunk = sm + kPfOffK + kc * kPfKChunk;
           __half2 amax[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) amax[e] = __float2half2_rn(0.0f);
@@ -333,11 +345,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
             }
             *pv = make_uint4(w[0], w[1], w[2], w[3]);
           }
+          fence_async_smem();
+          mbar_arrive(&ms.bar_v[step]);
         }
       }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&ms.bar_p);
     }
 
     // ---- epilogue: sums of the quantised numerators, lse, O / l in bf16

@@ -59,6 +59,7 @@ static_assert(kPfSmem <= 232448, "shared memory per CTA");
 
 struct PfMisc {
   uint64_t bar_q, bar_s, bar_p, bar_dq[4], bar_pv[4];
+  uint64_t bar_v[2];  // full-FP4 PV variant: channel blocks 0-1 / 2-3 re-quantised
   uint32_t tmem_base;
   int flag[2];   // per tile parity: some score exceeded its reference maximum
   __align__(16) float mref[64];    // per-head reference maximum (log2 domain); read as float4
