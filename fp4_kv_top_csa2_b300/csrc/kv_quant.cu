@@ -5,45 +5,75 @@
 // warp moves 1 KB in with two 16-byte loads per lane and 256 + 32 bytes out with one 8-byte and
 // one 1-byte store per lane, all coalesced).  HBM-bound: 1024 B read + 288 B written per row.
 //
-// The code of x is E2M1(fp32(x / s)) rounded to nearest even.  It is computed without the
-// division: x is bf16 (8 significant bits) and s an E4M3 value (4), so x / s either equals a
-// decision point T (a midpoint between E2M1 neighbours: 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) or
-// differs from it by more than 2^-11 relative -- far more than one fp32 rounding -- and T * s
-// (at most 7 significant bits) is exact in fp32.  So comparing |x| with T * s takes exactly the
-// decision the rounded quotient takes, ties included.  Three comparisons find the code: against
-// 1.75 s, then 0.75 s or 3.5 s (all "at least": the even code wins a tie there), then 0.25 s,
-// 1.25 s, 2.5 s or 5 s ("greater than": the even code is below).
+// The code of x is E2M1(fp32(x / s)) rounded to nearest even.  x is bf16 (8 significant bits)
+// and s an E4M3 value (4), so x / s either equals a decision point T (a midpoint between E2M1
+// neighbours: 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) or differs from it by more than 2^-9
+// relative -- far more than an fp32 rounding.  The kernel forms the quotient without a division:
+// q0 = x * rcp(s), then one correction q = q0 - (q0 s - x) rcp(s) (the remainder is exact in an
+// fma).  q is within an ulp of x / s, and equals T exactly when x = T s, so the hardware
+// conversion to E2M1 (round to nearest even, saturating at 6) takes the decision the rounded
+// quotient takes, ties included.  A group holding an infinity takes the comparison path instead
+// (|x| against the exact products T * s, three comparisons per value), which saturates it.
 #include "common.cuh"
 
 namespace csa2 {
 
+// Eight fp32 values -> eight E2M1 codes in one word (value 2k in the low nibble of byte k), by
+// the conversion instruction: round to nearest even, saturating at +-6, sign kept.
+__device__ __forceinline__ uint32_t e2m1x8_rn(const float *q) {
+  uint32_t w;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}\n"
+      : "=r"(w)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return w;
+}
+
 // Quantise one 16-channel group held as 8 packed bf16 pairs.  Returns the scale code and writes
 // the 8 code bytes (channel 2j low nibble, 2j+1 high nibble) into *codes64.
 __device__ __forceinline__ uint32_t quant_group16(const uint32_t (&v)[8], uint64_t *codes64) {
-  float x[16];
+  // amax by packed bf16 maxima of the magnitudes (exact)
+  uint32_t m = v[0] & 0x7FFF7FFFu;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    x[2 * i] = bf16_lo(v[i]);
-    x[2 * i + 1] = bf16_hi(v[i]);
+  for (int i = 1; i < 8; ++i) {
+    const uint32_t a = v[i] & 0x7FFF7FFFu;
+    __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&m),
+                               *reinterpret_cast<const __nv_bfloat162 *>(&a));
+    m = *reinterpret_cast<const uint32_t *>(&r);
   }
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const float amax = fmaxf(bf16_lo(m), bf16_hi(m));
   const uint32_t scode = float_to_e4m3_sat(__fdiv_rn(amax, 6.0f));
   const float sd = e4m3_to_float(scode);
   uint64_t packed = 0;
-  if (sd != 0.0f) {
+  if (sd != 0.0f && amax < INFINITY) {
+    const float rcp = __frcp_rn(sd);
+    float q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float x = (i & 1) ? bf16_hi(v[i >> 1]) : bf16_lo(v[i >> 1]);
+      const float q0 = x * rcp;
+      // q0 - (q0 s - x) rcp: the remainder's sign is chosen so that x = -0 keeps its sign
+      // (-0 + -0); written as x - q0 s it would come out +0
+      q[i] = fmaf(-fmaf(q0, sd, -x), rcp, q0);
+    }
+    packed = ((uint64_t)e2m1x8_rn(q + 8) << 32) | e2m1x8_rn(q);
+  } else if (sd != 0.0f) {
     const float t1 = 0.25f * sd, t2 = 0.75f * sd, t3 = 1.25f * sd, t4 = 1.75f * sd;
     const float t5 = 2.5f * sd, t6 = 3.5f * sd, t7 = 5.0f * sd;
     uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float a = fabsf(x[i]);
+      const float x = (i & 1) ? bf16_hi(v[i >> 1]) : bf16_lo(v[i >> 1]);
+      const float a = fabsf(x);
       const bool ge4 = a >= t4;
       const bool ge2 = a >= (ge4 ? t6 : t2);
       const bool gt1 = a > (ge2 ? (ge4 ? t7 : t3) : (ge4 ? t5 : t1));
       const uint32_t code = (ge4 ? 4u : 0u) | (ge2 ? 2u : 0u) | (gt1 ? 1u : 0u) |
-                            ((__float_as_uint(x[i]) >> 28) & 8u);
+                            ((__float_as_uint(x) >> 28) & 8u);
       if (i < 8) lo |= code << (4 * i);
       else hi |= code << (4 * (i - 8));
     }
