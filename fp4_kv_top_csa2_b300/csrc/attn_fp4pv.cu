@@ -10,10 +10,15 @@
 // The maximum must be known before any numerator is quantised, so the kernel makes two passes
 // over the token's tiles: the first computes S^T only and keeps each head's maximum; the second
 // recomputes S^T, quantises P (a 16-slot block is 16 lanes: block maxima by a half-warp
-// reduce-scatter, one scale rounded per lane) and re-quantises the tile's rows in place in shared
-// memory with packed fp16 comparisons (a thread per 8 channels of a 16-row block), in two steps of
-// two 128-channel blocks, so the MMAs O^T += Vt^T Pt^T of the first two blocks run while the
-// last two are re-quantised.  Pt and Vt are exact in fp16 (at most 6
+// reduce-scatter, one scale and its reciprocal rounded per lane) and re-quantises the tile's rows
+// in place in shared memory (a thread per 8 channels of a 16-row block), in two steps of two
+// 128-channel blocks, so the MMAs O^T += Vt^T Pt^T of the first two blocks run while the last two
+// are re-quantised.  Both roundings take the quotient x / sc to within an ulp (a product with the
+// reciprocal, corrected once by the exact remainder) and the hardware E2M1 conversion (nearest,
+// ties to even, saturating).  A row value has at most 6 significant bits and sc at most 4, so
+// x / sc equals a decision point exactly or lies far more than an ulp from it: Vt is exactly the
+// rounding of the quotient.  A numerator p has 24 bits: Pt can differ from that rounding only
+// where p / sc lies within an ulp of a decision point.  Pt and Vt are exact in fp16 (at most 6
 // significant bits), so O^T is one kind::f16 MMA per (channel block, 16 rows): the products a
 // block-scaled FP4 MMA would form, accumulated in fp32.
 //
@@ -29,25 +34,22 @@ __device__ __forceinline__ float fp4_scale(float amax) {
   return e4m3_to_float(float_to_e4m3_sat(__fdiv_rn(amax, 6.0f)));
 }
 
-// Block-scaled FP4 value of x >= 0 under scale sc: E2M1(x / sc) * sc, round to nearest with ties
-// to the even code, saturating at 6.  Decided by comparing x with the decision points T * sc
-// (T = 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5; each product exact in fp32), as the main-KV
-// quantiser does: for x with at most 8 significant bits (a dequantised row) this is exactly the
-// rounding of the fp32 quotient; for a numerator it can differ from it only where x / sc lies
-// within an ulp of a decision point.
-__device__ __forceinline__ float fp4_value(float x, float sc) {
-  // three comparisons pick the code (the even code wins a tie: "at least" against 1.75, 0.75 and
-  // 3.5, "greater than" against 0.25, 1.25, 2.5 and 5), without branches
-  const bool ge4 = x >= 1.75f * sc;
-  const bool ge2 = x >= (ge4 ? 3.5f : 0.75f) * sc;
-  const bool gt1 = x > (ge2 ? (ge4 ? 5.0f : 1.25f) : (ge4 ? 2.5f : 0.25f)) * sc;
-  const uint32_t code = (ge4 ? 4u : 0u) | (ge2 ? 2u : 0u) | (gt1 ? 1u : 0u);
-  return sc == 0.0f ? 0.0f : e2m1_to_float(code) * sc;
+// The quotient x / sc to within an ulp, without a division: q0 = x * rcp, corrected once by the
+// remainder (exact in an fma), written so that x = -0 gives -0.  rcp = 0 for sc = 0 gives 0.
+__device__ __forceinline__ float fp4_quot(float x, float sc, float rcp) {
+  const float q0 = x * rcp;
+  return fmaf(-fmaf(q0, sc, -x), rcp, q0);
 }
 
-// The E2M1 decision points in units of the scale, in increasing order (the packed re-quantisation
-// adds 0.5, 0.5, 0.5, 0.5, 1, 1, 2 as x passes them).
-__device__ constexpr float kFp4Cut[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+// Two quotients -> their E2M1 values (round to nearest even, saturating at 6, sign kept) as an
+// fp16 pair, lo in the low half, by the conversion instructions.
+__device__ __forceinline__ uint32_t e2m1_round_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n .reg .b8 b;\n cvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}\n"
+      : "=r"(r)
+      : "f"(lo), "f"(hi));
+  return r;
+}
 
 __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
     const uint16_t *__restrict__ q_bf16, int H, const int32_t *__restrict__ q_seq,
@@ -262,21 +264,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
           }
         }
         const float sc_mine = fp4_scale(t[0]);
+        const float rcp_mine = sc_mine == 0.0f ? 0.0f : __frcp_rn(sc_mine);
 #pragma unroll
         for (int uh = 0; uh < 2; ++uh) {
           uint32_t hv[4];
 #pragma unroll
           for (int k = 0; k < 8; k += 2) {
-            float pt[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int i = 8 * uh + k + e;
-              const float sc = __shfl_sync(0xffffffffu, sc_mine, (lane & 16) | i);
-              pt[e] = fp4_value(p[i], sc);
-              lpart[16 * hb + i] += pt[e];
-            }
-            const __half2 h2 = __floats2half2_rn(pt[0], pt[1]);  // exact: <= 6 significant bits
-            hv[k / 2] = *reinterpret_cast<const uint32_t *>(&h2);
+            const int i = 8 * uh + k;
+            const int src = (lane & 16) | i;
+            const float sc0 = __shfl_sync(0xffffffffu, sc_mine, src);
+            const float sc1 = __shfl_sync(0xffffffffu, sc_mine, src + 1);
+            const float r0 = __shfl_sync(0xffffffffu, rcp_mine, src);
+            const float r1 = __shfl_sync(0xffffffffu, rcp_mine, src + 1);
+            // Pt = E2M1(p / sc) * sc, exact in fp16 (at most 6 significant bits)
+            const uint32_t lv = e2m1_round_f16x2(fp4_quot(p[i], sc0, r0), fp4_quot(p[i + 1], sc1, r1));
+            const __half2 sc2 = __floats2half2_rn(sc0, sc1);  // exact: E4M3 values
+            const __half2 pt = __hmul2(*reinterpret_cast<const __half2 *>(&lv), sc2);
+            const float2 ptf = __half22float2(pt);
+            lpart[16 * hb + i] += ptf.x;
+            lpart[16 * hb + i + 1] += ptf.y;
+            hv[k / 2] = *reinterpret_cast<const uint32_t *>(&pt);
           }
           const int u = 2 * hb + uh;
           const int off = jrow * 128 + (((4 * hh + u) ^ (jrow & 7)) << 4);
@@ -289,9 +296,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
       mbar_arrive(&ms.bar_p);
       // ---- V re-quantised in place, in two steps of two 128-channel blocks (the PV MMAs of
       //      blocks 0-1 run during the second step): thread = 8 channels of one 16-row block.
-      //      S^T(t) is complete (its commit arrived), so Khat is no longer read by it.  Every
-      //      Khat value, scale and decision point T * sc is exact in fp16, so the code is
-      //      decided by packed fp16 comparisons and the level sc * E2M1 built by accumulation.
+      //      S^T(t) is complete (its commit arrived), so Khat is no longer read by it.  The
+      //      level E2M1(x / sc) times sc is exact in fp16.
       {
         const int b = tid >> 5;  // 16-row block 0..7
         const int u = lane & 7;  // 16-byte unit of the chunk
@@ -311,16 +317,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
             for (int e = 0; e < 4; ++e)
               amax[e] = __hmax2(amax[e], __habs2(*reinterpret_cast<const __half2 *>(&w[e])));
           }
-          __half2 sc2[4], th[4][7];
+          __half2 sc2[4];
+          float2 scf[4], rcp[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 m = __half22float2(amax[e]);
-            sc2[e] = __floats2half2_rn(fp4_scale(m.x), fp4_scale(m.y));  // exact: E4M3 values
-#pragma unroll
-            for (int k = 0; k < 7; ++k) th[e][k] = __hmul2(sc2[e], __float2half2_rn(kFp4Cut[k]));
+            scf[e] = make_float2(fp4_scale(m.x), fp4_scale(m.y));
+            rcp[e] = make_float2(scf[e].x == 0.0f ? 0.0f : __frcp_rn(scf[e].x),
+                                 scf[e].y == 0.0f ? 0.0f : __frcp_rn(scf[e].y));
+            sc2[e] = __floats2half2_rn(scf[e].x, scf[e].y);  // exact: E4M3 values
           }
-          const __half2 half = __float2half2_rn(0.5f), one = __float2half2_rn(1.0f),
-                        two = __float2half2_rn(2.0f);
 #pragma unroll 4
           for (int rr = 0; rr < 16; ++rr) {
             const int j = 16 * b + rr;
@@ -329,19 +335,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
             uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const __half2 a = __habs2(*reinterpret_cast<const __half2 *>(&w[e]));
-              // ties to the even code: "greater than" at 0.25, 1.25, 2.5, 5; "at least" at
-              // 0.75, 1.75, 3.5 (as fp4_value)
-              __half2 lv = __hmul2(__hgt2(a, th[e][0]), half);
-              lv = __hfma2(__hge2(a, th[e][1]), half, lv);
-              lv = __hfma2(__hgt2(a, th[e][2]), half, lv);
-              lv = __hfma2(__hge2(a, th[e][3]), half, lv);
-              lv = __hfma2(__hgt2(a, th[e][4]), one, lv);
-              lv = __hfma2(__hge2(a, th[e][5]), one, lv);
-              lv = __hfma2(__hgt2(a, th[e][6]), two, lv);
-              const __half2 q = __hmul2(lv, sc2[e]);  // exact: <= 6 significant bits
-              w[e] = (*reinterpret_cast<const uint32_t *>(&q) & 0x7FFF7FFFu) |
-                     (w[e] & 0x80008000u);
+              const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
+              const uint32_t lv = e2m1_round_f16x2(fp4_quot(f.x, scf[e].x, rcp[e].x),
+                                                   fp4_quot(f.y, scf[e].y, rcp[e].y));
+              const __half2 q = __hmul2(*reinterpret_cast<const __half2 *>(&lv), sc2[e]);  // exact
+              w[e] = *reinterpret_cast<const uint32_t *>(&q);
             }
             *pv = make_uint4(w[0], w[1], w[2], w[3]);
           }

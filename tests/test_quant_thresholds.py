@@ -57,39 +57,59 @@ def test_ties_go_to_the_even_code():
 E2M1_LEVELS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 
 
-def _fp16_ladder(a16, s16):
-    """The full-FP4 PV attention's re-quantisation of a dequantised row value |v| (fp16) under a
-    block scale s (fp16): the level grows by 0.5, 0.5, 0.5, 0.5, 1, 1, 2 as |v| passes the
-    decision points T * s (fp16 products), ties to the even code, then is multiplied by s."""
-    th = [np.float16(m) * s16 for m in MIDS]
-    half, one, two = np.float16(0.5), np.float16(1.0), np.float16(2.0)
-    lv = (a16 > th[0]).astype(np.float16) * half
-    lv = lv + (a16 >= th[1]).astype(np.float16) * half
-    lv = lv + (a16 > th[2]).astype(np.float16) * half
-    lv = lv + (a16 >= th[3]).astype(np.float16) * half
-    lv = lv + (a16 > th[4]).astype(np.float16) * one
-    lv = lv + (a16 >= th[5]).astype(np.float16) * one
-    lv = lv + (a16 > th[6]).astype(np.float16) * two
-    return th, lv * s16
+def _corrected_quotient(x32, s32):
+    """The kernels' division-free quotient in fp32: q0 = x * rcp(s), then q0 - (q0 s - x) rcp(s).
+    Both fma steps are emulated in float64: q0 s - x is exact there, and the last step is exact
+    to far below an fp32 ulp (enough for these checks)."""
+    r = np.float32(1.0) / s32
+    q0 = (x32 * r).astype(np.float32)
+    rem = (q0.astype(np.float64) * np.float64(s32) - x32.astype(np.float64)).astype(np.float32)
+    return (q0.astype(np.float64) - rem.astype(np.float64) * np.float64(r)).astype(np.float32)
 
 
-def test_fp16_requantisation_of_dequantised_rows_is_exact():
-    """Every dequantised cache value (E2M1 magnitude x positive E4M3 scale) and every decision
-    point T * s is exactly representable as a normal fp16 number, so packed fp16 comparisons
-    decide the FP4 code of v / s as rounding the exact quotient does, and the level times s is
-    exact too.  Checked for every such value against every positive E4M3 scale."""
+def test_requantisation_of_dequantised_rows_is_exact():
+    """The FP4 quantiser and the full-FP4 PV attention round x / s to E2M1 by a division-free
+    fp32 quotient and the hardware conversion (nearest, ties to even).  For the values the PV
+    variant re-quantises -- dequantised cache values, E2M1 magnitude x positive E4M3 scale --
+    against every positive E4M3 scale s:
+      * x / s equals a decision point exactly or lies more than 2^-12 (relative) from every one,
+        far beyond the quotient's error of an ulp, so the decision is the exact quotient's;
+      * at an exact decision point the corrected quotient is exactly that point, and the
+        rounding of the emulated quotient equals rounding the exact one everywhere;
+      * the level times s is exact and normal in fp16 (the MMA operand format).
+    Also: -0 keeps its sign through the quotient."""
     e4 = _e4m3_positive()
     vals = np.unique(np.outer(E2M1_LEVELS, e4).ravel())
-    a16 = vals.astype(np.float16)
-    assert (a16.astype(np.float64) == vals).all()
-    assert (vals[vals > 0] >= 2.0 ** -14).all()  # no fp16 subnormals
+    x32 = np.concatenate([vals, -vals]).astype(np.float32)
+    assert (np.abs(x32).astype(np.float64) == np.concatenate([vals, vals])).all()
     for s in e4:
-        s16 = np.float16(s)
-        assert float(s16) == s
-        th, q = _fp16_ladder(a16, s16)
-        assert all(float(t) == m * s and float(t) >= 2.0 ** -14 for t, m in zip(th, MIDS))
-        ref = E2M1_LEVELS[_rne_code(vals / s)] * s
-        assert (q.astype(np.float64) == ref).all(), s
-    # a block of zeros has scale 0 and stays zero
-    _, q0 = _fp16_ladder(np.zeros(3, np.float16), np.float16(0.0))
-    assert (q0 == 0).all()
+        s32 = np.float32(s)
+        exact = x32.astype(np.float64) / s
+        a = np.abs(exact)
+        near = np.min(np.abs(a[:, None] / MIDS[None, :] - 1.0), axis=1)
+        on = near == 0.0
+        assert (near[~on] > 2.0 ** -12).all(), s
+        q = _corrected_quotient(x32, s32)
+        assert (np.abs(q[on]).astype(np.float64) == a[on]).all(), s
+        assert (_rne_code(q.astype(np.float64)) == _rne_code(exact)).all(), s
+        lv = E2M1_LEVELS[_rne_code(exact)] * s
+        lv16 = lv.astype(np.float16)
+        assert (lv16.astype(np.float64) == lv).all() and (lv[lv > 0] >= 2.0 ** -14).all(), s
+    q = _corrected_quotient(np.array([-0.0, 0.0], np.float32), np.float32(0.375))
+    assert np.signbit(q).tolist() == [True, False]
+
+
+def test_corrected_quotient_codes_equal_rounded_quotient_codes():
+    """The FP4 quantiser's codes come from the division-free quotient (see above) and the
+    hardware E2M1 rounding.  For every finite bf16 value x and every positive E4M3 scale s whose
+    quotient stays finite in fp32 (a group's own scale keeps |x / s| below 8, or saturates at 448),
+    the rounding of the emulated quotient equals the rounding of the exact one."""
+    bits = np.arange(1 << 16, dtype=np.uint32) << 16
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    for s in _e4m3_positive():
+        xs = x[np.abs(x.astype(np.float64) / s) < 2.0 ** 120]
+        q = _corrected_quotient(xs, np.float32(s))
+        got = _rne_code(q.astype(np.float64))
+        ref = _rne_code(xs.astype(np.float64) / s)
+        assert (got == ref).all(), (s, xs[got != ref][:5])
