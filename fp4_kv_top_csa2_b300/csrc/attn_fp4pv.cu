@@ -15,10 +15,11 @@
 // 128-channel blocks, so the MMAs O^T += Vt^T Pt^T of the first two blocks run while the last two
 // are re-quantised.  Both roundings take the quotient x / sc to within an ulp (a product with the
 // reciprocal, corrected once by the exact remainder) and the hardware E2M1 conversion (nearest,
-// ties to even, saturating).  A row value has at most 6 significant bits and sc at most 4, so
-// x / sc equals a decision point exactly or lies far more than an ulp from it: Vt is exactly the
-// rounding of the quotient.  A numerator p has 24 bits: Pt can differ from that rounding only
-// where p / sc lies within an ulp of a decision point.  Pt and Vt are exact in fp16 (at most 6
+// ties to even, saturating); the rows' quotients are formed in packed fp16.  A row value has at
+// most 6 significant bits and sc at most 4, so x / sc equals a decision point exactly or lies
+// more than 2^-7 (relative) from one: Vt is exactly the rounding of the quotient.  A numerator
+// p has 24 bits: Pt can differ from that rounding only where p / sc lies within an ulp of a
+// decision point.  Pt and Vt are exact in fp16 (at most 6
 // significant bits), so O^T is one kind::f16 MMA per (channel block, 16 rows): the products a
 // block-scaled FP4 MMA would form, accumulated in fp32.
 //
@@ -48,6 +49,20 @@ __device__ __forceinline__ uint32_t e2m1_round_f16x2(float lo, float hi) {
   asm("{\n .reg .b8 b;\n cvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}\n"
       : "=r"(r)
       : "f"(lo), "f"(hi));
+  return r;
+}
+
+// The same for a pair of fp16 row values (at most 6 significant bits) under fp16 scales and
+// reciprocals: the quotient to within an fp16 ulp, exact at a decision point, then E2M1 and back
+// to fp16 by the conversion instructions.  Every such x / sc lies on a decision point or more than
+// 2^-7 (relative) from one, so the fp16 quotient decides as the exact one does.
+__device__ __forceinline__ uint32_t fp4_level_f16x2(__half2 x, __half2 sc, __half2 rcp) {
+  const __half2 q0 = __hmul2(x, rcp);
+  const __half2 q = __hfma2(__hneg2(__hfma2(q0, sc, __hneg2(x))), rcp, q0);
+  uint32_t r;
+  asm("{\n .reg .b8 b;\n cvt.rn.satfinite.e2m1x2.f16x2 b, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}\n"
+      : "=r"(r)
+      : "r"(*reinterpret_cast<const uint32_t *>(&q)));
   return r;
 }
 
@@ -317,15 +332,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
             for (int e = 0; e < 4; ++e)
               amax[e] = __hmax2(amax[e], __habs2(*reinterpret_cast<const __half2 *>(&w[e])));
           }
-          __half2 sc2[4];
-          float2 scf[4], rcp[4];
+          __half2 sc2[4], rc2[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 m = __half22float2(amax[e]);
-            scf[e] = make_float2(fp4_scale(m.x), fp4_scale(m.y));
-            rcp[e] = make_float2(scf[e].x == 0.0f ? 0.0f : __frcp_rn(scf[e].x),
-                                 scf[e].y == 0.0f ? 0.0f : __frcp_rn(scf[e].y));
-            sc2[e] = __floats2half2_rn(scf[e].x, scf[e].y);  // exact: E4M3 values
+            const float sx = fp4_scale(m.x), sy = fp4_scale(m.y);
+            sc2[e] = __floats2half2_rn(sx, sy);  // exact: E4M3 values
+            rc2[e] = __floats2half2_rn(sx == 0.0f ? 0.0f : __frcp_rn(sx),
+                                       sy == 0.0f ? 0.0f : __frcp_rn(sy));
           }
 #pragma unroll 4
           for (int rr = 0; rr < 16; ++rr) {
@@ -335,9 +349,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
             uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-              const uint32_t lv = e2m1_round_f16x2(fp4_quot(f.x, scf[e].x, rcp[e].x),
-                                                   fp4_quot(f.y, scf[e].y, rcp[e].y));
+              const uint32_t lv =
+                  fp4_level_f16x2(*reinterpret_cast<const __half2 *>(&w[e]), sc2[e], rc2[e]);
               const __half2 q = __hmul2(*reinterpret_cast<const __half2 *>(&lv), sc2[e]);  // exact
               w[e] = *reinterpret_cast<const uint32_t *>(&q);
             }

@@ -67,13 +67,25 @@ def _corrected_quotient(x32, s32):
     return (q0.astype(np.float64) - rem.astype(np.float64) * np.float64(r)).astype(np.float32)
 
 
+def _corrected_quotient_f16(x16, s32):
+    """The same quotient in packed fp16, as the full-FP4 PV attention forms it for row values:
+    rcp = fp16(fp32 1 / s), q0 = x * rcp, then q0 - (q0 s - x) rcp, each step rounded to fp16
+    once (a product of two fp16 values is exact in fp32; the fma steps are exact in float64)."""
+    s16 = np.float16(s32)
+    r16 = np.float16(np.float32(1.0) / s32)
+    q0 = (x16.astype(np.float32) * np.float32(r16)).astype(np.float16)
+    rem = (q0.astype(np.float64) * float(s16) - x16.astype(np.float64)).astype(np.float16)
+    return (q0.astype(np.float64) - rem.astype(np.float64) * float(r16)).astype(np.float16)
+
+
 def test_requantisation_of_dequantised_rows_is_exact():
     """The FP4 quantiser and the full-FP4 PV attention round x / s to E2M1 by a division-free
     fp32 quotient and the hardware conversion (nearest, ties to even).  For the values the PV
     variant re-quantises -- dequantised cache values, E2M1 magnitude x positive E4M3 scale --
     against every positive E4M3 scale s:
-      * x / s equals a decision point exactly or lies more than 2^-12 (relative) from every one,
-        far beyond the quotient's error of an ulp, so the decision is the exact quotient's;
+      * x / s equals a decision point exactly or lies more than 2^-7 (relative) from every one,
+        far beyond the quotient's error of an ulp (fp32, or fp16 for the PV variant's rows), so
+        the decision is the exact quotient's;
       * at an exact decision point the corrected quotient is exactly that point, and the
         rounding of the emulated quotient equals rounding the exact one everywhere;
       * the level times s is exact and normal in fp16 (the MMA operand format).
@@ -88,10 +100,15 @@ def test_requantisation_of_dequantised_rows_is_exact():
         a = np.abs(exact)
         near = np.min(np.abs(a[:, None] / MIDS[None, :] - 1.0), axis=1)
         on = near == 0.0
-        assert (near[~on] > 2.0 ** -12).all(), s
+        assert (near[~on] > 2.0 ** -7).all(), s
         q = _corrected_quotient(x32, s32)
         assert (np.abs(q[on]).astype(np.float64) == a[on]).all(), s
         assert (_rne_code(q.astype(np.float64)) == _rne_code(exact)).all(), s
+        # the PV variant's packed fp16 quotient, for a block's own scale (|x| <= amax <= 6.4 s)
+        own = np.abs(x32) <= 6.5 * s
+        q16 = _corrected_quotient_f16(x32[own].astype(np.float16), s32)
+        assert (np.abs(q16[on[own]]).astype(np.float64) == a[own][on[own]]).all(), s
+        assert (_rne_code(q16.astype(np.float64)) == _rne_code(exact[own])).all(), s
         lv = E2M1_LEVELS[_rne_code(exact)] * s
         lv16 = lv.astype(np.float16)
         assert (lv16.astype(np.float64) == lv).all() and (lv[lv > 0] >= 2.0 ** -14).all(), s
