@@ -66,6 +66,22 @@ __device__ __forceinline__ uint32_t fp4_level_f16x2(__half2 x, __half2 sc, __hal
   return r;
 }
 
+// The main-KV scale rule E4M3(fp32(amax / 6)) for a pair of fp16 block maxima of row values (at
+// most 6 significant bits), as an fp16 pair (exact: E4M3 values are fp16 normals).  The fp16
+// quotient amax * fp16(1/6), corrected once by the remainder, is exact where amax / 6 lies on an
+// E4M3 rounding boundary (a few maxima do, in the subnormal range) and within an ulp elsewhere,
+// far from every boundary; the hardware E4M3 conversion then rounds it as the fp32 quotient
+// rounds (checked for every possible maximum).
+__device__ __forceinline__ __half2 fp4_scale_f16x2(__half2 amax) {
+  const __half2 six = __float2half2_rn(6.0f), r6 = __float2half2_rn(1.0f / 6.0f);
+  const __half2 q0 = __hmul2(amax, r6);
+  const __half2 q = __hfma2(__hneg2(__hfma2(q0, six, __hneg2(amax))), r6, q0);
+  uint16_t e;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e) : "r"(*reinterpret_cast<const uint32_t *>(&q)));
+  const uint32_t h = e4m3x2_to_f16x2(e);
+  return *reinterpret_cast<const __half2 *>(&h);
+}
+
 __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
     const uint16_t *__restrict__ q_bf16, int H, const int32_t *__restrict__ q_seq,
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ sf,
@@ -335,11 +351,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
           __half2 sc2[4], rc2[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 m = __half22float2(amax[e]);
-            const float sx = fp4_scale(m.x), sy = fp4_scale(m.y);
-            sc2[e] = __floats2half2_rn(sx, sy);  // exact: E4M3 values
-            rc2[e] = __floats2half2_rn(sx == 0.0f ? 0.0f : __frcp_rn(sx),
-                                       sy == 0.0f ? 0.0f : __frcp_rn(sy));
+            sc2[e] = fp4_scale_f16x2(amax[e]);
+            const float2 sf2 = __half22float2(sc2[e]);
+            rc2[e] = __floats2half2_rn(sf2.x == 0.0f ? 0.0f : __frcp_rn(sf2.x),
+                                       sf2.y == 0.0f ? 0.0f : __frcp_rn(sf2.y));
           }
 #pragma unroll 4
           for (int rr = 0; rr < 16; ++rr) {

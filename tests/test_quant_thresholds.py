@@ -130,3 +130,44 @@ def test_corrected_quotient_codes_equal_rounded_quotient_codes():
         got = _rne_code(q.astype(np.float64))
         ref = _rne_code(xs.astype(np.float64) / s)
         assert (got == ref).all(), (s, xs[got != ref][:5])
+
+
+def _e4m3_rne(y):
+    """Nearest E4M3 value to each y >= 0 (codes 0x00..0x7E), ties to the even code, saturating at
+    448: a search over the whole code table."""
+    vals = np.concatenate([[0.0], _e4m3_positive()])
+    codes = np.arange(0x7F)
+    out = []
+    for v in np.asarray(y, dtype=np.float64):
+        if v >= 448.0:
+            out.append(448.0)
+            continue
+        d = np.abs(vals - v)
+        idx = np.nonzero(d == d.min())[0]
+        if len(idx) > 1:
+            idx = [i for i in idx if codes[i] % 2 == 0]
+        out.append(vals[idx[0]])
+    return np.array(out)
+
+
+def test_fp16_block_scale_of_row_values_is_exact():
+    """The full-FP4 PV attention computes V's block scales E4M3(fp32(amax / 6)) from fp16 block
+    maxima: the fp16 quotient q0 = amax * fp16(1/6), corrected once by the remainder, then the
+    hardware E4M3 rounding.  For every possible maximum of dequantised row values (E2M1 magnitude
+    x E4M3 scale, and 0) the result equals the rounding of the fp32 quotient, also when q0 is
+    one fp16 ulp off either way: the correction, not a lucky rounding, decides the ties (some
+    maxima put amax / 6 exactly on an E4M3 midpoint in the subnormal range)."""
+    amax = np.unique(np.outer(E2M1_LEVELS, _e4m3_positive()).ravel())
+    ref = _e4m3_rne((amax.astype(np.float32) / np.float32(6.0)).astype(np.float64))
+    a16 = amax.astype(np.float16)
+    assert (a16.astype(np.float64) == amax).all()
+    r6 = np.float16(np.float32(1.0) / np.float32(6.0))
+    q0 = (a16.astype(np.float32) * np.float32(r6)).astype(np.float16)
+    pos = amax > 0
+    for step in (0, -1, 1):
+        q0p = q0 if step == 0 else np.nextafter(q0, np.float16(np.inf * step)).astype(np.float16)
+        rem = (q0p.astype(np.float64) * 6.0 - amax).astype(np.float16)
+        q = (q0p.astype(np.float64) - rem.astype(np.float64) * float(r6)).astype(np.float16)
+        assert (_e4m3_rne(q[pos].astype(np.float64)) == ref[pos]).all(), step
+    ties = np.nonzero(np.abs(amax / 6 / 2.0 ** -9 % 1 - 0.5) == 0)[0]
+    assert ties.size > 0  # midpoints of the subnormal quantum occur
