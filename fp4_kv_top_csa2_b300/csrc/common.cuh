@@ -39,18 +39,14 @@ __device__ __forceinline__ float e2m1_to_float(uint32_t c) {
   return (c & 8u) ? -mag : mag;
 }
 
-// float >= 0 -> E4M3 code, round to nearest even, saturating at 448 (0x7E).
+// float >= 0 -> E4M3 code, round to nearest even (subnormals included), saturating at 448 (0x7E),
+// by the conversion instruction; +inf and NaN also give 0x7E.
 __device__ __forceinline__ uint32_t float_to_e4m3_sat(float s) {
-  if (!(s < 448.0f)) return 0x7Eu;  // also catches +inf
-  if (s < 0x1p-6f) {                 // subnormal range: quantum 2^-9
-    return (uint32_t)__float2int_rn(s * 512.0f);  // 8 -> code 8 == 2^-6, continuous
-  }
-  uint32_t u = __float_as_uint(s);
-  uint32_t exp = u >> 23, man = u & 0x7FFFFFu;
-  uint32_t r = man >> 20, rem = man & 0xFFFFFu;
-  uint32_t up = (rem > 0x80000u) || (rem == 0x80000u && (r & 1u));
-  // (exp - 127 + 7) << 3 | r, plus the rounding carry into the exponent field
-  return (((exp - 120u) << 3) | r) + up;
+  if (!(s < 448.0f)) return 0x7Eu;
+  uint16_t two;
+  // the first source lands in the upper byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(two) : "f"(0.0f), "f"(s));
+  return two & 0xFFu;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
