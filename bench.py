@@ -319,6 +319,7 @@ def run_ours(args, rank, world):
         # the headline step with every layer's local sliding window (128 FP8 local rows)
         line["hier_decode_swa"] = run_decode_config(HEADLINE_SWA, args, dev, peaks, flush)
         line["index_keys"] = run_index_keys(args, dev, peaks, flush)
+        line["kv_quant"] = run_kv_quant(args, dev, peaks, flush)
     if args.prefill and rank == 0:
         line["prefill"] = run_prefill(args, dev, peaks)
         line["prefill_hier"] = run_prefill_hier(args, dev)
@@ -471,6 +472,23 @@ def run_index_keys(args, dev, peaks, flush, n_rows=1 << 20):
             "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
             "gbs": round(by / (ms / 1e3) / 1e9, 1),
             "frac_of_hbm": round(by / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
+
+
+def run_kv_quant(args, dev, peaks, flush, n_rows=1 << 20):
+    """FP4 quantisation of 1,048,576 bf16 rows (the 1M-context cache build): 1,024 B read and
+    256 + 32 B written per row.  Rows drawn with a per-channel spread of two decades."""
+    import torch
+    from fp4_kv_top_csa2_b300 import csa2
+    g = torch.Generator(device=dev).manual_seed(0)
+    sigma = 10.0 ** (torch.rand(512, device=dev, generator=g) * 2 - 1)
+    x = (torch.randn(n_rows, 512, device=dev, generator=g) * sigma).to(torch.bfloat16)
+    codes = torch.empty((n_rows, 256), dtype=torch.uint8, device=dev)
+    sf = torch.empty((n_rows, 32), dtype=torch.uint8, device=dev)
+    ms = time_graph(lambda s: csa2.csa2_kv_quant_fp4(x, codes, sf, stream=s), args.steps, flush)
+    by = n_rows * (1024 + 256 + 32)
+    gbs = by / (ms / 1e3) / 1e9
+    return {"rows": n_rows, "ms": round(ms, 4), "gbs": round(gbs, 1),
+            "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
 
 
 def run_e2e(st, steps, dev, world=1, graph=False):
