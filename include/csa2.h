@@ -78,7 +78,9 @@ const char *csa2_error_string(int status);
  *          one new token per sequence into a ragged cache).  NULL means output row i.
  * codes    [*, d/2] uint8: byte j of a row = channel 2j (low nibble) | channel 2j+1 (high nibble).
  * sf       [*, d/16] uint8: byte g = E4M3 scale of channels 16g..16g+15.
- * Output codes and scales are bit-exact functions of the input (no accumulation order).
+ * Output codes and scales are bit-exact functions of the input (no accumulation order).  An
+ * infinite x saturates like any large value (its group's scale is 448, its code 0x7 or 0xF);
+ * NaN inputs are outside the definition and give unspecified codes.
  */
 int csa2_kv_quant_fp4(const void *x_bf16, int64_t n_rows, int d, const int64_t *out_rows,
                       uint8_t *codes, uint8_t *sf, void *stream);

@@ -58,6 +58,9 @@ def _edge_rows():
     z = np.zeros(512)
     z[::3] = -0.0
     rows.append(z)
+    inf = np.linspace(-5.0, 5.0, 512)  # groups holding an infinity saturate (scale 448, code 7)
+    inf[3], inf[16 + 9], inf[32], inf[33] = np.inf, -np.inf, np.inf, -np.inf
+    rows.append(inf)
     return torch.tensor(np.array(rows), dtype=torch.float32).to(torch.bfloat16)
 
 
