@@ -74,3 +74,44 @@ def test_dominant_rows_take_all_the_weight():
     vt = _requant_columns(kv[idx])
     want = vt[[3, 40, 41, 99]].mean(0)
     assert np.allclose(out[0], want, rtol=1e-13, atol=1e-13)
+
+
+# Worked example of P's re-quantisation.  The cache rows are one-hot: row j holds 1.0 in channel
+# j, which quantises to E2M1 6 x E4M3(1/6) = 6 x 0.171875 = 1.03125, so the dequantised row is
+# 1.03125 e_j.  Along the slots, channel j's 16-slot block then holds that single value, whose
+# block scale is E4M3(1.03125 / 6) = 0.171875 again: V re-quantises to itself.  The query puts
+# score ln(p_j) on slot j (maximum 0, so lse = ln sum Pt), and output channel j is
+# Pt_j * 1.03125 / sum Pt.  Block 0's largest numerator is 1, scale E4M3(1/6) = 0.171875; block
+# 1's is 0.5, scale E4M3(0.5/6 = 0.0833) = 0.0859375 (1.375 x 2^-4, nearer than 1.25 x 2^-4).
+# Pt = E2M1(p / sc) * sc by hand, e.g. 0.75 / 0.171875 = 4.36 -> 4 -> 0.6875.  Exact ties,
+# resolved to the even code: 0.04296875 / 0.171875 = 0.25 -> 0, 0.859375 / 0.171875 = 5 -> 4,
+# 0.30078125 / 0.171875 = 1.75 -> 2, 0.064453125 / 0.0859375 = 0.75 -> 1,
+# 0.21484375 / 0.0859375 = 2.5 -> 2.
+P_BLOCK0 = [1.0, 0.75, 0.5, 0.3, 0.25, 0.2, 0.1, 0.05,
+            0.04296875, 0.6, 0.4, 0.15, 0.12, 0.859375, 0.9, 0.30078125]
+PT_BLOCK0 = [1.03125, 0.6875, 0.515625, 0.2578125, 0.2578125, 0.171875, 0.0859375, 0.0859375,
+             0.0, 0.515625, 0.34375, 0.171875, 0.0859375, 0.6875, 1.03125, 0.34375]
+P_BLOCK1 = [0.5, 0.45, 0.3, 0.2, 0.1, 0.07, 0.04, 0.02,
+            0.064453125, 0.25, 0.15, 0.06, 0.03, 0.21484375, 0.38, 0.12]
+PT_BLOCK1 = [0.515625, 0.515625, 0.2578125, 0.171875, 0.0859375, 0.0859375, 0.04296875, 0.0,
+             0.0859375, 0.2578125, 0.12890625, 0.04296875, 0.04296875, 0.171875, 0.34375,
+             0.12890625]
+
+
+def test_numerators_requantised_per_block_worked_example():
+    n = 32
+    x = np.zeros((n, 512), dtype=np.float32)
+    x[np.arange(n), np.arange(n)] = 1.0
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    codes, sf = oracle.kv_quant_fp4(bits)
+    kv = oracle.kv_dequant_fp4(codes, sf)
+    assert np.array_equal(kv, 1.03125 * np.eye(n, 512))
+    p = np.array(P_BLOCK0 + P_BLOCK1)
+    q = np.zeros((1, 512))
+    q[0, :n] = np.log(p) / 1.03125
+    out, lse = oracle.attn_fp4pv(q, codes, sf, np.arange(n, dtype=np.int32), 1.0)
+    pt = np.array(PT_BLOCK0 + PT_BLOCK1)
+    total = pt.sum()
+    assert np.allclose(out[0, :n], pt * 1.03125 / total, rtol=1e-12, atol=0)
+    assert not out[0, n:].any()
+    assert abs(lse[0] - math.log(total)) < 1e-12
