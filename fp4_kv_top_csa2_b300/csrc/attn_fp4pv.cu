@@ -77,7 +77,9 @@ __device__ __forceinline__ __half2 fp4_scale_f16x2(__half2 amax) {
   const __half2 q0 = __hmul2(amax, r6);
   const __half2 q = __hfma2(__hneg2(__hfma2(q0, six, __hneg2(amax))), r6, q0);
   uint16_t e;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e) : "r"(*reinterpret_cast<const uint32_t *>(&q)));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;"
+      : "=h"(e)
+      : "r"(*reinterpret_cast<const uint32_t *>(&q)));
   const uint32_t h = e4m3x2_to_f16x2(e);
   return *reinterpret_cast<const __half2 *>(&h);
 }
@@ -308,7 +310,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
             const float r0 = __shfl_sync(0xffffffffu, rcp_mine, src);
             const float r1 = __shfl_sync(0xffffffffu, rcp_mine, src + 1);
             // Pt = E2M1(p / sc) * sc, exact in fp16 (at most 6 significant bits)
-            const uint32_t lv = e2m1_round_f16x2(fp4_quot(p[i], sc0, r0), fp4_quot(p[i + 1], sc1, r1));
+            const uint32_t lv =
+                e2m1_round_f16x2(fp4_quot(p[i], sc0, r0), fp4_quot(p[i + 1], sc1, r1));
             const __half2 sc2 = __floats2half2_rn(sc0, sc1);  // exact: E4M3 values
             const __half2 pt = __hmul2(*reinterpret_cast<const __half2 *>(&lv), sc2);
             const float2 ptf = __half22float2(pt);
@@ -342,7 +345,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_fp4pv_kernel(
 #pragma unroll 4
           for (int rr = 0; rr < 16; ++rr) {
             const int j = 16 * b + rr;
-            const uint4 v = *reinterpret_cast<const uint4 *>(chunk + j * 128 + ((u ^ (j & 7)) << 4));
+            const uint4 v =
+                *reinterpret_cast<const uint4 *>(chunk + j * 128 + ((u ^ (j & 7)) << 4));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
